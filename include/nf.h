@@ -1,0 +1,207 @@
+/*
+ * nf.h -- C ABI of the GB300 (sm_103a) inner-persistent row-normalization
+ * library (libnf.so).
+ *
+ * What the library computes, and where the operations come from:
+ *   - Fused residual add + RMSNorm forward, in place: the RMSNormAdd
+ *     benchmark with in-place update semantics in "optimize inner persistent
+ *     scheduler for static fusion" (NVIDIA/Fuser PR #5281), changes
+ *     walkthrough, test_rmsnorm_add_fwd.py entry.
+ *   - RMSNorm forward and LayerNorm forward: "TMA inner persistent
+ *     scheduler" (NVIDIA/Fuser PR #5587), description ("RMS norm and layer
+ *     norm implementations with workspace support").
+ *   - LayerNorm backward as a combined per-row (inner) and across-rows
+ *     (outer) reduction: "Llu/ln bwd" (NVIDIA/Fuser PR #207), title and the
+ *     discussion of "grid-parallel inner-and-outer normalization (special
+ *     case for layernorm backward)".
+ * The pages name the operations but print no formulas; each function below
+ * states the textbook definition it implements.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.   Activations are row-major, contiguous [rows, hidden] arrays of
+ *           bf16 (IEEE binary32 with the low 16 mantissa bits dropped),
+ *           row stride = hidden.  Weight, gamma and beta are [hidden] bf16.
+ *           mean/rstd are [rows] fp32; dgamma/dbeta are [hidden] fp32.
+ * Pointers. Every data pointer is a DEVICE pointer on the current CUDA
+ *           device (or managed memory).  bf16 pointers, dgamma, dbeta and
+ *           the workspace must be 16-byte aligned; mean/rstd 4-byte
+ *           aligned.  Null pointers are accepted only when rows == 0.
+ * hidden.   Must be one of the compiled sizes: 1024, 2048, 4096, 5120,
+ *           8192, 12288 (kernels are specialized per size; other values
+ *           return NF_ERR_UNSUPPORTED_HIDDEN).
+ * rows.     Any value >= 0; rows == 0 returns NF_OK without launching.
+ * eps.      Finite and > 0.
+ * Stream.   Work is enqueued on `stream` (NULL = the legacy default
+ *           stream) and the call returns without synchronizing.
+ * Ownership.The caller owns every buffer; the library allocates no device
+ *           memory.  It caches, per device, the SM count and the address
+ *           of its device status word.
+ * Errors.   Argument checks happen before any launch and return a status;
+ *           a failed launch returns NF_ERR_CUDA.  Nothing is thrown across
+ *           the ABI.  A kernel that gives up on a bounded wait records
+ *           NF_ERR_TIMEOUT in the device status word (read it with
+ *           nf_get_device_status) and returns without trapping.
+ * Aliasing. Outputs may not partially overlap inputs or each other; the
+ *           only aliasing allowed is stated per function.
+ * Results.  Accumulation is fp32; results are bit-identical from run to
+ *           run on the same device (every reduction has a fixed order).
+ */
+#ifndef NF_H_
+#define NF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NF_OK = 0,
+    NF_ERR_INVALID_ARG = 1,         /* null pointer, rows < 0, bad eps, bad overlap */
+    NF_ERR_UNSUPPORTED_HIDDEN = 2,  /* hidden not in the compiled set */
+    NF_ERR_MISALIGNED = 3,          /* pointer alignment rule broken */
+    NF_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the queried size */
+    NF_ERR_CUDA = 5,                /* a CUDA runtime call or launch failed */
+    NF_ERR_TIMEOUT = 6,             /* a kernel gave up on a bounded wait */
+    NF_ERR_UNSUPPORTED_PATH = 7     /* forced path not built for this op/size */
+} nf_status;
+
+/* = cudaStream_t.  NULL is the legacy default stream. */
+typedef struct CUstream_st* nf_stream;
+
+/* Kernel families.  NF_PATH_AUTO lets the library choose from rows, hidden
+ * and the SM count; the others force one family (for tests and ablations).
+ *   REG     -- row resident in registers, 128-bit loads, one row per group
+ *              of threads ("optimize inner persistent scheduler for static
+ *              fusion": static hidden size, warp-multiple block size).
+ *   CLUSTER -- one row split across a thread-block cluster, partial sums
+ *              exchanged through distributed shared memory (the small-batch
+ *              case of the same page: use more SMs when rows are few).
+ *   BULK    -- a producer warp stages rows into a shared-memory ring with
+ *              bulk asynchronous copies; consumer warps read 128-bit vectors
+ *              from shared memory; registers move from producer to
+ *              consumers ("TMA inner persistent scheduler").               */
+typedef enum {
+    NF_PATH_AUTO = 0,
+    NF_PATH_REG = 1,
+    NF_PATH_CLUSTER = 2,
+    NF_PATH_BULK = 3
+} nf_path;
+
+/* Operation ids for nf_plan_query. */
+typedef enum {
+    NF_OP_FUSED_ADD_RMSNORM = 0,
+    NF_OP_RMSNORM_FWD = 1,
+    NF_OP_LAYERNORM_FWD = 2,
+    NF_OP_LAYERNORM_BWD = 3,
+    NF_OP_RMSNORM_BWD = 4
+} nf_op;
+
+/* A launch plan, as chosen for (op, rows, hidden) on the current device. */
+typedef struct {
+    int32_t path;            /* nf_path actually used (never AUTO) */
+    int32_t grid;            /* CTAs in the main launch */
+    int32_t block;           /* threads per CTA */
+    int32_t cluster;         /* CTAs per cluster (1 = none) */
+    int32_t rows_per_cta;    /* rows a CTA handles at once */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t launches;        /* kernel launches per call */
+    int32_t partials;        /* column-partial slots (backward ops), else 0 */
+} nf_plan;
+
+/* Fused residual add + RMSNorm forward, in place.  For each row r:
+ *     s_j          = x[r][j] + residual[r][j]          (fp32)
+ *     residual[r][j] <- bf16(s_j)
+ *     x[r][j]       <- bf16( s_j * rsqrt(mean_k(s_k^2) + eps) * weight[j] )
+ * The normalization reads the unrounded fp32 sum s.  x and residual are
+ * both read and written; they must not overlap each other, and weight must
+ * not overlap either. */
+nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight,
+                               int64_t rows, int64_t hidden, float eps, nf_stream stream);
+
+/* RMSNorm forward:  y[r][j] = bf16( x[r][j] * rsqrt(mean_k(x[r][k]^2) + eps) * weight[j] ).
+ * y may be x itself (in place); any other overlap is rejected. */
+nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight,
+                         int64_t rows, int64_t hidden, float eps, nf_stream stream);
+
+/* LayerNorm forward with biased variance:
+ *     mean[r] = (1/H) sum_j x[r][j]
+ *     var     = (1/H) sum_j (x[r][j] - mean[r])^2        (two passes over the resident row)
+ *     rstd[r] = rsqrt(var + eps)
+ *     y[r][j] = bf16( (x[r][j] - mean[r]) * rstd[r] * gamma[j] + beta[j] )
+ * mean and rstd (fp32, [rows]) are the values a backward pass needs; either
+ * may be NULL to skip it.  y may be x itself. */
+nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x,
+                           const void* gamma, const void* beta,
+                           int64_t rows, int64_t hidden, float eps, nf_stream stream);
+
+/* Bytes of workspace nf_layernorm_bwd needs for (rows, hidden) on the
+ * current device (0 when rows == 0 or hidden is unsupported).  The value
+ * depends on the device's SM count, so query it on the device that runs
+ * the call.  Returns 0 also if the device cannot be queried. */
+size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden);
+
+/* LayerNorm backward.  With xhat = (x - mean) * rstd and g = dy * gamma:
+ *   inner (per row):   dx[r][j] = bf16( rstd[r] * ( g_j - mean_k(g_k) - xhat_j * mean_k(g_k * xhat_k) ) )
+ *   outer (per column): dgamma[j] = sum_r dy[r][j] * xhat[r][j],  dbeta[j] = sum_r dy[r][j]
+ * mean/rstd are the forward's saved values (eps is folded into rstd, so
+ * none is passed).  dgamma/dbeta are overwritten, not accumulated.  The
+ * column sums go through `workspace` in two stages -- per-CTA partials,
+ * then a fixed-order sum -- so they are deterministic.  workspace is a
+ * caller-owned device buffer, 16-byte aligned, of at least
+ * nf_layernorm_bwd_workspace_size(rows, hidden) bytes; its contents on
+ * entry do not matter.  dx may be dy or x itself (exact alias).  With
+ * rows == 0 nothing is read and dgamma/dbeta, where not NULL, are set to 0
+ * (an empty column sum). */
+nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta,
+                           const void* dy, const void* x, const float* mean, const float* rstd,
+                           const void* gamma, int64_t rows, int64_t hidden,
+                           void* workspace, size_t workspace_bytes, nf_stream stream);
+
+/* Force a kernel family for every later call in this process (NF_PATH_AUTO
+ * restores the library's choice).  A call whose op/size has no kernel of the
+ * forced family returns NF_ERR_UNSUPPORTED_PATH.  Not thread-safe with
+ * respect to calls in flight on other host threads; meant for tests and
+ * ablations. */
+nf_status nf_set_path(nf_path path);
+
+/* The plan a call of `op` with (rows, hidden) would use now on the current
+ * device, without launching anything. */
+nf_status nf_plan_query(nf_op op, int64_t rows, int64_t hidden, nf_plan* out);
+
+/* Pure host planning, no CUDA call: the plan for (op, rows, hidden) on a
+ * device with `sm_count` SMs under the kernel-family choice `path`
+ * (NF_PATH_AUTO = the library's own rule).  nf_plan_query and every entry
+ * point use exactly this function with the device's SM count and the
+ * nf_set_path setting.  Returns NF_ERR_UNSUPPORTED_HIDDEN,
+ * NF_ERR_UNSUPPORTED_PATH or NF_ERR_INVALID_ARG (rows < 0, sm_count < 1,
+ * unknown op or path, out == NULL) without touching *out. */
+nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_count,
+                          nf_path path, nf_plan* out);
+
+/* Copy the device status word of the current device to the host after the
+ * work queued on `stream` finishes (this synchronizes `stream`), reset it to
+ * NF_OK, and return the copied value (NF_OK or NF_ERR_TIMEOUT), or
+ * NF_ERR_CUDA if the copy itself fails. */
+nf_status nf_get_device_status(nf_stream stream);
+
+/* Test hook for the bounded-wait machinery: launch one CTA that waits on a
+ * shared-memory barrier which nothing completes, giving up after
+ * `timeout_ns` nanoseconds (clamped to [1e3, 1e9]).  The kernel records
+ * NF_ERR_TIMEOUT in the device status word and returns normally; the
+ * context stays usable. */
+nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nf_status_string(nf_status status);
+
+/* Library version string (static). */
+const char* nf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF_H_ */

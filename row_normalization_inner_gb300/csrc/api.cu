@@ -1,0 +1,383 @@
+// C ABI of libnf.so: argument validation, planning and dispatch.
+//
+// Every entry point validates all arguments before it touches the GPU,
+// chooses a plan with nf_plan_compute (pure host code) and launches on the
+// caller's stream.  The scheduler lessons of "TMA inner persistent
+// scheduler" (NVIDIA/Fuser PR #5587, reviewer guide: a missing null check,
+// an unchecked cast, a possible divide by zero) apply here as: check every
+// pointer, never divide by a derived count that could be zero, and return a
+// status instead of crashing.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/nf.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace nf {
+
+// The device status word: kernels that give up on a bounded wait record
+// their error code here (first one wins).
+__device__ int g_device_status = 0;
+
+bool reg_shape(int64_t hidden, int* tpr, int* rpc) {
+    switch (hidden) {
+        case 1024:  *tpr = RegShape<1024>::TPR;  *rpc = RegShape<1024>::RPC;  return true;
+        case 2048:  *tpr = RegShape<2048>::TPR;  *rpc = RegShape<2048>::RPC;  return true;
+        case 4096:  *tpr = RegShape<4096>::TPR;  *rpc = RegShape<4096>::RPC;  return true;
+        case 5120:  *tpr = RegShape<5120>::TPR;  *rpc = RegShape<5120>::RPC;  return true;
+        case 8192:  *tpr = RegShape<8192>::TPR;  *rpc = RegShape<8192>::RPC;  return true;
+        case 12288: *tpr = RegShape<12288>::TPR; *rpc = RegShape<12288>::RPC; return true;
+        default: return false;
+    }
+}
+
+namespace {
+
+// Resident stage-1 CTAs per SM for the LayerNorm backward register path.
+// The stage-1 grid is SMs x this, so the row-to-partial assignment (and
+// therefore the bit pattern of dgamma/dbeta) depends only on the device.
+int bwd_ctas_per_sm(int64_t hidden) {
+    // The stage-1 kernels keep gamma, the row and 2 x 32 column
+    // accumulators per thread in registers (~170-185 registers), so one
+    // CTA fits per SM at every compiled size.
+    (void)hidden;
+    return 1;
+}
+
+// Automatic choice between the register and the cluster forward paths: a
+// row goes to a cluster when one-CTA-per-row-group would occupy fewer than
+// half of the SMs.
+bool prefer_cluster(int64_t rows, int rpc, int sms) {
+    const int64_t ctas = (rows + rpc - 1) / rpc;
+    return ctas * 2 < sms;
+}
+
+std::atomic<int> g_forced_path{NF_PATH_AUTO};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int*> g_status_addr[kMaxDevices];
+
+nf_status current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return NF_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return NF_ERR_CUDA;
+    return NF_OK;
+}
+
+nf_status device_sm_count(int* sms) {
+    int dev;
+    if (nf_status st = current_device(&dev)) return st;
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return NF_ERR_CUDA;
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+    }
+    *sms = v;
+    return NF_OK;
+}
+
+nf_status device_status_addr(int** addr) {
+    int dev;
+    if (nf_status st = current_device(&dev)) return st;
+    int* p = g_status_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_device_status) != cudaSuccess || !q) return NF_ERR_CUDA;
+        p = static_cast<int*>(q);
+        g_status_addr[dev].store(p, std::memory_order_release);
+    }
+    *addr = p;
+    return NF_OK;
+}
+
+bool hidden_ok(int64_t h) {
+    int a, b;
+    return reg_shape(h, &a, &b);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Span {
+    const void* p;
+    int64_t bytes;
+};
+
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.bytes <= 0 || b.bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + static_cast<uintptr_t>(b.bytes) && b0 < a0 + static_cast<uintptr_t>(a.bytes);
+}
+
+// Overlap allowed only as the exact same buffer.
+bool bad_overlap_except_alias(Span out, Span in) {
+    if (out.p == in.p && out.bytes == in.bytes) return false;
+    return overlap(out, in);
+}
+
+nf_status common_checks(int64_t rows, int64_t hidden, float eps, bool check_eps) {
+    if (!hidden_ok(hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
+    if (rows < 0) return NF_ERR_INVALID_ARG;
+    // keep rows * hidden * 4 bytes representable
+    if (rows > (INT64_MAX / 8) / hidden) return NF_ERR_INVALID_ARG;
+    if (check_eps && !(std::isfinite(eps) && eps > 0.f)) return NF_ERR_INVALID_ARG;
+    return NF_OK;
+}
+
+nf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NF_OK : NF_ERR_CUDA; }
+
+nf_status plan_for_call(nf_op op, int64_t rows, int64_t hidden, nf_plan* plan) {
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    return nf_plan_compute(op, rows, hidden, sms,
+                           static_cast<nf_path>(g_forced_path.load(std::memory_order_relaxed)), plan);
+}
+
+// The selftest kernel: one thread waits on a barrier nothing will complete.
+__global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait(&bar, 0, timeout_ns)) record_status(status, kStatusTimeout);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace nf
+
+using namespace nf;
+
+extern "C" {
+
+nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_count, nf_path path,
+                          nf_plan* out) {
+    if (!out || rows < 0 || sm_count < 1) return NF_ERR_INVALID_ARG;
+    if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_BULK) return NF_ERR_INVALID_ARG;
+    int tpr, rpc;
+    if (!reg_shape(hidden, &tpr, &rpc)) return NF_ERR_UNSUPPORTED_HIDDEN;
+    const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
+                     op == NF_OP_LAYERNORM_FWD;
+    if (op == NF_OP_RMSNORM_BWD) return NF_ERR_UNSUPPORTED_PATH;  // no kernel yet
+
+    nf_path p = path;
+    if (p == NF_PATH_AUTO) p = (fwd && prefer_cluster(rows, rpc, sm_count)) ? NF_PATH_CLUSTER : NF_PATH_REG;
+    if (p == NF_PATH_BULK) return NF_ERR_UNSUPPORTED_PATH;
+    if (p == NF_PATH_CLUSTER && !fwd) return NF_ERR_UNSUPPORTED_PATH;
+
+    nf_plan pl;
+    std::memset(&pl, 0, sizeof pl);
+    pl.path = p;
+    constexpr int64_t kMaxGrid = 0x7FFFFFFF;
+    if (p == NF_PATH_REG && fwd) {
+        const int64_t blocks = (rows + rpc - 1) / rpc;
+        pl.grid = static_cast<int32_t>(blocks < kMaxGrid ? blocks : kMaxGrid);
+        pl.block = tpr * rpc;
+        pl.cluster = 1;
+        pl.rows_per_cta = rpc;
+        pl.launches = 1;
+    } else if (p == NF_PATH_CLUSTER) {
+        int c, t;
+        if (!cluster_shape(hidden, &c, &t)) return NF_ERR_UNSUPPORTED_HIDDEN;
+        const int64_t max_clusters = kMaxGrid / c;
+        const int64_t clusters = rows < max_clusters ? rows : max_clusters;
+        pl.grid = static_cast<int32_t>(clusters * c);
+        pl.block = t;
+        pl.cluster = c;
+        pl.rows_per_cta = 1;
+        pl.launches = 1;
+    } else {  // register-path backward: persistent stage 1 + column reduce
+        const int64_t blocks = (rows + rpc - 1) / rpc;
+        const int64_t resident = static_cast<int64_t>(sm_count) * bwd_ctas_per_sm(hidden);
+        int64_t g = blocks < resident ? blocks : resident;
+        if (g < 1) g = 1;
+        pl.grid = static_cast<int32_t>(g);
+        pl.block = tpr * rpc;
+        pl.cluster = 1;
+        pl.rows_per_cta = rpc;
+        pl.launches = 2;
+        pl.partials = static_cast<int32_t>(g * rpc);
+    }
+    *out = pl;
+    return NF_OK;
+}
+
+nf_status nf_set_path(nf_path path) {
+    if (path < NF_PATH_AUTO || path > NF_PATH_BULK) return NF_ERR_INVALID_ARG;
+    g_forced_path.store(path, std::memory_order_relaxed);
+    return NF_OK;
+}
+
+nf_status nf_plan_query(nf_op op, int64_t rows, int64_t hidden, nf_plan* out) {
+    if (!out) return NF_ERR_INVALID_ARG;
+    if (!hidden_ok(hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
+    if (rows < 0) return NF_ERR_INVALID_ARG;
+    return plan_for_call(op, rows, hidden, out);
+}
+
+nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int64_t rows,
+                               int64_t hidden, float eps, nf_stream stream) {
+    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (rows == 0) return NF_OK;
+    if (!x || !residual || !weight) return NF_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16)) return NF_ERR_MISALIGNED;
+    const int64_t act = rows * hidden * 2, par = hidden * 2;
+    if (overlap({x, act}, {residual, act}) || overlap({x, act}, {weight, par}) ||
+        overlap({residual, act}, {weight, par}))
+        return NF_ERR_INVALID_ARG;
+    nf_plan pl;
+    if (nf_status st = plan_for_call(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, &pl)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_CLUSTER)
+        return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
+    return from_cuda(launch_fused_reg(hidden, x, residual, weight, rows, eps, pl.grid, s));
+}
+
+nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t rows, int64_t hidden,
+                         float eps, nf_stream stream) {
+    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (rows == 0) return NF_OK;
+    if (!y || !x || !weight) return NF_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(x, 16) || !aligned(weight, 16)) return NF_ERR_MISALIGNED;
+    const int64_t act = rows * hidden * 2, par = hidden * 2;
+    if (bad_overlap_except_alias({y, act}, {x, act}) || overlap({y, act}, {weight, par}))
+        return NF_ERR_INVALID_ARG;
+    nf_plan pl;
+    if (nf_status st = plan_for_call(NF_OP_RMSNORM_FWD, rows, hidden, &pl)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_CLUSTER)
+        return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
+    return from_cuda(launch_rms_reg(hidden, y, x, weight, rows, eps, pl.grid, s));
+}
+
+nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                           const void* beta, int64_t rows, int64_t hidden, float eps,
+                           nf_stream stream) {
+    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (rows == 0) return NF_OK;
+    if (!y || !x || !gamma || !beta) return NF_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16))
+        return NF_ERR_MISALIGNED;
+    if (!aligned(mean, 4) || !aligned(rstd, 4)) return NF_ERR_MISALIGNED;
+    const int64_t act = rows * hidden * 2, par = hidden * 2, stat = rows * 4;
+    if (bad_overlap_except_alias({y, act}, {x, act}) || overlap({y, act}, {gamma, par}) ||
+        overlap({y, act}, {beta, par}) || overlap({mean, stat}, {rstd, stat}))
+        return NF_ERR_INVALID_ARG;
+    for (Span o : {Span{mean, stat}, Span{rstd, stat}})
+        if (overlap(o, {y, act}) || overlap(o, {x, act}) || overlap(o, {gamma, par}) ||
+            overlap(o, {beta, par}))
+            return NF_ERR_INVALID_ARG;
+    nf_plan pl;
+    if (nf_status st = plan_for_call(NF_OP_LAYERNORM_FWD, rows, hidden, &pl)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_CLUSTER)
+        return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
+                                               pl.grid, s));
+    return from_cuda(launch_ln_fwd_reg(hidden, y, mean, rstd, x, gamma, beta, rows, eps, pl.grid, s));
+}
+
+size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
+    if (!hidden_ok(hidden) || rows <= 0) return 0;
+    nf_plan pl;
+    if (plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl) != NF_OK) return 0;
+    return static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+}
+
+nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                           const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                           int64_t hidden, void* workspace, size_t workspace_bytes,
+                           nf_stream stream) {
+    if (nf_status st = common_checks(rows, hidden, 0.f, false)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {
+        // an empty sum: dgamma = dbeta = 0
+        if (dgamma && !aligned(dgamma, 16)) return NF_ERR_MISALIGNED;
+        if (dbeta && !aligned(dbeta, 16)) return NF_ERR_MISALIGNED;
+        if (dgamma && cudaMemsetAsync(dgamma, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
+        if (dbeta && cudaMemsetAsync(dbeta, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
+        return NF_OK;
+    }
+    if (!dx || !dgamma || !dbeta || !dy || !x || !mean || !rstd || !gamma || !workspace)
+        return NF_ERR_INVALID_ARG;
+    if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(x, 16) || !aligned(gamma, 16) ||
+        !aligned(workspace, 16) || !aligned(dgamma, 16) || !aligned(dbeta, 16) ||
+        !aligned(mean, 4) || !aligned(rstd, 4))
+        return NF_ERR_MISALIGNED;
+    nf_plan pl;
+    if (nf_status st = plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
+    const size_t need = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t act = rows * hidden * 2, par = hidden * 2, stat = rows * 4, grad = hidden * 4;
+    const Span sdx{dx, act}, sdg{dgamma, grad}, sdb{dbeta, grad}, sws{workspace, static_cast<int64_t>(need)};
+    const Span ins[] = {{dy, act}, {x, act}, {mean, stat}, {rstd, stat}, {gamma, par}};
+    if (overlap(sdg, sdb) || overlap(sdx, sdg) || overlap(sdx, sdb) || overlap(sws, sdx) ||
+        overlap(sws, sdg) || overlap(sws, sdb))
+        return NF_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i) {
+        const Span& in = ins[i];
+        // dx may be exactly dy or x (each row is read before it is written)
+        const bool dx_clash = i < 2 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
+        if (dx_clash || overlap(sdg, in) || overlap(sdb, in) || overlap(sws, in))
+            return NF_ERR_INVALID_ARG;
+    }
+    float* ws = static_cast<float*>(workspace);
+    if (cudaError_t e = launch_ln_bwd_reg(hidden, dx, ws, dy, x, mean, rstd, gamma, rows, pl.grid, s))
+        return from_cuda(e);
+    return from_cuda(launch_column_reduce(ws, dgamma, dbeta, pl.partials, hidden, s));
+}
+
+nf_status nf_get_device_status(nf_stream stream) {
+    int* addr;
+    if (nf_status st = device_status_addr(&addr)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, addr, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NF_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return NF_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemsetAsync(addr, 0, sizeof(int), s) != cudaSuccess) return NF_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return NF_ERR_CUDA;
+    }
+    return static_cast<nf_status>(v);
+}
+
+nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream) {
+    int* addr;
+    if (nf_status st = device_status_addr(&addr)) return st;
+    if (timeout_ns < 1000) timeout_ns = 1000;
+    if (timeout_ns > 1000000000) timeout_ns = 1000000000;
+    return from_cuda(launch_wait_selftest(addr, static_cast<uint64_t>(timeout_ns),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* nf_status_string(nf_status status) {
+    switch (status) {
+        case NF_OK: return "NF_OK";
+        case NF_ERR_INVALID_ARG: return "NF_ERR_INVALID_ARG";
+        case NF_ERR_UNSUPPORTED_HIDDEN: return "NF_ERR_UNSUPPORTED_HIDDEN";
+        case NF_ERR_MISALIGNED: return "NF_ERR_MISALIGNED";
+        case NF_ERR_WORKSPACE_TOO_SMALL: return "NF_ERR_WORKSPACE_TOO_SMALL";
+        case NF_ERR_CUDA: return "NF_ERR_CUDA";
+        case NF_ERR_TIMEOUT: return "NF_ERR_TIMEOUT";
+        case NF_ERR_UNSUPPORTED_PATH: return "NF_ERR_UNSUPPORTED_PATH";
+        default: return "NF_ERR_UNKNOWN";
+    }
+}
+
+const char* nf_version(void) { return "nf 0.1 (sm_103a)"; }
+
+}  // extern "C"

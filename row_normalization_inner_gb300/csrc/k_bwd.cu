@@ -1,0 +1,183 @@
+// LayerNorm backward: the combined inner + outer reduction ("Llu/ln bwd",
+// NVIDIA/Fuser PR #207: "grid-parallel inner-and-outer normalization
+// (special case for layernorm backward)"), with the cross-CTA partials kept
+// in a workspace ("TMA inner persistent scheduler": "with workspace
+// support").
+//
+// Stage 1 (register path): `grid` persistent CTAs of RPC row groups.  Row
+// group `slot` owns the contiguous row stripe
+//     [rows * slot / nslots, rows * (slot + 1) / nslots),  nslots = grid * RPC,
+// so which rows feed which partial depends only on (rows, nslots).  For each
+// row it computes, with xhat = (x - mean) * rstd and g = dy * gamma,
+//     inner:  A = sum_j g_j / H,  B = sum_j g_j xhat_j / H  (one row reduction of 2 values)
+//             dx_j = rstd * (g_j - A - xhat_j * B)
+//     outer:  acc_gamma_j += dy_j * xhat_j,  acc_beta_j += dy_j  (per-thread registers)
+// and at the end writes its column partials to ws[slot][0][:], ws[slot][1][:].
+// Stage 2 sums the nslots partials of every column in slot order, so dgamma
+// and dbeta are bit-identical from run to run.
+#include "common.cuh"
+#include "launch.h"
+
+namespace nf {
+namespace {
+
+template <int H>
+struct BGeo {
+    static constexpr int TPR = RegShape<H>::TPR;
+    static constexpr int RPC = RegShape<H>::RPC;
+    static constexpr int NV = H / kVec;
+    static constexpr int VPT = NV / TPR;
+    static constexpr int W = TPR / 32;
+    static_assert(NV % TPR == 0 && TPR % 32 == 0, "static row split");
+};
+
+template <int H>
+__global__ void __launch_bounds__(BGeo<H>::TPR * BGeo<H>::RPC)
+layernorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const uint16_t* x,
+                  const float* __restrict__ mean, const float* __restrict__ rstd,
+                  const uint16_t* __restrict__ gamma, int64_t rows) {
+    using G = BGeo<H>;
+    __shared__ float red[2][G::RPC * G::W * 2];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    const int64_t nslots = static_cast<int64_t>(gridDim.x) * G::RPC;
+    const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::RPC + group;
+    const int64_t r0 = rows * slot / nslots;
+    const int64_t r1 = rows * (slot + 1) / nslots;
+    const int64_t maxlen = (rows + nslots - 1) / nslots;  // >= every stripe's length
+
+    uint4 gm[G::VPT];
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k) gm[k] = ld_param(gamma + (k * G::TPR + t) * kVec);
+    float acc_g[G::VPT][8], acc_b[G::VPT][8];
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { acc_g[k][e] = 0.f; acc_b[k][e] = 0.f; }
+
+    for (int64_t it = 0; it < maxlen; ++it) {
+        const int64_t r = r0 + it;
+        const bool active = r < r1;
+        uint4 xv[G::VPT], dv[G::VPT];
+        float mu = 0.f, rs = 0.f;
+        float v[2] = {0.f, 0.f};
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int vi = k * G::TPR + t;
+                xv[k] = ld_stream(x + r * H + vi * kVec);
+                dv[k] = ld_stream(dy + r * H + vi * kVec);
+            }
+            mu = __ldg(mean + r);
+            rs = __ldg(rstd + r);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], gf[8];
+                unpack8(xv[k], xf);
+                unpack8(dv[k], df);
+                unpack8(gm[k], gf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xh = (xf[e] - mu) * rs;
+                    const float g = df[e] * gf[e];
+                    v[0] += g;
+                    v[1] += g * xh;
+                    acc_g[k][e] += df[e] * xh;
+                    acc_b[k][e] += df[e];
+                }
+            }
+        }
+        group_sum<G::TPR, 2>(v, red[it & 1], group, t);
+        if (active) {
+            const float A = v[0] * (1.0f / H);
+            const float B = v[1] * (1.0f / H);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], gf[8], o[8];
+                unpack8(xv[k], xf);
+                unpack8(dv[k], df);
+                unpack8(gm[k], gf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float xh = (xf[e] - mu) * rs;
+                    o[e] = rs * (df[e] * gf[e] - A - xh * B);
+                }
+                st_stream(dx + r * H + (k * G::TPR + t) * kVec, pack8(o));
+            }
+        }
+    }
+
+    float* wg = ws + slot * 2 * H;
+    float* wb = wg + H;
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k) {
+        const int j = (k * G::TPR + t) * kVec;
+        float4* pg = reinterpret_cast<float4*>(wg + j);
+        float4* pb = reinterpret_cast<float4*>(wb + j);
+        pg[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
+        pg[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+        pb[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
+        pb[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
+    }
+}
+
+// dgamma[j] = sum_{slot} ws[slot][0][j], dbeta[j] = sum_{slot} ws[slot][1][j],
+// in a fixed order: thread row ty sums slots ty, ty+8, ty+16, ... and the 8
+// row sums are then added in ty order.  Each thread owns 4 adjacent columns
+// of the [2][H] plane (float4 loads, coalesced across the warp).
+constexpr int kColThreadsX = 32, kColThreadsY = 8;
+
+__global__ void __launch_bounds__(kColThreadsX * kColThreadsY)
+column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
+              float* __restrict__ dbeta, int nslots, int hidden) {
+    __shared__ float4 part[kColThreadsY][kColThreadsX];
+    const int tx = threadIdx.x % kColThreadsX, ty = threadIdx.x / kColThreadsX;
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColThreadsX + tx;  // float4 index in [2][H]
+    const bool ok = c4 * 4 < 2 * static_cast<int64_t>(hidden);
+    const int which = ok ? static_cast<int>((c4 * 4) / hidden) : 0;
+    const int64_t j = ok ? (c4 * 4) % hidden : 0;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) {
+#pragma unroll 4
+        for (int p = ty; p < nslots; p += kColThreadsY) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(
+                ws + (static_cast<int64_t>(p) * 2 + which) * hidden + j));
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+    }
+    part[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && ok) {
+        float4 tot = part[0][tx];
+#pragma unroll
+        for (int y = 1; y < kColThreadsY; ++y) {
+            const float4 v = part[y][tx];
+            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+        }
+        float* out = (which == 0 ? dgamma : dbeta) + j;
+        *reinterpret_cast<float4*>(out) = tot;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                              const float* mean, const float* rstd, const void* gamma,
+                              int64_t rows, int grid, cudaStream_t st) {
+    NF_HIDDEN_SWITCH(hidden, {
+        layernorm_bwd_reg<H><<<grid, BGeo<H>::TPR * BGeo<H>::RPC, 0, st>>>(
+            static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
+            static_cast<const uint16_t*>(x), mean, rstd, static_cast<const uint16_t*>(gamma), rows);
+        return cudaGetLastError();
+    })
+}
+
+cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
+                                 int64_t hidden, cudaStream_t st) {
+    const int64_t cols4 = 2 * hidden / 4;
+    const int grid = static_cast<int>((cols4 + kColThreadsX - 1) / kColThreadsX);
+    column_reduce<<<grid, kColThreadsX * kColThreadsY, 0, st>>>(ws, dgamma, dbeta, nslots,
+                                                                 static_cast<int>(hidden));
+    return cudaGetLastError();
+}
+
+}  // namespace nf

@@ -1,0 +1,221 @@
+// Register-persistent forward kernels: fused residual add + RMSNorm (in
+// place), RMSNorm forward, LayerNorm forward.
+//
+// One row per group of TPR threads, RPC groups per CTA.  The hidden size is
+// a template constant, so the thread count, the vectors per thread and the
+// loops are all static ("optimize inner persistent scheduler for static
+// fusion", description item 2(1): static bdimx when the hidden size is
+// fixed; bdimx a multiple of the warp size).  Each thread loads its VPT
+// 128-bit vectors once, keeps the row in registers as fp32, and reduces it
+// in the same pass that loads it (the page's compute-with-first-consumer
+// change): sum of squares for RMSNorm; for LayerNorm the sum, then the
+// centered sum of squares over the resident values (two passes, no reload).
+#include "common.cuh"
+#include "launch.h"
+
+namespace nf {
+namespace {
+
+template <int H>
+struct Geo {
+    static constexpr int TPR = RegShape<H>::TPR;
+    static constexpr int RPC = RegShape<H>::RPC;
+    static constexpr int NV = H / kVec;
+    static constexpr int VPT = NV / TPR;
+    static constexpr int W = TPR / 32;
+    static_assert(NV % TPR == 0, "hidden/8 must be a multiple of the row's thread count");
+    static_assert(TPR % 32 == 0, "a row uses whole warps");
+};
+
+// residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
+template <int H>
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
+                      const uint16_t* __restrict__ w, int64_t rows, float eps) {
+    using G = Geo<H>;
+    __shared__ float red[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t row = blk * G::RPC + group;
+        const bool active = row < rows;
+        uint16_t* xr = x + row * H;
+        uint16_t* rr = res + row * H;
+        float s[G::VPT][8];
+        float ss[1] = {0.f};
+        if (active) {
+            uint4 xv[G::VPT], rv[G::VPT];
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int v = k * G::TPR + t;
+                xv[k] = ld_stream(xr + v * kVec);
+                rv[k] = ld_stream(rr + v * kVec);
+            }
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float a[8], b[8];
+                unpack8(xv[k], a);
+                unpack8(rv[k], b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    s[k][e] = a[e] + b[e];
+                    ss[0] += s[k][e] * s[k][e];
+                }
+                st_stream(rr + (k * G::TPR + t) * kVec, pack8(s[k]));
+            }
+        }
+        group_sum<G::TPR, 1>(ss, red, group, t);
+        if (active) {
+            const float rstd = rsqrtf(ss[0] * (1.0f / H) + eps);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int v = k * G::TPR + t;
+                float wf[8], o[8];
+                unpack8(ld_param(w + v * kVec), wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = s[k][e] * rstd * wf[e];
+                st_stream(xr + v * kVec, pack8(o));
+            }
+        }
+        if constexpr (G::W > 1) __syncthreads();  // `red` is reused by the next row block
+    }
+}
+
+// y <- bf16(x * rsqrt(mean(x^2) + eps) * w)
+template <int H>
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
+                int64_t rows, float eps) {
+    using G = Geo<H>;
+    __shared__ float red[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t row = blk * G::RPC + group;
+        const bool active = row < rows;
+        float f[G::VPT][8];
+        float ss[1] = {0.f};
+        if (active) {
+            uint4 xv[G::VPT];
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                unpack8(xv[k], f[k]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss[0] += f[k][e] * f[k][e];
+            }
+        }
+        group_sum<G::TPR, 1>(ss, red, group, t);
+        if (active) {
+            const float rstd = rsqrtf(ss[0] * (1.0f / H) + eps);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int v = k * G::TPR + t;
+                float wf[8], o[8];
+                unpack8(ld_param(w + v * kVec), wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = f[k][e] * rstd * wf[e];
+                st_stream(y + row * H + v * kVec, pack8(o));
+            }
+        }
+        if constexpr (G::W > 1) __syncthreads();
+    }
+}
+
+// mean = sum(x)/H ; var = sum((x-mean)^2)/H ; rstd = rsqrt(var + eps)
+// y <- bf16((x - mean) * rstd * gamma + beta)
+template <int H>
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                  const uint16_t* x, const uint16_t* __restrict__ gamma,
+                  const uint16_t* __restrict__ beta, int64_t rows, float eps) {
+    using G = Geo<H>;
+    __shared__ float red1[G::RPC * G::W];
+    __shared__ float red2[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t row = blk * G::RPC + group;
+        const bool active = row < rows;
+        float f[G::VPT][8];
+        float acc[1] = {0.f};
+        if (active) {
+            uint4 xv[G::VPT];
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                unpack8(xv[k], f[k]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[0] += f[k][e];
+            }
+        }
+        group_sum<G::TPR, 1>(acc, red1, group, t);
+        const float mean = acc[0] * (1.0f / H);
+        float sq[1] = {0.f};
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = f[k][e] - mean;
+                    sq[0] += d * d;
+                }
+        }
+        group_sum<G::TPR, 1>(sq, red2, group, t);
+        if (active) {
+            const float rstd = rsqrtf(sq[0] * (1.0f / H) + eps);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int v = k * G::TPR + t;
+                float gf[8], bf[8], o[8];
+                unpack8(ld_param(gamma + v * kVec), gf);
+                unpack8(ld_param(beta + v * kVec), bf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = (f[k][e] - mean) * rstd * gf[e] + bf[e];
+                st_stream(y + row * H + v * kVec, pack8(o));
+            }
+            if (t == 0) {
+                if (mean_out) mean_out[row] = mean;
+                if (rstd_out) rstd_out[row] = rstd;
+            }
+        }
+        if constexpr (G::W > 1) __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
+                             float eps, int grid, cudaStream_t st) {
+    NF_HIDDEN_SWITCH(hidden, {
+        fused_add_rmsnorm_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
+            static_cast<uint16_t*>(x), static_cast<uint16_t*>(res),
+            static_cast<const uint16_t*>(w), rows, eps);
+        return cudaGetLastError();
+    })
+}
+
+cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
+                           float eps, int grid, cudaStream_t st) {
+    NF_HIDDEN_SWITCH(hidden, {
+        rmsnorm_fwd_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
+            static_cast<uint16_t*>(y), static_cast<const uint16_t*>(x),
+            static_cast<const uint16_t*>(w), rows, eps);
+        return cudaGetLastError();
+    })
+}
+
+cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
+                              const void* gamma, const void* beta, int64_t rows, float eps,
+                              int grid, cudaStream_t st) {
+    NF_HIDDEN_SWITCH(hidden, {
+        layernorm_fwd_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
+            static_cast<uint16_t*>(y), mean, rstd, static_cast<const uint16_t*>(x),
+            static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta), rows, eps);
+        return cudaGetLastError();
+    })
+}
+
+}  // namespace nf

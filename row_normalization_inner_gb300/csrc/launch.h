@@ -1,0 +1,52 @@
+// Host-side launchers, one per kernel family.  Internal to libnf.so: the
+// C ABI in include/nf.h validates arguments, picks a plan and calls these.
+// Every launcher takes an already validated hidden size from the compiled
+// set and returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nf {
+
+// Row-group shape of the register path for `hidden`: threads per row,
+// rows per CTA.  False if `hidden` is not compiled.
+bool reg_shape(int64_t hidden, int* tpr, int* rpc);
+// Cluster path: CTAs per row (the cluster size) and threads per CTA.
+bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);
+// Bulk path: threads per CTA (one producer warp group + consumers), ring
+// stages and dynamic shared memory for `op` (0 fused, 1 rms, 2 ln fwd,
+// 3 ln bwd, 4 rms bwd).  False if no bulk kernel exists for (op, hidden).
+bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes);
+
+// Register path (rows resident in registers).
+cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
+                             float eps, int grid, cudaStream_t st);
+cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
+                           float eps, int grid, cudaStream_t st);
+cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
+                              const void* gamma, const void* beta, int64_t rows, float eps,
+                              int grid, cudaStream_t st);
+
+// Cluster path (one row split across a cluster of CTAs).
+cudaError_t launch_fused_cluster(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
+                                 float eps, int grid, cudaStream_t st);
+cudaError_t launch_rms_cluster(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
+                               float eps, int grid, cudaStream_t st);
+cudaError_t launch_ln_fwd_cluster(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
+                                  const void* gamma, const void* beta, int64_t rows, float eps,
+                                  int grid, cudaStream_t st);
+
+// LayerNorm backward, stage 1 (register path): `grid` persistent CTAs,
+// RPC row groups each, one column-partial slot per group.
+cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                              const float* mean, const float* rstd, const void* gamma,
+                              int64_t rows, int grid, cudaStream_t st);
+// Stage 2: dgamma/dbeta = fixed-order sum over the slots of ws[slot][2][hidden].
+cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
+                                 int64_t hidden, cudaStream_t st);
+
+// Bounded-wait self test (see nf_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace nf

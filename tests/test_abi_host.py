@@ -1,0 +1,207 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every symbol include/nf.h declares, rejects bad arguments before touching
+the GPU, and plans launches as documented."""
+import os
+import re
+
+import pytest
+import torch
+
+import row_normalization_inner_gb300 as nf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nf.h")
+HAVE_GPU = torch.cuda.is_available()
+
+# Fake, never dereferenced addresses.  Every call below that uses them must
+# return from argument validation; the few that would reach a launch are
+# only made when there is no GPU (then the first CUDA call fails cleanly).
+A = 0x10000000
+B = 0x20000000
+C = 0x30000000
+D = 0x40000000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from row_normalization_inner_gb300 import build
+    build.build()
+    yield
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(nf.EXPORTS) == _declared()
+
+
+def test_library_exports_every_declared_symbol():
+    lib = nf.lib()
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_in_dynamic_table():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", nf.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = set(l.split()[-1] for l in out.splitlines() if l.strip())
+    for name in _declared():
+        assert name in syms, name
+
+
+def test_status_strings_and_version():
+    assert nf.status_string(0) == "NF_OK"
+    assert nf.status_string(6) == "NF_ERR_TIMEOUT"
+    assert nf.status_string(99) == "NF_ERR_UNKNOWN"
+    assert "sm_103a" in nf.version()
+
+
+# ---------------------------------------------------------------- validation
+
+@pytest.mark.parametrize("hidden", [0, 1, 8, 1000, 3072, 4095, 16384, -4096])
+def test_unsupported_hidden(hidden):
+    assert nf.nf_fused_add_rmsnorm(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_rmsnorm_fwd(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_layernorm_fwd(A, 0, 0, B, C, D, 4, hidden, 1e-5, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, hidden, A, 1 << 30, None) == \
+        nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_layernorm_bwd_workspace_size(4, hidden) == 0
+
+
+def test_negative_rows_and_bad_eps():
+    assert nf.nf_fused_add_rmsnorm(A, B, C, -1, 4096, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    for eps in (0.0, -1e-6, float("nan"), float("inf")):
+        assert nf.nf_fused_add_rmsnorm(A, B, C, 4, 4096, eps, None) == nf.NF_ERR_INVALID_ARG
+        assert nf.nf_rmsnorm_fwd(A, B, C, 4, 4096, eps, None) == nf.NF_ERR_INVALID_ARG
+        assert nf.nf_layernorm_fwd(A, 0, 0, B, C, D, 4, 4096, eps, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, -3, 4096, A, 0, None) == nf.NF_ERR_INVALID_ARG
+
+
+def test_huge_rows_rejected():
+    assert nf.nf_rmsnorm_fwd(A, B, C, 2 ** 62, 4096, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+
+
+def test_zero_rows_is_a_no_op_even_with_null_pointers():
+    assert nf.nf_fused_add_rmsnorm(None, None, None, 0, 4096, 1e-6, None) == nf.NF_OK
+    assert nf.nf_rmsnorm_fwd(None, None, None, 0, 8192, 1e-6, None) == nf.NF_OK
+    assert nf.nf_layernorm_fwd(None, None, None, None, None, None, 0, 1024, 1e-5, None) == nf.NF_OK
+    assert nf.nf_layernorm_bwd(None, None, None, None, None, None, None, None, 0, 1024, None, 0,
+                               None) == nf.NF_OK
+    assert nf.nf_layernorm_bwd_workspace_size(0, 4096) == 0
+
+
+def test_null_pointers():
+    assert nf.nf_fused_add_rmsnorm(None, B, C, 4, 4096, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_fused_add_rmsnorm(A, B, None, 4, 4096, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_rmsnorm_fwd(A, None, C, 4, 4096, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_layernorm_fwd(A, 0, 0, B, None, D, 4, 4096, 1e-5, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_layernorm_bwd(A, B, C, D, A + 0x100000, None, C, D, 4, 4096, A, 1 << 30,
+                               None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, 4096, None, 1 << 30,
+                               None) == nf.NF_ERR_INVALID_ARG
+
+
+def test_misaligned_pointers():
+    assert nf.nf_fused_add_rmsnorm(A + 8, B, C, 4, 4096, 1e-6, None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_fused_add_rmsnorm(A, B + 2, C, 4, 4096, 1e-6, None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_fused_add_rmsnorm(A, B, C + 4, 4, 4096, 1e-6, None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_rmsnorm_fwd(A, B + 8, C, 4, 4096, 1e-6, None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_layernorm_fwd(A, B + 2, 0, C, D, D + 0x10000, 4, 4096, 1e-5, None) == \
+        nf.NF_ERR_MISALIGNED
+    assert nf.nf_layernorm_fwd(A, 0, 0, C, D + 8, D + 0x10000, 4, 4096, 1e-5, None) == \
+        nf.NF_ERR_MISALIGNED
+    assert nf.nf_layernorm_bwd(A, B + 4, C, D, A + 0x800000, B + 0x800000, C + 0x800000,
+                               D + 0x800000, 4, 4096, D + 0x900000, 1 << 30,
+                               None) == nf.NF_ERR_MISALIGNED
+
+
+def test_overlaps_rejected():
+    rows, hidden = 16, 4096
+    act = rows * hidden * 2
+    # fused: x and residual overlap
+    assert nf.nf_fused_add_rmsnorm(A, A + act // 2, C, rows, hidden, 1e-6, None) == \
+        nf.NF_ERR_INVALID_ARG
+    assert nf.nf_fused_add_rmsnorm(A, A, C, rows, hidden, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    # fused: weight inside x
+    assert nf.nf_fused_add_rmsnorm(A, B, A + 1024, rows, hidden, 1e-6, None) == \
+        nf.NF_ERR_INVALID_ARG
+    # rms: y partially overlapping x
+    assert nf.nf_rmsnorm_fwd(A + 8192, A, C, rows, hidden, 1e-6, None) == nf.NF_ERR_INVALID_ARG
+    # layernorm fwd: mean overlapping rstd
+    assert nf.nf_layernorm_fwd(A, D, D + 8, B, C, C + 0x10000, rows, hidden, 1e-5, None) == \
+        nf.NF_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(HAVE_GPU, reason="valid fake pointers would reach a launch")
+def test_exact_alias_passes_validation_without_gpu():
+    # y == x is allowed: validation passes and the first CUDA call fails
+    # cleanly because this machine has no GPU.
+    rows, hidden = 16, 4096
+    assert nf.nf_rmsnorm_fwd(A, A, C, rows, hidden, 1e-6, None) == nf.NF_ERR_CUDA
+    assert nf.nf_fused_add_rmsnorm(A, B, C, rows, hidden, 1e-6, None) == nf.NF_ERR_CUDA
+    assert nf.nf_layernorm_bwd_workspace_size(16, 4096) == 0
+
+
+def test_set_path_rejects_unknown():
+    assert nf.nf_set_path(17) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(-1) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
+
+
+# ---------------------------------------------------------------- planning (pure host)
+
+@pytest.mark.parametrize("hidden", nf.HIDDEN_SET)
+@pytest.mark.parametrize("rows", [1, 7, 16, 75, 76, 77, 151, 152, 4096, 65536, 2 ** 33])
+def test_forward_plans(hidden, rows):
+    sms = 152
+    for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd"):
+        st, reg = nf.nf_plan_compute(op, rows, hidden, sms, "reg")
+        assert st == nf.NF_OK
+        assert reg["path"] == "reg" and reg["cluster"] == 1 and reg["launches"] == 1
+        assert reg["block"] % 32 == 0 and reg["block"] <= 1024
+        tpr = reg["block"] // reg["rows_per_cta"]
+        assert (hidden // 8) % tpr == 0          # static split into whole vectors
+        assert 1 <= reg["grid"] <= 2 ** 31 - 1
+        assert reg["grid"] == min(-(-rows // reg["rows_per_cta"]), 2 ** 31 - 1)
+        st, cl = nf.nf_plan_compute(op, rows, hidden, sms, "cluster")
+        assert st == nf.NF_OK
+        assert cl["path"] == "cluster" and 2 <= cl["cluster"] <= 8
+        assert cl["grid"] % cl["cluster"] == 0
+        assert (hidden // 8) % (cl["cluster"] * cl["block"]) == 0
+        st, auto = nf.nf_plan_compute(op, rows, hidden, sms)
+        assert st == nf.NF_OK
+        want = "cluster" if -(-rows // reg["rows_per_cta"]) * 2 < sms else "reg"
+        assert auto["path"] == want
+
+
+@pytest.mark.parametrize("hidden", nf.HIDDEN_SET)
+@pytest.mark.parametrize("rows", [1, 3, 151, 152, 153, 16384, 65537])
+def test_backward_plans(hidden, rows):
+    for sms in (1, 148, 152):
+        st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms)
+        assert st == nf.NF_OK
+        assert p["path"] == "reg" and p["launches"] == 2
+        blocks = -(-rows // p["rows_per_cta"])
+        assert 1 <= p["grid"] <= min(blocks, sms * 4)
+        assert p["partials"] == p["grid"] * p["rows_per_cta"]
+        # every row lands in exactly one stripe and stripes cover 0..rows
+        n = p["partials"]
+        bounds = [rows * s // n for s in range(n + 1)]
+        assert bounds[0] == 0 and bounds[-1] == rows
+        assert all(b1 >= b0 for b0, b1 in zip(bounds, bounds[1:]))
+        assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) <= -(-rows // n)
+    assert nf.nf_plan_compute("layernorm_bwd", 16, hidden, 152, "cluster")[0] == \
+        nf.NF_ERR_UNSUPPORTED_PATH
+
+
+def test_plan_invalid_arguments():
+    assert nf.nf_plan_compute("fused_add_rmsnorm", -1, 4096, 152)[0] == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_plan_compute("fused_add_rmsnorm", 4, 4096, 0)[0] == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_plan_compute("fused_add_rmsnorm", 4, 4097, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_plan_compute(9, 4, 4096, 152)[0] == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_plan_compute(0, 4, 4096, 152, 9)[0] == nf.NF_ERR_INVALID_ARG
