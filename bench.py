@@ -242,14 +242,21 @@ def _ev():
     return torch.cuda.Event(enable_timing=True)
 
 
+SLEEP_CYCLES = 200_000  # ~0.1 ms of GPU-side spin before each timed launch
+
+
 def time_single_launches(fn, reps, flush=None, stream=None):
     """Median device time (ms) of single launches, each after an optional
-    L2 flush done outside the timed region."""
+    L2 flush done outside the timed region.  A short GPU-side sleep after
+    the flush keeps the stream busy while the host enqueues the start event
+    and the launch, so host launch latency does not leak into the interval.
+    Must run with `stream` as the current stream."""
     ts = []
     s = stream or torch.cuda.current_stream()
     for _ in range(reps):
         if flush is not None:
             flush()
+        torch.cuda._sleep(SLEEP_CYCLES)
         a, b = _ev(), _ev()
         a.record(s)
         fn()
@@ -259,55 +266,85 @@ def time_single_launches(fn, reps, flush=None, stream=None):
     return statistics.median(ts), min(ts)
 
 
+def _raw(nf, name, *args):
+    """A zero-overhead closure over one C entry point with fixed arguments."""
+    f = getattr(nf.lib(), name)
+    st = f(*args)
+    if st != 0:
+        raise RuntimeError(f"{name}: status {st}")
+    return lambda: f(*args)
+
+
 def ops_suite(nf, peak, stream, flush):
-    """Per-operation throughput: each op at its workload sizes, 20 single
-    launches (rotating through input sets larger than L2, or flushing)."""
+    """Per-operation throughput: each op at its workload sizes, single
+    launches with an L2 flush before each (median of the launches)."""
     out = {}
     dev = "cuda"
+    sh = stream.cuda_stream
 
     def roof(nbytes, ms):
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 2)}
 
+    # launch + event floor: a GPU-side no-op between the two events
+    ms, _ = time_single_launches(lambda: torch.cuda._sleep(0), 30, flush)
+    out["floor (empty launch)"] = {"us": round(ms * 1e3, 2)}
     # RMSNorm forward, prefill sizes
     for h in (4096, 8192):
         x, w = workloads.rms_inputs(ROWS, h, device=dev)
         y = torch.empty_like(x)
-        ms, _ = time_single_launches(lambda: nf.rmsnorm_fwd(x, w, EPS, out=y, stream=stream), 20, flush)
+        fn = _raw(nf, "nf_rmsnorm_fwd", y.data_ptr(), x.data_ptr(), w.data_ptr(), ROWS, h, EPS, sh)
+        ms, _ = time_single_launches(fn, 20, flush)
         out[f"rmsnorm_fwd {ROWS}x{h}"] = roof(rms_bytes(ROWS, h), ms)
         del x, y
     # LayerNorm forward
     for h in (1024, 4096, 12288):
         x, g, b = workloads.layernorm_fwd_inputs(ROWS, h, device=dev)
         y = torch.empty_like(x)
-        ms, _ = time_single_launches(lambda: nf.layernorm_fwd(x, g, b, EPS, out=y, stream=stream), 20, flush)
+        m = torch.empty(ROWS, device=dev)
+        r = torch.empty(ROWS, device=dev)
+        fn = _raw(nf, "nf_layernorm_fwd", y.data_ptr(), m.data_ptr(), r.data_ptr(), x.data_ptr(),
+                  g.data_ptr(), b.data_ptr(), ROWS, h, EPS, sh)
+        ms, _ = time_single_launches(fn, 20, flush)
         out[f"layernorm_fwd {ROWS}x{h}"] = roof(ln_fwd_bytes(ROWS, h), ms)
         del x, y
     # LayerNorm backward (both stages)
     for h in (1024, 4096, 8192):
         x, dy, g = workloads.layernorm_bwd_inputs(ROWS, h, device=dev)
         _, mean, rstd = nf.layernorm_fwd(x, g, torch.zeros_like(g), EPS, stream=stream)
-        ws = torch.empty(max(nf.nf_layernorm_bwd_workspace_size(ROWS, h), 16), dtype=torch.uint8,
-                         device=dev)
+        nws = max(nf.nf_layernorm_bwd_workspace_size(ROWS, h), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
         dx = torch.empty_like(x)
-        ms, _ = time_single_launches(
-            lambda: nf.layernorm_bwd(dy, x, mean, rstd, g, workspace=ws, out=dx, stream=stream), 20, flush)
-        out[f"layernorm_bwd {ROWS}x{h}"] = roof(ln_bwd_bytes(ROWS, h), ms)
+        dg = torch.empty(h, device=dev)
+        db = torch.empty(h, device=dev)
+        fn = _raw(nf, "nf_layernorm_bwd", dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
+                  x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), g.data_ptr(), ROWS, h,
+                  ws.data_ptr(), nws, sh)
+        ms, _ = time_single_launches(fn, 20, flush)
+        d = roof(ln_bwd_bytes(ROWS, h), ms)
+        d["path"] = nf.nf_plan_query("layernorm_bwd", ROWS, h)["path"]
+        out[f"layernorm_bwd {ROWS}x{h}"] = d
         del x, dy, dx, ws
     # fused add+RMSNorm small-batch sweep (latency; L2 flushed before each launch)
     for h in (4096, 8192):
         for rows in (1, 2, 4, 8, 32, 128):
             x, r, w = workloads.fused_inputs(rows, h, draw_rows=128, device=dev)
-            ms, _ = time_single_launches(lambda: nf.fused_add_rmsnorm(x, r, w, 1e-6, stream=stream), 30, flush)
+            fn = _raw(nf, "nf_fused_add_rmsnorm", x.data_ptr(), r.data_ptr(), w.data_ptr(), rows, h,
+                      1e-6, sh)
+            ms, _ = time_single_launches(fn, 30, flush)
             d = roof(fused_bytes(rows, h), ms)
             d["path"] = nf.nf_plan_query("fused_add_rmsnorm", rows, h)["path"]
             out[f"fused_add_rmsnorm {rows}x{h}"] = d
     # fused add+RMSNorm prefill, every size of the workload table
-    for rows in (4096, 65536):
+    for rows in (4096, 16384, 65536):
         for h in (2048, 4096, 5120, 8192):
             x, r, w = workloads.fused_inputs(rows, h, residual_scale=4.0, device=dev)
-            ms, _ = time_single_launches(lambda: nf.fused_add_rmsnorm(x, r, w, EPS, stream=stream), 10, flush)
-            out[f"fused_add_rmsnorm {rows}x{h}"] = roof(fused_bytes(rows, h), ms)
+            fn = _raw(nf, "nf_fused_add_rmsnorm", x.data_ptr(), r.data_ptr(), w.data_ptr(), rows, h,
+                      EPS, sh)
+            ms, _ = time_single_launches(fn, 10, flush)
+            d = roof(fused_bytes(rows, h), ms)
+            d["path"] = nf.nf_plan_query("fused_add_rmsnorm", rows, h)["path"]
+            out[f"fused_add_rmsnorm {rows}x{h}"] = d
             del x, r
     torch.cuda.empty_cache()
     return out
@@ -377,7 +414,8 @@ def run_gpu(args):
     dom_avg_ms = sum(dom_ms) / len(dom_ms)
     dom_bytes = fused_bytes(ROWS, DOMINANT_HIDDEN)
     achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9
-    traffic = _profiled_traffic(nf, "fused_add_rmsnorm", ROWS, DOMINANT_HIDDEN)
+    dom_path = nf.nf_plan_query("fused_add_rmsnorm", ROWS, DOMINANT_HIDDEN)["path"]
+    traffic = _profiled_traffic("fused_add_rmsnorm", dom_path, ROWS, DOMINANT_HIDDEN)
 
     # end to end through the C ABI with pinned host buffers
     e2e = None
@@ -450,7 +488,7 @@ def run_gpu(args):
             "rows_per_s": round(world * ROWS * len(HIDDENS) * args.steps / (ms_total * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "kernel": f"fused_add_rmsnorm hidden={DOMINANT_HIDDEN} rows={ROWS}",
+                         "kernel": f"fused_add_rmsnorm ({dom_path} path) hidden={DOMINANT_HIDDEN} rows={ROWS}",
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
                          "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
@@ -464,14 +502,14 @@ def run_gpu(args):
     return 0
 
 
-def _profiled_traffic(nf, op, rows, hidden):
+def _profiled_traffic(op, path, rows, hidden):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the kernel source that is built now; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        ent = d[f"{op} {rows}x{hidden}"]
+        ent = d[f"{op} {path} {rows}x{hidden}"]
         import hashlib
         h = hashlib.sha256()
         for fn in ent["sources"]:

@@ -138,9 +138,10 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x,
                            int64_t rows, int64_t hidden, float eps, nf_stream stream);
 
 /* Bytes of workspace nf_layernorm_bwd needs for (rows, hidden) on the
- * current device (0 when rows == 0 or hidden is unsupported).  The value
- * depends on the device's SM count, so query it on the device that runs
- * the call.  Returns 0 also if the device cannot be queried. */
+ * current device, under any kernel family (0 when rows == 0 or hidden is
+ * unsupported).  The value depends on the device's SM count, so query it
+ * on the device that runs the call.  Returns 0 also if the device cannot
+ * be queried. */
 size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden);
 
 /* LayerNorm backward.  With xhat = (x - mean) * rstd and g = dy * gamma:

@@ -57,6 +57,17 @@ bool prefer_cluster(int64_t rows, int rpc, int sms) {
     return ctas * 2 < sms;
 }
 
+// The library's own path choice.  Forward ops: a row goes to a cluster
+// when one CTA per row group would occupy fewer than half of the SMs;
+// otherwise the register path.  Backward: the register path.
+nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
+    (void)hidden;
+    const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
+                     op == NF_OP_LAYERNORM_FWD;
+    if (fwd && prefer_cluster(rows, rpc, sms)) return NF_PATH_CLUSTER;
+    return NF_PATH_REG;
+}
+
 std::atomic<int> g_forced_path{NF_PATH_AUTO};
 
 constexpr int kMaxDevices = 64;
@@ -176,8 +187,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
     if (op == NF_OP_RMSNORM_BWD) return NF_ERR_UNSUPPORTED_PATH;  // no kernel yet
 
     nf_path p = path;
-    if (p == NF_PATH_AUTO) p = (fwd && prefer_cluster(rows, rpc, sm_count)) ? NF_PATH_CLUSTER : NF_PATH_REG;
-    if (p == NF_PATH_BULK) return NF_ERR_UNSUPPORTED_PATH;
+    if (p == NF_PATH_AUTO) p = auto_path(op, rows, hidden, rpc, sm_count);
     if (p == NF_PATH_CLUSTER && !fwd) return NF_ERR_UNSUPPORTED_PATH;
 
     nf_plan pl;
@@ -201,6 +211,18 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.cluster = c;
         pl.rows_per_cta = 1;
         pl.launches = 1;
+    } else if (p == NF_PATH_BULK) {
+        int threads, stages, smem;
+        if (!bulk_shape(op, hidden, &threads, &stages, &smem)) return NF_ERR_UNSUPPORTED_PATH;
+        int64_t g = rows < sm_count ? rows : sm_count;
+        if (g < 1) g = 1;
+        pl.grid = static_cast<int32_t>(g);
+        pl.block = threads;
+        pl.cluster = 1;
+        pl.rows_per_cta = stages;  // rows in flight per CTA (ring stages)
+        pl.smem_bytes = smem;
+        pl.launches = fwd ? 1 : 2;
+        pl.partials = fwd ? 0 : static_cast<int32_t>(g);
     } else {  // register-path backward: persistent stage 1 + column reduce
         const int64_t blocks = (rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(sm_count) * bwd_ctas_per_sm(hidden);
@@ -245,6 +267,11 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
+    if (pl.path == NF_PATH_BULK) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        return from_cuda(launch_fused_bulk(hidden, x, residual, weight, rows, eps, pl.grid, status, s));
+    }
     return from_cuda(launch_fused_reg(hidden, x, residual, weight, rows, eps, pl.grid, s));
 }
 
@@ -262,6 +289,11 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
+    if (pl.path == NF_PATH_BULK) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        return from_cuda(launch_rms_bulk(hidden, y, x, weight, rows, eps, pl.grid, status, s));
+    }
     return from_cuda(launch_rms_reg(hidden, y, x, weight, rows, eps, pl.grid, s));
 }
 
@@ -288,14 +320,29 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
                                                pl.grid, s));
+    if (pl.path == NF_PATH_BULK) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        return from_cuda(launch_ln_fwd_bulk(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
+                                            pl.grid, status, s));
+    }
     return from_cuda(launch_ln_fwd_reg(hidden, y, mean, rstd, x, gamma, beta, rows, eps, pl.grid, s));
 }
 
 size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
     if (!hidden_ok(hidden) || rows <= 0) return 0;
-    nf_plan pl;
-    if (plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl) != NF_OK) return 0;
-    return static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+    int sms;
+    if (device_sm_count(&sms) != NF_OK) return 0;
+    // enough for every backward path, so a later nf_set_path cannot make a
+    // previously sized workspace too small
+    size_t most = 0;
+    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK}) {
+        nf_plan pl;
+        if (nf_plan_compute(NF_OP_LAYERNORM_BWD, rows, hidden, sms, p, &pl) != NF_OK) continue;
+        const size_t b = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+        if (b > most) most = b;
+    }
+    return most;
 }
 
 nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
@@ -336,8 +383,16 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
             return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (cudaError_t e = launch_ln_bwd_reg(hidden, dx, ws, dy, x, mean, rstd, gamma, rows, pl.grid, s))
+    if (pl.path == NF_PATH_BULK) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        if (cudaError_t e = launch_ln_bwd_bulk(hidden, dx, ws, dy, x, mean, rstd, gamma, rows,
+                                               pl.grid, status, s))
+            return from_cuda(e);
+    } else if (cudaError_t e = launch_ln_bwd_reg(hidden, dx, ws, dy, x, mean, rstd, gamma, rows,
+                                                 pl.grid, s)) {
         return from_cuda(e);
+    }
     return from_cuda(launch_column_reduce(ws, dgamma, dbeta, pl.partials, hidden, s));
 }
 

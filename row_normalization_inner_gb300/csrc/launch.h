@@ -46,6 +46,20 @@ cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* d
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
                                  int64_t hidden, cudaStream_t st);
 
+// Bulk-copy staged path: `grid` persistent CTAs (one per SM), each over a
+// contiguous row stripe; `status` is the device status word.
+cudaError_t launch_fused_bulk(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
+                              float eps, int grid, int* status, cudaStream_t st);
+cudaError_t launch_rms_bulk(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
+                            float eps, int grid, int* status, cudaStream_t st);
+cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
+                               const void* gamma, const void* beta, int64_t rows, float eps,
+                               int grid, int* status, cudaStream_t st);
+// Stage 1 of LayerNorm backward on the bulk path: one column-partial slot per CTA.
+cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                               const float* mean, const float* rstd, const void* gamma,
+                               int64_t rows, int grid, int* status, cudaStream_t st);
+
 // Bounded-wait self test (see nf_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
 

@@ -173,6 +173,13 @@ def test_forward_plans(hidden, rows):
         assert cl["path"] == "cluster" and 2 <= cl["cluster"] <= 8
         assert cl["grid"] % cl["cluster"] == 0
         assert (hidden // 8) % (cl["cluster"] * cl["block"]) == 0
+        st, bk = nf.nf_plan_compute(op, rows, hidden, sms, "bulk")
+        assert st == nf.NF_OK
+        assert bk["path"] == "bulk" and bk["cluster"] == 1 and bk["launches"] == 1
+        assert bk["grid"] == min(rows, sms) and bk["block"] % 128 == 0
+        assert (hidden // 8) % (bk["block"] - 128) == 0   # consumers split the row evenly
+        assert 2 <= bk["rows_per_cta"] <= 16               # ring stages
+        assert bk["smem_bytes"] <= 227 * 1024
         st, auto = nf.nf_plan_compute(op, rows, hidden, sms)
         assert st == nf.NF_OK
         want = "cluster" if -(-rows // reg["rows_per_cta"]) * 2 < sms else "reg"
@@ -197,6 +204,10 @@ def test_backward_plans(hidden, rows):
         assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) <= -(-rows // n)
     assert nf.nf_plan_compute("layernorm_bwd", 16, hidden, 152, "cluster")[0] == \
         nf.NF_ERR_UNSUPPORTED_PATH
+    for sms in (1, 152):
+        st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "bulk")
+        assert st == nf.NF_OK and p["path"] == "bulk" and p["launches"] == 2
+        assert p["grid"] == min(rows, sms) and p["partials"] == p["grid"]
 
 
 def test_plan_invalid_arguments():

@@ -18,7 +18,8 @@ from gpu_helpers import check_bf16, check_f32, host_f64, ulp_diff_bf16
 
 pytestmark = pytest.mark.gpu
 
-FWD_PATHS = ("reg", "cluster")
+FWD_PATHS = ("reg", "cluster", "bulk")
+BWD_PATHS = ("reg", "bulk")
 RAGGED_ROWS = (1, 3, 37, 152, 301)
 
 
@@ -222,40 +223,46 @@ def _oracle_bwd_chunked(dy, x, mean, rstd, g, chunk=2048):
     return np.concatenate(dxs), dgs, dbs
 
 
+@pytest.mark.parametrize("path", BWD_PATHS)
 @pytest.mark.parametrize("hidden", workloads.HIDDEN_SET)
 @pytest.mark.parametrize("rows", (1, 3, 37, 152, 301, 1000))
-def test_layernorm_bwd_all_sizes(rows, hidden):
+def test_layernorm_bwd_all_sizes(rows, hidden, path):
     x, dy, g = _ln_bwd_case(rows, hidden, seed=rows)
     mean, rstd = _saved_stats(x)
     dx_ref, dg_ref, db_ref = oracle.layernorm_bwd(dy, x, mean, rstd, g)
-    dx, dg, db = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+    with nf.forced_path(path):
+        dx, dg, db = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
     torch.cuda.synchronize()
-    check_bf16(dx, dx_ref, f"ln bwd dx {rows}x{hidden}")
-    check_f32(dg, dg_ref, f"ln bwd dgamma {rows}x{hidden}")
-    check_f32(db, db_ref, f"ln bwd dbeta {rows}x{hidden}")
+    check_bf16(dx, dx_ref, f"ln bwd dx {rows}x{hidden}/{path}")
+    check_f32(dg, dg_ref, f"ln bwd dgamma {rows}x{hidden}/{path}")
+    check_f32(db, db_ref, f"ln bwd dbeta {rows}x{hidden}/{path}")
 
 
+@pytest.mark.parametrize("path", ("auto",) + BWD_PATHS)
 @pytest.mark.parametrize("hidden", (1024, 4096, 8192))
-def test_layernorm_bwd_full_size(hidden):
+def test_layernorm_bwd_full_size(hidden, path):
     rows = 16384
     x, dy, g = _ln_bwd_case(rows, hidden)
     mean, rstd = _saved_stats(x)
-    dx, dg, db = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+    with nf.forced_path(path):
+        dx, dg, db = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
     torch.cuda.synchronize()
     dx_ref, dg_ref, db_ref = _oracle_bwd_chunked(dy, x, mean, rstd, g)
-    check_f32(dg, dg_ref, f"ln bwd full dgamma {hidden}")
-    check_f32(db, db_ref, f"ln bwd full dbeta {hidden}")
+    check_f32(dg, dg_ref, f"ln bwd full dgamma {hidden}/{path}")
+    check_f32(db, db_ref, f"ln bwd full dbeta {hidden}/{path}")
     idx = _sample_rows(rows, seed=hidden)
-    check_bf16(dx.cpu()[torch.from_numpy(idx)], dx_ref[idx], f"ln bwd full dx {hidden}")
+    check_bf16(dx.cpu()[torch.from_numpy(idx)], dx_ref[idx], f"ln bwd full dx {hidden}/{path}")
 
 
-def test_layernorm_bwd_in_place_alias():
-    rows, hidden = 64, 4096
+@pytest.mark.parametrize("path", BWD_PATHS)
+def test_layernorm_bwd_in_place_alias(path):
+    rows, hidden = 640, 4096
     x, dy, g = _ln_bwd_case(rows, hidden, seed=5)
     mean, rstd = _saved_stats(x)
     dx_ref, dg_ref, db_ref = oracle.layernorm_bwd(dy, x, mean, rstd, g)
     dyd = dy.cuda()
-    dx, dg, db = nf.layernorm_bwd(dyd, x.cuda(), mean.cuda(), rstd.cuda(), g.cuda(), out=dyd)
+    with nf.forced_path(path):
+        dx, dg, db = nf.layernorm_bwd(dyd, x.cuda(), mean.cuda(), rstd.cuda(), g.cuda(), out=dyd)
     torch.cuda.synchronize()
     check_bf16(dyd, dx_ref, "ln bwd dx written over dy")
     check_f32(dg, dg_ref, "ln bwd dgamma (aliased)")
@@ -286,19 +293,26 @@ def test_layernorm_bwd_zero_rows_zeroes_grads():
 
 # ---------------------------------------------------------------- determinism, empty, status
 
-def test_determinism_bitwise():
+@pytest.mark.parametrize("path", FWD_PATHS)
+def test_determinism_bitwise_forward(path):
     rows, hidden = 1000, 8192
     x, res, w = workloads.fused_inputs(rows, hidden)
     outs = []
     for _ in range(2):
         xd, rd = x.cuda(), res.cuda()
-        nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-6)
+        with nf.forced_path(path):
+            nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-6)
         outs.append((xd.cpu(), rd.cpu()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("path", BWD_PATHS)
+def test_determinism_bitwise_backward(path):
     xb, dy, g = _ln_bwd_case(3000, 4096)
     mean, rstd = _saved_stats(xb)
-    r1 = nf.layernorm_bwd(dy.cuda(), xb.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
-    r2 = nf.layernorm_bwd(dy.cuda(), xb.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+    with nf.forced_path(path):
+        r1 = nf.layernorm_bwd(dy.cuda(), xb.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+        r2 = nf.layernorm_bwd(dy.cuda(), xb.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
     for a, b in zip(r1, r2):
         assert torch.equal(a.cpu(), b.cpu())
 
@@ -317,6 +331,8 @@ def test_plan_query_matches_pure_planner():
     for op in ("fused_add_rmsnorm", "layernorm_fwd", "layernorm_bwd"):
         for rows in (1, 16, 4096):
             assert nf.nf_plan_query(op, rows, 4096) == nf.nf_plan_compute(op, rows, 4096, sms)[1]
+    with nf.forced_path("bulk"):
+        assert nf.nf_plan_query("fused_add_rmsnorm", 4096, 8192)["path"] == "bulk"
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
