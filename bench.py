@@ -18,8 +18,9 @@ pinned host buffers (host->device copy of x and residual, the call, and the
 device->host copy of both results, every step); `cpu_baseline` (the fp64
 oracle on the host cores, a bounded sample); `clocks` sampled with
 nvidia-smi during the timed region; and `ops`, per-operation GB/s and
-roofline fractions for RMSNorm forward, LayerNorm forward / backward and the
-small-batch sweep (single launches with an L2 flush between them).
+roofline fractions for every fused size, RMSNorm forward, LayerNorm forward /
+backward and the small-batch sweep (launches captured back to back in a CUDA
+graph over enough input sets that each replay touches twice the L2 size).
 
 `--impl reference` times the oracle instead (the reference arm of this
 path), on a bounded sample of the same workload.
@@ -242,111 +243,128 @@ def _ev():
     return torch.cuda.Event(enable_timing=True)
 
 
-SLEEP_CYCLES = 200_000  # ~0.1 ms of GPU-side spin before each timed launch
-
-
-def time_single_launches(fn, reps, flush=None, stream=None):
-    """Median device time (ms) of single launches, each after an optional
-    L2 flush done outside the timed region.  A short GPU-side sleep after
-    the flush keeps the stream busy while the host enqueues the start event
-    and the launch, so host launch latency does not leak into the interval.
-    Must run with `stream` as the current stream."""
-    ts = []
-    s = stream or torch.cuda.current_stream()
-    for _ in range(reps):
-        if flush is not None:
-            flush()
-        torch.cuda._sleep(SLEEP_CYCLES)
-        a, b = _ev(), _ev()
-        a.record(s)
-        fn()
-        b.record(s)
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts), min(ts)
-
-
-def _raw(nf, name, *args):
-    """A zero-overhead closure over one C entry point with fixed arguments."""
-    f = getattr(nf.lib(), name)
-    st = f(*args)
-    if st != 0:
-        raise RuntimeError(f"{name}: status {st}")
-    return lambda: f(*args)
-
-
-def ops_suite(nf, peak, stream, flush):
-    """Per-operation throughput: each op at its workload sizes, single
-    launches with an L2 flush before each (median of the launches)."""
-    out = {}
-    dev = "cuda"
+def graph_time_ms(launch, n, stream, replays=5):
+    """Mean device time per launch: `n` launches captured back to back in
+    one CUDA graph (launch(i, stream_handle) enqueues launch i), the graph
+    replayed `replays` times between CUDA events; median of the replays.
+    Timing many launches at once keeps the event timer's granularity (4 us
+    on the GB300 machines) and host launch latency out of the result."""
     sh = stream.cuda_stream
+    launch(0, sh)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            launch(i, sh)
+    ts = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        stream.synchronize()
+        for _ in range(replays):
+            a, b = _ev(), _ev()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / n)
+    del g
+    return statistics.median(ts)
 
-    def roof(nbytes, ms):
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 2)}
 
-    # launch + event floor: a GPU-side no-op between the two events
-    ms, _ = time_single_launches(lambda: torch.cuda._sleep(0), 30, flush)
-    out["floor (empty launch)"] = {"us": round(ms * 1e3, 2)}
-    # RMSNorm forward, prefill sizes
-    for h in (4096, 8192):
-        x, w = workloads.rms_inputs(ROWS, h, device=dev)
+def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
+    """Inputs for timing `op` at (rows, hidden) on L2-cold data: enough
+    independent input sets that the launches of one graph replay touch at
+    least twice the L2 size.  Returns (launch(i, stream), sets, bytes)."""
+    lib = nf.lib()
+    if op == "fused_add_rmsnorm":
+        foot, nbytes = 4 * hidden * rows, fused_bytes(rows, hidden)
+    elif op == "rmsnorm_fwd":
+        foot, nbytes = 4 * hidden * rows, rms_bytes(rows, hidden)
+    elif op == "layernorm_fwd":
+        foot, nbytes = (4 * hidden + 8) * rows, ln_fwd_bytes(rows, hidden)
+    else:
+        foot, nbytes = (6 * hidden + 8) * rows, ln_bwd_bytes(rows, hidden)
+    sets = max(1, min(16384, -(-2 * l2_bytes // foot)))
+    tot = sets * rows
+    a2 = rows * hidden * 2  # bytes per set of one bf16 activation
+    if op == "fused_add_rmsnorm":
+        x, r, w = workloads.fused_inputs(tot, hidden, residual_scale=4.0, device=dev)
+        px, pr, pw = x.data_ptr(), r.data_ptr(), w.data_ptr()
+        keep = (x, r, w)
+        fn = lambda i, sh: lib.nf_fused_add_rmsnorm(px + (i % sets) * a2, pr + (i % sets) * a2, pw,  # noqa: E731
+                                                     rows, hidden, eps, sh)
+    elif op == "rmsnorm_fwd":
+        x, w = workloads.rms_inputs(tot, hidden, device=dev)
         y = torch.empty_like(x)
-        fn = _raw(nf, "nf_rmsnorm_fwd", y.data_ptr(), x.data_ptr(), w.data_ptr(), ROWS, h, EPS, sh)
-        ms, _ = time_single_launches(fn, 20, flush)
-        out[f"rmsnorm_fwd {ROWS}x{h}"] = roof(rms_bytes(ROWS, h), ms)
-        del x, y
-    # LayerNorm forward
-    for h in (1024, 4096, 12288):
-        x, g, b = workloads.layernorm_fwd_inputs(ROWS, h, device=dev)
+        px, py, pw = x.data_ptr(), y.data_ptr(), w.data_ptr()
+        keep = (x, y, w)
+        fn = lambda i, sh: lib.nf_rmsnorm_fwd(py + (i % sets) * a2, px + (i % sets) * a2, pw,  # noqa: E731
+                                               rows, hidden, eps, sh)
+    elif op == "layernorm_fwd":
+        x, g, b = workloads.layernorm_fwd_inputs(tot, hidden, device=dev)
         y = torch.empty_like(x)
-        m = torch.empty(ROWS, device=dev)
-        r = torch.empty(ROWS, device=dev)
-        fn = _raw(nf, "nf_layernorm_fwd", y.data_ptr(), m.data_ptr(), r.data_ptr(), x.data_ptr(),
-                  g.data_ptr(), b.data_ptr(), ROWS, h, EPS, sh)
-        ms, _ = time_single_launches(fn, 20, flush)
-        out[f"layernorm_fwd {ROWS}x{h}"] = roof(ln_fwd_bytes(ROWS, h), ms)
-        del x, y
-    # LayerNorm backward (both stages)
-    for h in (1024, 4096, 8192):
-        x, dy, g = workloads.layernorm_bwd_inputs(ROWS, h, device=dev)
-        _, mean, rstd = nf.layernorm_fwd(x, g, torch.zeros_like(g), EPS, stream=stream)
-        nws = max(nf.nf_layernorm_bwd_workspace_size(ROWS, h), 16)
-        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        m = torch.empty(tot, device=dev)
+        rs = torch.empty(tot, device=dev)
+        px, py, pg, pb, pm, pr = (t.data_ptr() for t in (x, y, g, b, m, rs))
+        keep = (x, y, g, b, m, rs)
+        fn = lambda i, sh: lib.nf_layernorm_fwd(py + (i % sets) * a2, pm + (i % sets) * rows * 4,  # noqa: E731
+                                                 pr + (i % sets) * rows * 4, px + (i % sets) * a2,
+                                                 pg, pb, rows, hidden, eps, sh)
+    else:
+        x, dy, g = workloads.layernorm_bwd_inputs(tot, hidden, device=dev)
+        _, m, rs = nf.layernorm_fwd(x, g, torch.zeros_like(g), eps)
         dx = torch.empty_like(x)
-        dg = torch.empty(h, device=dev)
-        db = torch.empty(h, device=dev)
-        fn = _raw(nf, "nf_layernorm_bwd", dx.data_ptr(), dg.data_ptr(), db.data_ptr(), dy.data_ptr(),
-                  x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), g.data_ptr(), ROWS, h,
-                  ws.data_ptr(), nws, sh)
-        ms, _ = time_single_launches(fn, 20, flush)
-        d = roof(ln_bwd_bytes(ROWS, h), ms)
-        d["path"] = nf.nf_plan_query("layernorm_bwd", ROWS, h)["path"]
-        out[f"layernorm_bwd {ROWS}x{h}"] = d
-        del x, dy, dx, ws
-    # fused add+RMSNorm small-batch sweep (latency; L2 flushed before each launch)
+        nws = max(nf.nf_layernorm_bwd_workspace_size(rows, hidden), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        dg = torch.empty(hidden, device=dev)
+        db = torch.empty(hidden, device=dev)
+        px, pdy, pg, pm, pr, pdx, pws, pdg, pdb = (t.data_ptr() for t in (x, dy, g, m, rs, dx, ws, dg, db))
+        keep = (x, dy, g, m, rs, dx, ws, dg, db)
+        fn = lambda i, sh: lib.nf_layernorm_bwd(pdx + (i % sets) * a2, pdg, pdb, pdy + (i % sets) * a2,  # noqa: E731
+                                                 px + (i % sets) * a2, pm + (i % sets) * rows * 4,
+                                                 pr + (i % sets) * rows * 4, pg, rows, hidden, pws, nws, sh)
+
+    def launch(i, sh, _keep=keep):
+        st = fn(i, sh)
+        if st != 0:
+            raise RuntimeError(f"{op} {rows}x{hidden}: status {st}")
+    return launch, sets, nbytes
+
+
+def time_op(nf, op, rows, hidden, eps, l2_bytes, stream, min_launches=20):
+    launch, sets, nbytes = op_case(nf, op, rows, hidden, eps, l2_bytes)
+    n = max(sets, min_launches)
+    ms = graph_time_ms(launch, n, stream)
+    del launch
+    torch.cuda.empty_cache()
+    return ms, nbytes
+
+
+def ops_suite(nf, peak, stream, l2_bytes):
+    """Per-operation device time at every workload size: launches captured
+    back to back in a CUDA graph over L2-cold input sets (section 9 of the
+    design notes)."""
+    out = {}
+
+    def entry(op, rows, h, eps):
+        ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[f"{op} {rows}x{h}"] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                   "us": round(ms * 1e3, 3),
+                                   "path": nf.nf_plan_query(op, rows, h)["path"]}
+
     for h in (4096, 8192):
-        for rows in (1, 2, 4, 8, 32, 128):
-            x, r, w = workloads.fused_inputs(rows, h, draw_rows=128, device=dev)
-            fn = _raw(nf, "nf_fused_add_rmsnorm", x.data_ptr(), r.data_ptr(), w.data_ptr(), rows, h,
-                      1e-6, sh)
-            ms, _ = time_single_launches(fn, 30, flush)
-            d = roof(fused_bytes(rows, h), ms)
-            d["path"] = nf.nf_plan_query("fused_add_rmsnorm", rows, h)["path"]
-            out[f"fused_add_rmsnorm {rows}x{h}"] = d
-    # fused add+RMSNorm prefill, every size of the workload table
+        for rows in (1, 2, 4, 8, 16, 32, 128):
+            entry("fused_add_rmsnorm", rows, h, 1e-6)
     for rows in (4096, 16384, 65536):
         for h in (2048, 4096, 5120, 8192):
-            x, r, w = workloads.fused_inputs(rows, h, residual_scale=4.0, device=dev)
-            fn = _raw(nf, "nf_fused_add_rmsnorm", x.data_ptr(), r.data_ptr(), w.data_ptr(), rows, h,
-                      EPS, sh)
-            ms, _ = time_single_launches(fn, 10, flush)
-            d = roof(fused_bytes(rows, h), ms)
-            d["path"] = nf.nf_plan_query("fused_add_rmsnorm", rows, h)["path"]
-            out[f"fused_add_rmsnorm {rows}x{h}"] = d
-            del x, r
-    torch.cuda.empty_cache()
+            entry("fused_add_rmsnorm", rows, h, EPS)
+    for h in (4096, 8192):
+        entry("rmsnorm_fwd", ROWS, h, EPS)
+    for h in (1024, 4096, 12288):
+        entry("layernorm_fwd", ROWS, h, EPS)
+    for h in (1024, 4096, 8192):
+        entry("layernorm_bwd", ROWS, h, EPS)
     return out
 
 
@@ -456,15 +474,9 @@ def run_gpu(args):
 
     ops = None
     if rank == 0 and not args.no_ops:
-        scratch = torch.empty(2 * torch.cuda.get_device_properties(local).L2_cache_size // 4 + 1,
-                              dtype=torch.float32, device=dev)
-
-        def flush():
-            scratch.fill_(1.0)
         del sets
         torch.cuda.empty_cache()
-        with torch.cuda.stream(stream):  # flush, events and kernels on one stream
-            ops = ops_suite(nf, peak, stream, flush)
+        ops = ops_suite(nf, peak, stream, torch.cuda.get_device_properties(local).L2_cache_size)
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -105,7 +105,7 @@ typedef struct {
     int32_t grid;            /* CTAs in the main launch */
     int32_t block;           /* threads per CTA */
     int32_t cluster;         /* CTAs per cluster (1 = none) */
-    int32_t rows_per_cta;    /* rows a CTA handles at once */
+    int32_t rows_per_cta;    /* rows a CTA computes at once (bulk: consumer row groups) */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t launches;        /* kernel launches per call */
     int32_t partials;        /* column-partial slots (backward ops), else 0 */

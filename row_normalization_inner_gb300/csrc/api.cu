@@ -212,17 +212,17 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.rows_per_cta = 1;
         pl.launches = 1;
     } else if (p == NF_PATH_BULK) {
-        int threads, stages, smem;
-        if (!bulk_shape(op, hidden, &threads, &stages, &smem)) return NF_ERR_UNSUPPORTED_PATH;
+        int threads, stages, smem, groups;
+        if (!bulk_shape(op, hidden, &threads, &stages, &smem, &groups)) return NF_ERR_UNSUPPORTED_PATH;
         int64_t g = rows < sm_count ? rows : sm_count;
         if (g < 1) g = 1;
         pl.grid = static_cast<int32_t>(g);
         pl.block = threads;
         pl.cluster = 1;
-        pl.rows_per_cta = stages;  // rows in flight per CTA (ring stages)
+        pl.rows_per_cta = groups;  // rows being computed at once per CTA
         pl.smem_bytes = smem;
         pl.launches = fwd ? 1 : 2;
-        pl.partials = fwd ? 0 : static_cast<int32_t>(g);
+        pl.partials = fwd ? 0 : static_cast<int32_t>(g * groups);
     } else {  // register-path backward: persistent stage 1 + column reduce
         const int64_t blocks = (rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(sm_count) * bwd_ctas_per_sm(hidden);

@@ -7,24 +7,31 @@
 // is the producer: one elected thread issues, per row, one 1-D bulk
 // asynchronous copy (cp.async.bulk, global -> this CTA's shared memory) per
 // input tensor into a ring of S stages, each completing on the stage's
-// "full" mbarrier.  The remaining NCWG warp groups are consumers: they wait
-// on "full", read the row from shared memory with 128-bit loads into
-// registers, release the stage on its "empty" mbarrier at once (so the next
-// copy starts while they still compute), reduce and normalize the row in
-// registers and store the results with 128-bit streaming stores.  So up to
-// S rows per SM are in flight regardless of the register budget.
+// "full" mbarrier.  The consumers are NG independent row groups of GW warps
+// each; row i of the stripe belongs to group i % NG, and every group owns a
+// private slice of SG ring stages which it consumes strictly in order (so a
+// stage's barrier phases and the group's row sequence move in lockstep and
+// a parity wait can never match a phase from an earlier use).  A group
+// waits on its row's "full" barrier, reads the row from shared memory with
+// 128-bit loads into registers (4 vectors of 8 bf16 per thread), releases the
+// stage on its
+// "empty" mbarrier at once (so the next copy starts while it computes),
+// reduces the row within the group (warp shuffles, then a named barrier
+// private to the group), normalizes in registers and stores with 128-bit
+// streaming stores.  Up to S rows per SM are in flight in the ring and NG
+// rows are being computed at once, independent of the register budget.
 //
 // Register sharing: with SHARE the producer warp group drops to 40
-// registers per thread (setmaxnreg.dec) and the consumer groups rise to
+// registers per thread (setmaxnreg.dec) and the consumer warps rise to
 // CONS_REGS.  The host only launches the SHARE variant after checking that
 // the kernel's launch register count covers the split; otherwise it
 // launches the variant without setmaxnreg (same results).
 //
 // Every mbarrier wait is bounded (2 s on the global timer).  A consumer
-// that gives up raises a CTA-wide flag that all consumer warps read after
-// the next consumer barrier, so they leave together; the producer, on
-// giving up, waits (bounded) for the copies it already issued and leaves.
-// Either records NF_ERR_TIMEOUT in the device status word.
+// warp that gives up contributes a failure count to its group's reduction,
+// so the whole group sees the same total and leaves together; the producer,
+// on giving up, waits (bounded) for the copies it already issued and
+// leaves.  Either records NF_ERR_TIMEOUT in the device status word.
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,17 +39,18 @@ namespace nf {
 
 enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3 };
 
-template <int H> struct BulkShape;
-// NCWG consumer warp groups per CTA (so 128 * NCWG consumer threads).
-template <> struct BulkShape<1024>  { static constexpr int NCWG = 1; };
-template <> struct BulkShape<2048>  { static constexpr int NCWG = 1; };
-template <> struct BulkShape<4096>  { static constexpr int NCWG = 1; };
-template <> struct BulkShape<5120>  { static constexpr int NCWG = 1; };
-template <> struct BulkShape<8192>  { static constexpr int NCWG = 2; };
-template <> struct BulkShape<12288> { static constexpr int NCWG = 2; };
+// Row-group shape: GW warps per row (so each thread holds 4 vectors of its
+// row) and NG concurrent row groups per CTA.
+template <int OP, int H>
+struct BulkShape {
+    static constexpr int GW = H / kVec / 4 / 32;
+    static constexpr int NG_FWD = (H >= 12288) ? 1 : (16 / GW > 0 ? 16 / GW : 1);
+    static constexpr int NG_BWD = (GW >= 5) ? 1 : 8 / GW;
+    static constexpr int NG = OP == 3 ? NG_BWD : NG_FWD;
+};
 
 constexpr int kSmemBudget = 200 * 1024;  // ring + barriers + reduction scratch
-constexpr int kMaxStages = 16;
+constexpr int kMaxStagesPerGroup = 8;
 constexpr int kProducerRegs = 40;
 
 template <int OP> struct OpIO {
@@ -51,28 +59,35 @@ template <int OP> struct OpIO {
 
 template <int OP, int H>
 struct BGeo {
-    static constexpr int NCWG = BulkShape<H>::NCWG;
-    static constexpr int NCT = 128 * NCWG;            // consumer threads
-    static constexpr int NCW = NCT / 32;              // consumer warps
+    static constexpr int GW = BulkShape<OP, H>::GW;
+    static constexpr int NG = BulkShape<OP, H>::NG;
+    static constexpr int GT = GW * 32;                // threads per row group
+    static constexpr int NCT = NG * GT;               // consumer threads
     static constexpr int THREADS = 128 + NCT;
     static constexpr int NV = H / kVec;
-    static constexpr int VPT = NV / NCT;
-    static_assert(NV % NCT == 0, "row must split evenly over the consumer threads");
+    static constexpr int VPT = NV / GT;
+    static_assert(NV % GT == 0 && VPT == 4, "four vectors per consumer thread");
+    static_assert(THREADS <= 1024, "CTA size");
+    static_assert(GW == 1 || NG <= 15, "named barriers 1..NG");
     static constexpr int ROW_BYTES = H * 2;
     static constexpr int STAGE_BYTES = ROW_BYTES * OpIO<OP>::NIN;
-    static constexpr int S0 = kSmemBudget / STAGE_BYTES;
-    static constexpr int S = S0 > kMaxStages ? kMaxStages : S0;
-    static_assert(S >= 2, "need at least two stages");
-    // consumer register target: what the launch allocation leaves after the producer drops to 40
-    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
-    static constexpr int CONS_REGS_RAW = (LAUNCH_REGS * THREADS - 128 * kProducerRegs) / NCT / 8 * 8;
-    static constexpr int CONS_REGS = CONS_REGS_RAW > 248 ? 248 : CONS_REGS_RAW;
+    static constexpr int SG0 = kSmemBudget / STAGE_BYTES / NG;
+    static constexpr int SG = SG0 > kMaxStagesPerGroup ? kMaxStagesPerGroup : SG0;  // stages per group
+    static_assert(SG >= 2, "need at least two stages per row group");
+    static constexpr int S = SG * NG;                  // ring stages
+    // registers: the launch allocation, and what consumers get after the
+    // producer group drops to kProducerRegs
+    static constexpr int LAUNCH_REGS0 = (65536 / THREADS) / 8 * 8;
+    static constexpr int LAUNCH_REGS = LAUNCH_REGS0 > 248 ? 248 : LAUNCH_REGS0;
+    static constexpr int CONS_REGS0 = (LAUNCH_REGS * THREADS - 128 * kProducerRegs) / NCT / 8 * 8;
+    static constexpr int CONS_REGS = CONS_REGS0 > 248 ? 248 : CONS_REGS0;
+    // reduction scratch per group: 4 buffers (2 row parities x 2 reductions) x GW x 3 floats
+    static constexpr int RED_PER_GROUP = 4 * GW * 3;
     // dynamic shared memory layout
     static constexpr int RING = S * STAGE_BYTES;
-    static constexpr int BAR_OFF = RING;                    // full[S], empty[S]
-    static constexpr int RED_OFF = BAR_OFF + 2 * S * 8;     // 2 buffers x NCW x 2 floats
-    static constexpr int FLAG_OFF = RED_OFF + 2 * NCW * 2 * 4;
-    static constexpr int SMEM = FLAG_OFF + 16;
+    static constexpr int BAR_OFF = RING;                     // full[S], empty[S]
+    static constexpr int RED_OFF = BAR_OFF + 2 * S * 8;
+    static constexpr int SMEM = RED_OFF + NG * RED_PER_GROUP * 4;
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -81,8 +96,8 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync(int nct) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nct) : "memory");
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -92,20 +107,25 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
     return v;
 }
 
-template <int N>
-__device__ __forceinline__ void consumer_sum(float (&v)[N], float* red, int ct, int ncw, int nct) {
+// Sum N values over the GW warps of one row group; every thread of the
+// group gets the same totals (warps summed in a fixed order).  `rb` is this
+// reduction's private GW*N-float buffer.
+template <int GW, int N>
+__device__ __forceinline__ void group_reduce(float (&v)[N], float* rb, int gwarp, int lane, int gid) {
     warp_sum<N>(v);
-    const int warp = ct >> 5, lane = ct & 31;
-    if (lane == 0) {
+    if constexpr (GW > 1) {
+        if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < N; ++i) red[warp * N + i] = v[i];
-    }
-    consumer_sync(nct);
+            for (int i = 0; i < N; ++i) rb[gwarp * N + i] = v[i];
+        }
+        named_sync(1 + gid, GW * 32);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        float s = 0.f;
-        for (int w = 0; w < ncw; ++w) s += red[w * N + i];
-        v[i] = s;
+        for (int i = 0; i < N; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < GW; ++w) s += rb[w * N + i];
+            v[i] = s;
+        }
     }
 }
 
@@ -118,7 +138,7 @@ struct BulkArgs {
     const uint16_t* p1;      // beta
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
-    float* ws;               // ln bwd column partials [grid][2][H]
+    float* ws;               // ln bwd column partials [grid * NG][2][H]
     int* status;
     int64_t rows;
     float eps;
@@ -131,8 +151,6 @@ norm_bulk_kernel(BulkArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::BAR_OFF);
     uint64_t* empty = full + G::S;
-    float* red = reinterpret_cast<float*>(smem + G::RED_OFF);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::FLAG_OFF);
 
     const int64_t nct = gridDim.x;
     const int64_t r0 = a.rows * blockIdx.x / nct;
@@ -142,9 +160,8 @@ norm_bulk_kernel(BulkArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < G::S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], G::NCW);
+            mbar_init(&empty[s], G::GW);  // the GW warps of the group that consumed it
         }
-        *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -156,8 +173,9 @@ norm_bulk_kernel(BulkArgs a) {
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < n; ++i) {
-                const int s = i % G::S;
-                const uint32_t par = ((i / G::S) & 1) ^ 1;
+                const int q = i / G::NG;  // row index within its group
+                const int s = (i % G::NG) * G::SG + q % G::SG;
+                const uint32_t par = ((q / G::SG) & 1) ^ 1;
                 if (!mbar_wait(&empty[s], par, kWaitLimitNs)) { ok = false; break; }
                 mbar_arrive_expect_tx(&full[s], G::STAGE_BYTES);
                 const int64_t row = r0 + i;
@@ -170,25 +188,29 @@ norm_bulk_kernel(BulkArgs a) {
             if (!ok) {
                 record_status(a.status, kStatusTimeout);
                 // let the copies already issued land before the CTA can exit
+                // (the last S issued rows cover every stage exactly once)
                 const int first = issued > G::S ? issued - G::S : 0;
-                for (int i = first; i < issued; ++i)
-                    mbar_wait(&full[i % G::S], (i / G::S) & 1, kWaitLimitNs / 4);
+                for (int i = first; i < issued; ++i) {
+                    const int q = i / G::NG;
+                    mbar_wait(&full[(i % G::NG) * G::SG + q % G::SG], (q / G::SG) & 1, kWaitLimitNs / 4);
+                }
             }
         }
         return;
     }
 
-    // ---------------- consumer warp groups
+    // ---------------- consumer row groups
     if constexpr (SHARE) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(G::CONS_REGS));
     const int ct = threadIdx.x - 128;
-    const int lane = ct & 31;
+    const int gid = ct / G::GT;          // row group
+    const int gt = ct % G::GT;           // thread within the group
+    const int gwarp = gt >> 5, lane = gt & 31;
+    float* red = reinterpret_cast<float*>(smem + G::RED_OFF) + gid * G::RED_PER_GROUP;
 
-    uint4 prm0[G::VPT], prm1[G::VPT];  // weight/gamma and beta, loaded once
+    uint4 prm0[G::VPT];  // weight / gamma, loaded once (beta is re-read from L1 per row)
 #pragma unroll
     for (int k = 0; k < G::VPT; ++k) {
-        prm0[k] = ld_param(a.p0 + (k * G::NCT + ct) * kVec);
-        if constexpr (OP == kLnFwd) prm1[k] = ld_param(a.p1 + (k * G::NCT + ct) * kVec);
-        else prm1[k] = make_uint4(0, 0, 0, 0);
+        prm0[k] = ld_param(a.p0 + (k * G::GT + gt) * kVec);
     }
     float acc_g[OP == kLnBwd ? G::VPT : 1][8], acc_b[OP == kLnBwd ? G::VPT : 1][8];
     if constexpr (OP == kLnBwd) {
@@ -197,31 +219,35 @@ norm_bulk_kernel(BulkArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) { acc_g[k][e] = 0.f; acc_b[k][e] = 0.f; }
     }
-    // saved statistics of the next row, fetched one row ahead
+    // saved statistics of the group's next row, fetched one row ahead
     float nmu = 0.f, nrs = 0.f;
     if constexpr (OP == kLnBwd) {
-        if (n > 0) { nmu = __ldg(a.mean + r0); nrs = __ldg(a.rstd + r0); }
+        if (gid < n) { nmu = __ldg(a.mean + r0 + gid); nrs = __ldg(a.rstd + r0 + gid); }
     }
 
-    for (int i = 0; i < n; ++i) {
-        const int s = i % G::S;
-        const uint32_t par = (i / G::S) & 1;
+    bool failed = false;
+    int j = 0;  // this group's row counter (selects the reduction buffers)
+    for (int i = gid; i < n; i += G::NG, ++j) {
+        const int s = gid * G::SG + j % G::SG;   // j == i / NG
+        const uint32_t par = (j / G::SG) & 1;
         const int64_t row = r0 + i;
-        if (!mbar_wait(&full[s], par, kWaitLimitNs)) *abort_flag = 1;
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[s], par, kWaitLimitNs));
+        const float fail = ok ? 0.f : 1.f;
         const uint8_t* st = smem + s * G::STAGE_BYTES;
         uint4 v0[G::VPT], v1[G::VPT];
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) {
-            v0[k] = lds128(st + (k * G::NCT + ct) * 16);
-            if constexpr (OpIO<OP>::NIN == 2) v1[k] = lds128(st + G::ROW_BYTES + (k * G::NCT + ct) * 16);
+            v0[k] = lds128(st + (k * G::GT + gt) * 16);
+            if constexpr (OpIO<OP>::NIN == 2) v1[k] = lds128(st + G::ROW_BYTES + (k * G::GT + gt) * 16);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled now
-        float* rb = red + (i & 1) * G::NCW * 2;
+        float* rb0 = red + ((j & 1) * 2 + 0) * G::GW * 3;
+        float* rb1 = red + ((j & 1) * 2 + 1) * G::GW * 3;
 
         if constexpr (OP == kFused || OP == kRms) {
             float f[G::VPT][8];
-            float ss[1] = {0.f};
+            float v[2] = {0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 unpack8(v0[k], f[k]);
@@ -232,63 +258,69 @@ norm_bulk_kernel(BulkArgs a) {
                     for (int e = 0; e < 8; ++e) f[k][e] += b[e];
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss[0] += f[k][e] * f[k][e];
+                for (int e = 0; e < 8; ++e) v[0] += f[k][e] * f[k][e];
             }
-            consumer_sum<1>(ss, rb, ct, G::NCW, G::NCT);
-            if (*abort_flag) break;
+            group_reduce<G::GW, 2>(v, rb0, gwarp, lane, gid);
+            if (v[1] != 0.f) { failed = true; break; }
             if constexpr (OP == kFused) {
 #pragma unroll
                 for (int k = 0; k < G::VPT; ++k)
-                    st_stream(a.out1 + row * H + (k * G::NCT + ct) * kVec, pack8(f[k]));
+                    st_stream(a.out1 + row * H + (k * G::GT + gt) * kVec, pack8(f[k]));
             }
-            const float rstd = rsqrtf(ss[0] * (1.0f / H) + a.eps);
+            const float rstd = rsqrtf(v[0] * (1.0f / H) + a.eps);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 float w[8], o[8];
                 unpack8(prm0[k], w);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = f[k][e] * rstd * w[e];
-                st_stream(a.out0 + row * H + (k * G::NCT + ct) * kVec, pack8(o));
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
         } else if constexpr (OP == kLnFwd) {
-            float f[G::VPT][8];
-            float sm[1] = {0.f};
+            // the row stays packed (bf16) in registers and is widened on each
+            // of the three passes: fewer live registers, same values
+            float v[2] = {0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(v0[k], f[k]);
+                float f[8];
+                unpack8(v0[k], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sm[0] += f[k][e];
+                for (int e = 0; e < 8; ++e) v[0] += f[e];
             }
-            consumer_sum<1>(sm, rb, ct, G::NCW, G::NCT);
-            if (*abort_flag) break;
-            const float mean = sm[0] * (1.0f / H);
+            group_reduce<G::GW, 2>(v, rb0, gwarp, lane, gid);
+            if (v[1] != 0.f) { failed = true; break; }
+            const float mean = v[0] * (1.0f / H);
             float sq[1] = {0.f};
 #pragma unroll
-            for (int k = 0; k < G::VPT; ++k)
+            for (int k = 0; k < G::VPT; ++k) {
+                float f[8];
+                unpack8(v0[k], f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = f[k][e] - mean;
+                    const float d = f[e] - mean;
                     sq[0] += d * d;
                 }
-            consumer_sum<1>(sq, rb + G::NCW, ct, G::NCW, G::NCT);
+            }
+            group_reduce<G::GW, 1>(sq, rb1, gwarp, lane, gid);
             const float rstd = rsqrtf(sq[0] * (1.0f / H) + a.eps);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float g[8], b[8], o[8];
+                float f[8], g[8], b[8], o[8];
+                unpack8(v0[k], f);
                 unpack8(prm0[k], g);
-                unpack8(prm1[k], b);
+                unpack8(ld_param(a.p1 + (k * G::GT + gt) * kVec), b);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (f[k][e] - mean) * rstd * g[e] + b[e];
-                st_stream(a.out0 + row * H + (k * G::NCT + ct) * kVec, pack8(o));
+                for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
-            if (ct == 0) {
+            if (gt == 0) {
                 if (a.mean) a.mean[row] = mean;
                 if (a.rstd) a.rstd[row] = rstd;
             }
         } else {  // kLnBwd
             const float mu = nmu, rs = nrs;
-            if (i + 1 < n) { nmu = __ldg(a.mean + row + 1); nrs = __ldg(a.rstd + row + 1); }
-            float v[2] = {0.f, 0.f};
+            if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
+            float v[3] = {0.f, 0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 float xf[8], df[8], gf[8];
@@ -305,8 +337,8 @@ norm_bulk_kernel(BulkArgs a) {
                     acc_b[k][e] += df[e];
                 }
             }
-            consumer_sum<2>(v, rb, ct, G::NCW, G::NCT);
-            if (*abort_flag) break;
+            group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
+            if (v[2] != 0.f) { failed = true; break; }
             const float A = v[0] * (1.0f / H), B = v[1] * (1.0f / H);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
@@ -316,24 +348,25 @@ norm_bulk_kernel(BulkArgs a) {
                 unpack8(prm0[k], gf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = rs * (df[e] * gf[e] - A - (xf[e] - mu) * rs * B);
-                st_stream(a.out0 + row * H + (k * G::NCT + ct) * kVec, pack8(o));
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
         }
     }
-    if (*abort_flag) {
-        if (ct == 0) record_status(a.status, kStatusTimeout);
+    if (failed) {
+        if (gt == 0) record_status(a.status, kStatusTimeout);
         return;
     }
     if constexpr (OP == kLnBwd) {
-        float* wg = a.ws + static_cast<int64_t>(blockIdx.x) * 2 * H;
+        const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::NG + gid;
+        float* wg = a.ws + slot * 2 * H;
         float* wb = wg + H;
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) {
-            const int j = (k * G::NCT + ct) * kVec;
-            reinterpret_cast<float4*>(wg + j)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
-            reinterpret_cast<float4*>(wg + j)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
-            reinterpret_cast<float4*>(wb + j)[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
-            reinterpret_cast<float4*>(wb + j)[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
+            const int jj = (k * G::GT + gt) * kVec;
+            reinterpret_cast<float4*>(wg + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
+            reinterpret_cast<float4*>(wg + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+            reinterpret_cast<float4*>(wb + jj)[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
+            reinterpret_cast<float4*>(wb + jj)[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
         }
     }
 }
@@ -344,9 +377,9 @@ template <int OP, int H>
 cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
     using G = BGeo<OP, H>;
     // Pick the register-sharing variant only when the launch allocation
-    // covers the split (otherwise setmaxnreg.inc could wait forever).
-    // Per process (the binary is the same on every device); a benign race
-    // at worst repeats the query.  -1 unknown, 0 plain variant, 1 sharing.
+    // covers the split (otherwise setmaxnreg.inc could wait forever) and
+    // the consumers really gain registers.  Per process (the binary is the
+    // same on every device); a benign race at worst repeats the query.
     static int share_ok = -1;
     static bool attr_set[2] = {false, false};
     if (share_ok < 0) {
@@ -355,7 +388,6 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
         if (cudaFuncGetAttributes(&fa, norm_bulk_kernel<OP, H, true>) == cudaSuccess) {
             const long pool = static_cast<long>(fa.numRegs) * G::THREADS;
             const long need = 128L * kProducerRegs + static_cast<long>(G::NCT) * G::CONS_REGS;
-            // only worth it (and only well-formed) when consumers really gain registers
             ok = (fa.numRegs >= kProducerRegs && fa.numRegs < G::CONS_REGS && pool >= need) ? 1 : 0;
         }
         share_ok = ok;
@@ -386,10 +418,11 @@ cudaError_t launch_bulk_op(int64_t hidden, const BulkArgs& a, int grid, cudaStre
 }
 
 template <int OP>
-bool shape_of(int64_t hidden, int* threads, int* stages, int* smem) {
+bool shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* groups) {
     switch (hidden) {
-#define NF_BULK_CASE(HV) \
-        case HV: *threads = BGeo<OP, HV>::THREADS; *stages = BGeo<OP, HV>::S; *smem = BGeo<OP, HV>::SMEM; return true;
+#define NF_BULK_CASE(HV)                                                                \
+        case HV: *threads = BGeo<OP, HV>::THREADS; *stages = BGeo<OP, HV>::S;           \
+                 *smem = BGeo<OP, HV>::SMEM; *groups = BGeo<OP, HV>::NG; return true;
         NF_BULK_CASE(1024) NF_BULK_CASE(2048) NF_BULK_CASE(4096)
         NF_BULK_CASE(5120) NF_BULK_CASE(8192) NF_BULK_CASE(12288)
 #undef NF_BULK_CASE
@@ -399,12 +432,12 @@ bool shape_of(int64_t hidden, int* threads, int* stages, int* smem) {
 
 }  // namespace
 
-bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes) {
+bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups) {
     switch (op) {
-        case kFused: return shape_of<kFused>(hidden, threads, stages, smem_bytes);
-        case kRms: return shape_of<kRms>(hidden, threads, stages, smem_bytes);
-        case kLnFwd: return shape_of<kLnFwd>(hidden, threads, stages, smem_bytes);
-        case kLnBwd: return shape_of<kLnBwd>(hidden, threads, stages, smem_bytes);
+        case kFused: return shape_of<kFused>(hidden, threads, stages, smem_bytes, groups);
+        case kRms: return shape_of<kRms>(hidden, threads, stages, smem_bytes, groups);
+        case kLnFwd: return shape_of<kLnFwd>(hidden, threads, stages, smem_bytes, groups);
+        case kLnBwd: return shape_of<kLnBwd>(hidden, threads, stages, smem_bytes, groups);
         default: return false;
     }
 }

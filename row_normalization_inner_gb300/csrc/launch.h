@@ -14,10 +14,11 @@ namespace nf {
 bool reg_shape(int64_t hidden, int* tpr, int* rpc);
 // Cluster path: CTAs per row (the cluster size) and threads per CTA.
 bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);
-// Bulk path: threads per CTA (one producer warp group + consumers), ring
-// stages and dynamic shared memory for `op` (0 fused, 1 rms, 2 ln fwd,
-// 3 ln bwd, 4 rms bwd).  False if no bulk kernel exists for (op, hidden).
-bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes);
+// Bulk path: threads per CTA (one producer warp group + consumer row
+// groups), ring stages, dynamic shared memory and consumer row groups for
+// `op` (0 fused, 1 rms, 2 ln fwd, 3 ln bwd).  False if no bulk kernel
+// exists for (op, hidden).
+bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups);
 
 // Register path (rows resident in registers).
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
@@ -55,7 +56,8 @@ cudaError_t launch_rms_bulk(int64_t hidden, void* y, const void* x, const void* 
 cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                                const void* gamma, const void* beta, int64_t rows, float eps,
                                int grid, int* status, cudaStream_t st);
-// Stage 1 of LayerNorm backward on the bulk path: one column-partial slot per CTA.
+// Stage 1 of LayerNorm backward on the bulk path: one column-partial slot
+// per consumer row group (grid * groups slots).
 cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st);

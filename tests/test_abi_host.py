@@ -176,10 +176,12 @@ def test_forward_plans(hidden, rows):
         st, bk = nf.nf_plan_compute(op, rows, hidden, sms, "bulk")
         assert st == nf.NF_OK
         assert bk["path"] == "bulk" and bk["cluster"] == 1 and bk["launches"] == 1
-        assert bk["grid"] == min(rows, sms) and bk["block"] % 128 == 0
-        assert (hidden // 8) % (bk["block"] - 128) == 0   # consumers split the row evenly
-        assert 2 <= bk["rows_per_cta"] <= 16               # ring stages
-        assert bk["smem_bytes"] <= 227 * 1024
+        assert bk["grid"] == min(rows, sms) and bk["block"] % 32 == 0
+        groups = bk["rows_per_cta"]                        # consumer row groups
+        assert 1 <= groups <= 16 and (bk["block"] - 128) % groups == 0
+        # each consumer thread of a group holds exactly 4 vectors of the row
+        assert hidden // 8 == 4 * ((bk["block"] - 128) // groups)
+        assert bk["block"] <= 1024 and bk["smem_bytes"] <= 227 * 1024
         st, auto = nf.nf_plan_compute(op, rows, hidden, sms)
         assert st == nf.NF_OK
         want = "cluster" if -(-rows // reg["rows_per_cta"]) * 2 < sms else "reg"
@@ -207,7 +209,8 @@ def test_backward_plans(hidden, rows):
     for sms in (1, 152):
         st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "bulk")
         assert st == nf.NF_OK and p["path"] == "bulk" and p["launches"] == 2
-        assert p["grid"] == min(rows, sms) and p["partials"] == p["grid"]
+        assert p["grid"] == min(rows, sms)
+        assert p["partials"] == p["grid"] * p["rows_per_cta"]
 
 
 def test_plan_invalid_arguments():
