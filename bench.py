@@ -54,6 +54,8 @@ HIDDENS = (4096, 5120, 8192)
 EPS = 1e-5
 DOMINANT_HIDDEN = 8192
 FALLBACK_HBM_GBS = 6800.0
+E2E_CHUNKS = 4
+E2E_STREAMS = 3
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -74,6 +76,11 @@ def ln_bwd_bytes(rows, hidden):
     return (6 * hidden + 8) * rows + 10 * hidden
 
 
+def rms_bwd_bytes(rows, hidden):
+    # read x, dy; write dx; read w once; write dw (fp32) once
+    return 6 * hidden * rows + 6 * hidden
+
+
 # ---------------------------------------------------------------- environment helpers
 
 def measured_peaks():
@@ -84,6 +91,21 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (every rank gets it); `dist` None = one rank."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world, step_bytes, steps, ms):
+    """Whole-job throughput: the bytes every rank moved over the slowest
+    rank's time (weak scaling: each rank runs its own replica)."""
+    return world * step_bytes * steps / (ms * 1e-3) / 1e9
 
 
 def dist_env():
@@ -282,6 +304,8 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         foot, nbytes = 4 * hidden * rows, rms_bytes(rows, hidden)
     elif op == "layernorm_fwd":
         foot, nbytes = (4 * hidden + 8) * rows, ln_fwd_bytes(rows, hidden)
+    elif op == "rmsnorm_bwd":
+        foot, nbytes = 6 * hidden * rows, rms_bwd_bytes(rows, hidden)
     else:
         foot, nbytes = (6 * hidden + 8) * rows, ln_bwd_bytes(rows, hidden)
     sets = max(1, min(16384, -(-2 * l2_bytes // foot)))
@@ -310,6 +334,16 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         fn = lambda i, sh: lib.nf_layernorm_fwd(py + (i % sets) * a2, pm + (i % sets) * rows * 4,  # noqa: E731
                                                  pr + (i % sets) * rows * 4, px + (i % sets) * a2,
                                                  pg, pb, rows, hidden, eps, sh)
+    elif op == "rmsnorm_bwd":
+        x, dy, w = workloads.rms_bwd_inputs(tot, hidden, device=dev)
+        dx = torch.empty_like(x)
+        nws = max(nf.nf_rmsnorm_bwd_workspace_size(rows, hidden), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        dw = torch.empty(hidden, device=dev)
+        px, pdy, pw, pdx, pws, pdw = (t.data_ptr() for t in (x, dy, w, dx, ws, dw))
+        keep = (x, dy, w, dx, ws, dw)
+        fn = lambda i, sh: lib.nf_rmsnorm_bwd(pdx + (i % sets) * a2, pdw, pdy + (i % sets) * a2,  # noqa: E731
+                                               px + (i % sets) * a2, pw, rows, hidden, eps, pws, nws, sh)
     else:
         x, dy, g = workloads.layernorm_bwd_inputs(tot, hidden, device=dev)
         _, m, rs = nf.layernorm_fwd(x, g, torch.zeros_like(g), eps)
@@ -365,6 +399,8 @@ def ops_suite(nf, peak, stream, l2_bytes):
         entry("layernorm_fwd", ROWS, h, EPS)
     for h in (1024, 4096, 8192):
         entry("layernorm_bwd", ROWS, h, EPS)
+    for h in (4096, 8192):
+        entry("rmsnorm_bwd", ROWS, h, EPS)
     return out
 
 
@@ -422,55 +458,76 @@ def run_gpu(args):
         dist.barrier()
     ms_total = start.elapsed_time(end)
     dom_ms = [a.elapsed_time(b) for a, b in dom_events]
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     clocks = sampler.stop(t_begin, t_end) if sampler else None
 
-    value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, args.steps, ms_total)
     dom_avg_ms = sum(dom_ms) / len(dom_ms)
     dom_bytes = fused_bytes(ROWS, DOMINANT_HIDDEN)
     achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9
     dom_path = nf.nf_plan_query("fused_add_rmsnorm", ROWS, DOMINANT_HIDDEN)["path"]
     traffic = _profiled_traffic("fused_add_rmsnorm", dom_path, ROWS, DOMINANT_HIDDEN)
 
-    # end to end through the C ABI with pinned host buffers
+    # end to end through the C ABI with pinned host buffers: every step copies
+    # x and residual in from pinned host memory, runs the call and copies both
+    # results back.  Rows are independent, so each hidden size's batch is cut
+    # into E2E_CHUNKS row chunks spread over E2E_STREAMS streams (a fixed
+    # chunk -> stream map), and host->device copies, kernels and
+    # device->host copies of different chunks overlap.
     e2e = None
     if not args.no_e2e:
         hosts = [(x.cpu().pin_memory(), r.cpu().pin_memory()) for (x, r, _) in sets]
         outs = [(torch.empty_like(hx).pin_memory(), torch.empty_like(hr).pin_memory()) for hx, hr in hosts]
         h2d = sum(hx.numel() * 2 + hr.numel() * 2 for hx, hr in hosts)
         d2h = h2d
+        streams = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
+        work = []
+        cr = ROWS // E2E_CHUNKS
+        for (hx, hr), (ox, orr), (x, r, w) in zip(hosts, outs, sets):
+            for c in range(E2E_CHUNKS):
+                sl = slice(c * cr, (c + 1) * cr)
+                work.append((hx[sl], hr[sl], ox[sl], orr[sl], x[sl], r[sl], w))
 
         def e2e_step():
-            for (hx, hr), (ox, orr), (x, r, w) in zip(hosts, outs, sets):
-                x.copy_(hx, non_blocking=True)
-                r.copy_(hr, non_blocking=True)
-                nf.fused_add_rmsnorm(x, r, w, EPS, stream=stream)
-                ox.copy_(x, non_blocking=True)
-                orr.copy_(r, non_blocking=True)
-        e2e_steps = max(3, min(args.steps // 20, 50))
-        with torch.cuda.stream(stream):
-            e2e_step()
-            torch.cuda.synchronize()
-            if dist is not None:
-                dist.barrier()
+            for k, (hx, hr, ox, orr, x, r, w) in enumerate(work):
+                s = streams[k % E2E_STREAMS]
+                with torch.cuda.stream(s):
+                    x.copy_(hx, non_blocking=True)
+                    r.copy_(hr, non_blocking=True)
+                    nf.fused_add_rmsnorm(x, r, w, EPS, stream=s)
+                    ox.copy_(x, non_blocking=True)
+                    orr.copy_(r, non_blocking=True)
+
+        def timed(nsteps):
             a, b = _ev(), _ev()
             a.record(stream)
-            for _ in range(e2e_steps):
+            for s in streams:
+                s.wait_event(a)
+            for _ in range(nsteps):
                 e2e_step()
+            for s in streams:
+                ev = _ev()
+                ev.record(s)
+                stream.wait_event(ev)
             b.record(stream)
             b.synchronize()
-        e_ms = a.elapsed_time(b)
+            return a.elapsed_time(b)
+
+        e2e_steps = max(3, min(args.steps // 20, 50))
+        timed(1)
+        torch.cuda.synchronize()
         if dist is not None:
-            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * step_bytes * e2e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            dist.barrier()
+        e_ms = timed(e2e_steps)
+        e_ms = max_over_ranks(e_ms, dist, dev)
+        # check once that the round trip really returned the device results
+        torch.cuda.synchronize()
+        assert torch.equal(outs[-1][0][-1], sets[-1][0][-1].cpu())
+        e2e = {"value": round(whole_job_gbs(world, step_bytes, e2e_steps, e_ms), 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "ms_per_step": round(e_ms / e2e_steps, 3)}
-        del hosts, outs
+               "ms_per_step": round(e_ms / e2e_steps, 3),
+               "pipeline": f"{E2E_CHUNKS} row chunks per hidden size over {E2E_STREAMS} streams"}
+        del hosts, outs, work
 
     ops = None
     if rank == 0 and not args.no_ops:

@@ -27,9 +27,11 @@
  *           device (or managed memory).  bf16 pointers, dgamma, dbeta and
  *           the workspace must be 16-byte aligned; mean/rstd 4-byte
  *           aligned.  Null pointers are accepted only when rows == 0.
- * hidden.   Must be one of the compiled sizes: 1024, 2048, 4096, 5120,
- *           8192, 12288 (kernels are specialized per size; other values
- *           return NF_ERR_UNSUPPORTED_HIDDEN).
+ * hidden.   The compiled sizes 1024, 2048, 4096, 5120, 8192, 12288 get
+ *           kernels specialized per size.  Any other multiple of 8 up to
+ *           32768 (forward ops) or 16384 (backward ops) runs on the
+ *           runtime-hidden kernels (NF_PATH_DYNAMIC).  Other values return
+ *           NF_ERR_UNSUPPORTED_HIDDEN.
  * rows.     Any value >= 0; rows == 0 returns NF_OK without launching.
  * eps.      Finite and > 0.
  * Stream.   Work is enqueued on `stream` (NULL = the legacy default
@@ -82,12 +84,18 @@ typedef struct CUstream_st* nf_stream;
  *   BULK    -- a producer warp stages rows into a shared-memory ring with
  *              bulk asynchronous copies; consumer warps read 128-bit vectors
  *              from shared memory; registers move from producer to
- *              consumers ("TMA inner persistent scheduler").               */
+ *              consumers ("TMA inner persistent scheduler").
+ *   DYNAMIC -- the hidden size is a runtime argument (any multiple of 8 up
+ *              to 32768 forward, 16384 backward); the row still sits in
+ *              registers under a compile-time per-thread bound ("TMA inner
+ *              persistent scheduler": dynamic block dimensions).  The only
+ *              family for hidden sizes outside the compiled set.           */
 typedef enum {
     NF_PATH_AUTO = 0,
     NF_PATH_REG = 1,
     NF_PATH_CLUSTER = 2,
-    NF_PATH_BULK = 3
+    NF_PATH_BULK = 3,
+    NF_PATH_DYNAMIC = 4
 } nf_path;
 
 /* Operation ids for nf_plan_query. */
@@ -160,6 +168,26 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta,
                            const void* dy, const void* x, const float* mean, const float* rstd,
                            const void* gamma, int64_t rows, int64_t hidden,
                            void* workspace, size_t workspace_bytes, nf_stream stream);
+
+/* Bytes of workspace nf_rmsnorm_bwd needs for (rows, hidden) on the current
+ * device, under any kernel family (same rules as the LayerNorm query). */
+size_t nf_rmsnorm_bwd_workspace_size(int64_t rows, int64_t hidden);
+
+/* RMSNorm backward (the RMS counterpart of the combined inner + outer
+ * reduction of "Llu/ln bwd"; "TMA inner persistent scheduler": RMS norm
+ * "with workspace support").  For y = x * rstd * w with
+ * rstd = rsqrt(mean_k(x_k^2) + eps), g = dy * w and xhat = x * rstd:
+ *   inner (per row):    dx[r][j] = bf16( rstd * ( g_j - xhat_j * mean_k(g_k * xhat_k) ) )
+ *   outer (per column): dw[j]    = sum_r dy[r][j] * xhat[r][j]          (fp32, overwritten)
+ * rstd is recomputed from x inside the kernel (one more sum in the same
+ * row reduction, no extra memory traffic), so the forward need not save
+ * it; pass the forward's eps.  The column sums go through `workspace` in
+ * two fixed-order stages (deterministic).  dx may be dy or x itself.
+ * rows == 0 sets dw (if not NULL) to 0.  Same pointer, alignment and
+ * workspace rules as nf_layernorm_bwd. */
+nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, const void* weight,
+                         int64_t rows, int64_t hidden, float eps, void* workspace,
+                         size_t workspace_bytes, nf_stream stream);
 
 /* Force a kernel family for every later call in this process (NF_PATH_AUTO
  * restores the library's choice).  A call whose op/size has no kernel of the

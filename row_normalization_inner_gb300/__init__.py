@@ -31,8 +31,9 @@ NF_ERR_CUDA = 5
 NF_ERR_TIMEOUT = 6
 NF_ERR_UNSUPPORTED_PATH = 7
 
-NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK = 0, 1, 2, 3
-PATHS = {"auto": NF_PATH_AUTO, "reg": NF_PATH_REG, "cluster": NF_PATH_CLUSTER, "bulk": NF_PATH_BULK}
+NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK, NF_PATH_DYNAMIC = 0, 1, 2, 3, 4
+PATHS = {"auto": NF_PATH_AUTO, "reg": NF_PATH_REG, "cluster": NF_PATH_CLUSTER, "bulk": NF_PATH_BULK,
+         "dynamic": NF_PATH_DYNAMIC}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 NF_OP_FUSED_ADD_RMSNORM, NF_OP_RMSNORM_FWD, NF_OP_LAYERNORM_FWD, NF_OP_LAYERNORM_BWD, \
@@ -40,12 +41,15 @@ NF_OP_FUSED_ADD_RMSNORM, NF_OP_RMSNORM_FWD, NF_OP_LAYERNORM_FWD, NF_OP_LAYERNORM
 OPS = {"fused_add_rmsnorm": 0, "rmsnorm_fwd": 1, "layernorm_fwd": 2, "layernorm_bwd": 3,
        "rmsnorm_bwd": 4}
 
-HIDDEN_SET = (1024, 2048, 4096, 5120, 8192, 12288)
+HIDDEN_SET = (1024, 2048, 4096, 5120, 8192, 12288)   # compiled sizes
+DYN_MAX_HIDDEN_FWD = 32768    # runtime-hidden path: any multiple of 8 up to these
+DYN_MAX_HIDDEN_BWD = 16384
 
 # Every symbol include/nf.h declares.
 EXPORTS = (
     "nf_fused_add_rmsnorm", "nf_rmsnorm_fwd", "nf_layernorm_fwd",
     "nf_layernorm_bwd_workspace_size", "nf_layernorm_bwd",
+    "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
     "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
 )
@@ -85,6 +89,8 @@ def _bind(lib):
         "nf_layernorm_fwd": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
         "nf_layernorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
         "nf_layernorm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
+        "nf_rmsnorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+        "nf_rmsnorm_bwd": (_S, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_set_path": (_S, [_S]),
         "nf_plan_query": (_S, [_S, _I64, _I64, ctypes.POINTER(Plan)]),
         "nf_plan_compute": (_S, [_S, _I64, _I64, ctypes.c_int32, _S, ctypes.POINTER(Plan)]),
@@ -143,6 +149,16 @@ def nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, 
                      workspace_bytes, stream) -> int:
     return lib().nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
                                   workspace, workspace_bytes, stream)
+
+
+def nf_rmsnorm_bwd_workspace_size(rows, hidden) -> int:
+    return lib().nf_rmsnorm_bwd_workspace_size(rows, hidden)
+
+
+def nf_rmsnorm_bwd(dx, dw, dy, x, weight, rows, hidden, eps, workspace, workspace_bytes,
+                   stream) -> int:
+    return lib().nf_rmsnorm_bwd(dx, dw, dy, x, weight, rows, hidden, eps, workspace,
+                                workspace_bytes, stream)
 
 
 def nf_set_path(path) -> int:
@@ -271,6 +287,24 @@ def layernorm_bwd(dy, x, mean, rstd, gamma, workspace=None, out=None, stream=Non
                             hidden, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                             _stream(stream)), "nf_layernorm_bwd")
     return dx, dgamma, dbeta
+
+
+def rmsnorm_bwd(dy, x, weight, eps: float = 1e-6, workspace=None, out=None, stream=None):
+    """Returns (dx bf16, dw fp32).  rstd is recomputed from x in the kernel."""
+    import torch
+    for t, n in ((dy, "dy"), (x, "x"), (weight, "weight")):
+        _need(t, torch.bfloat16, n)
+    rows, hidden = _rows_hidden(x)
+    dx = torch.empty_like(x) if out is None else out
+    dw = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    need = nf_rmsnorm_bwd_workspace_size(rows, hidden)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(nf_rmsnorm_bwd(dx.data_ptr(), dw.data_ptr(), dy.data_ptr(), x.data_ptr(),
+                          weight.data_ptr(), rows, hidden, eps, workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), _stream(stream)),
+           "nf_rmsnorm_bwd")
+    return dx, dw
 
 
 def set_path(path):

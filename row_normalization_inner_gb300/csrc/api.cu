@@ -59,14 +59,22 @@ bool prefer_cluster(int64_t rows, int rpc, int sms) {
 
 // The library's own path choice.  Forward ops: a row goes to a cluster
 // when one CTA per row group would occupy fewer than half of the SMs;
-// otherwise the register path.  Backward: the register path.
+// otherwise the register path.  Backward ops: the bulk path, whose ring
+// keeps many rows in flight while the consumers hold the column
+// accumulators in registers.
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
     (void)hidden;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    if (fwd && prefer_cluster(rows, rpc, sms)) return NF_PATH_CLUSTER;
+    if (!fwd) return NF_PATH_BULK;
+    if (prefer_cluster(rows, rpc, sms)) return NF_PATH_CLUSTER;
     return NF_PATH_REG;
 }
+
+// Column-partial planes a backward op keeps per slot (LayerNorm: dgamma and
+// dbeta; RMSNorm: dw).
+int bwd_planes(nf_op op) { return op == NF_OP_LAYERNORM_BWD ? 2 : 1; }
+
 
 std::atomic<int> g_forced_path{NF_PATH_AUTO};
 
@@ -107,9 +115,16 @@ nf_status device_status_addr(int** addr) {
     return NF_OK;
 }
 
+// A size with kernels specialized at compile time.
 bool hidden_ok(int64_t h) {
     int a, b;
     return reg_shape(h, &a, &b);
+}
+
+// A size some kernel of `op` handles (compiled, or the runtime-hidden path).
+bool hidden_supported(nf_op op, int64_t h) {
+    int t;
+    return hidden_ok(h) || dyn_shape(op, h, &t);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -131,8 +146,8 @@ bool bad_overlap_except_alias(Span out, Span in) {
     return overlap(out, in);
 }
 
-nf_status common_checks(int64_t rows, int64_t hidden, float eps, bool check_eps) {
-    if (!hidden_ok(hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
+nf_status common_checks(nf_op op, int64_t rows, int64_t hidden, float eps, bool check_eps) {
+    if (!hidden_supported(op, hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
     if (rows < 0) return NF_ERR_INVALID_ARG;
     // keep rows * hidden * 4 bytes representable
     if (rows > (INT64_MAX / 8) / hidden) return NF_ERR_INVALID_ARG;
@@ -147,6 +162,23 @@ nf_status plan_for_call(nf_op op, int64_t rows, int64_t hidden, nf_plan* plan) {
     if (nf_status st = device_sm_count(&sms)) return st;
     return nf_plan_compute(op, rows, hidden, sms,
                            static_cast<nf_path>(g_forced_path.load(std::memory_order_relaxed)), plan);
+}
+
+size_t bwd_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
+    if (!hidden_supported(op, hidden) || rows <= 0) return 0;
+    int sms;
+    if (device_sm_count(&sms) != NF_OK) return 0;
+    // enough for every backward path, so a later nf_set_path cannot make a
+    // previously sized workspace too small
+    size_t most = 0;
+    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC}) {
+        nf_plan pl;
+        if (nf_plan_compute(op, rows, hidden, sms, p, &pl) != NF_OK) continue;
+        const size_t b = static_cast<size_t>(pl.partials) * bwd_planes(op) *
+                         static_cast<size_t>(hidden) * sizeof(float);
+        if (b > most) most = b;
+    }
+    return most;
 }
 
 // The selftest kernel: one thread waits on a barrier nothing will complete.
@@ -179,15 +211,18 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
                           nf_plan* out) {
     if (!out || rows < 0 || sm_count < 1) return NF_ERR_INVALID_ARG;
     if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return NF_ERR_INVALID_ARG;
-    if (path < NF_PATH_AUTO || path > NF_PATH_BULK) return NF_ERR_INVALID_ARG;
-    int tpr, rpc;
-    if (!reg_shape(hidden, &tpr, &rpc)) return NF_ERR_UNSUPPORTED_HIDDEN;
+    if (path < NF_PATH_AUTO || path > NF_PATH_DYNAMIC) return NF_ERR_INVALID_ARG;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    if (op == NF_OP_RMSNORM_BWD) return NF_ERR_UNSUPPORTED_PATH;  // no kernel yet
+    int tpr = 0, rpc = 1, dyn_threads = 0;
+    const bool compiled = reg_shape(hidden, &tpr, &rpc);
+    const bool dyn_ok = dyn_shape(op, hidden, &dyn_threads);
+    if (!compiled && !dyn_ok) return NF_ERR_UNSUPPORTED_HIDDEN;
 
     nf_path p = path;
-    if (p == NF_PATH_AUTO) p = auto_path(op, rows, hidden, rpc, sm_count);
+    if (p == NF_PATH_AUTO) p = compiled ? auto_path(op, rows, hidden, rpc, sm_count) : NF_PATH_DYNAMIC;
+    if (p != NF_PATH_DYNAMIC && !compiled) return NF_ERR_UNSUPPORTED_PATH;
+    if (p == NF_PATH_DYNAMIC && !dyn_ok) return NF_ERR_UNSUPPORTED_PATH;
     if (p == NF_PATH_CLUSTER && !fwd) return NF_ERR_UNSUPPORTED_PATH;
 
     nf_plan pl;
@@ -211,6 +246,22 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.cluster = c;
         pl.rows_per_cta = 1;
         pl.launches = 1;
+    } else if (p == NF_PATH_DYNAMIC) {
+        pl.block = dyn_threads;
+        pl.cluster = 1;
+        pl.rows_per_cta = 1;
+        if (fwd) {
+            pl.grid = static_cast<int32_t>(rows < kMaxGrid ? rows : kMaxGrid);
+            pl.launches = 1;
+        } else {
+            const int64_t per_sm = 1024 / dyn_threads > 0 ? 1024 / dyn_threads : 1;
+            const int64_t resident = static_cast<int64_t>(sm_count) * per_sm;
+            int64_t g = rows < resident ? rows : resident;
+            if (g < 1) g = 1;
+            pl.grid = static_cast<int32_t>(g);
+            pl.launches = 2;
+            pl.partials = static_cast<int32_t>(g);
+        }
     } else if (p == NF_PATH_BULK) {
         int threads, stages, smem, groups;
         if (!bulk_shape(op, hidden, &threads, &stages, &smem, &groups)) return NF_ERR_UNSUPPORTED_PATH;
@@ -240,21 +291,22 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
 }
 
 nf_status nf_set_path(nf_path path) {
-    if (path < NF_PATH_AUTO || path > NF_PATH_BULK) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_DYNAMIC) return NF_ERR_INVALID_ARG;
     g_forced_path.store(path, std::memory_order_relaxed);
     return NF_OK;
 }
 
 nf_status nf_plan_query(nf_op op, int64_t rows, int64_t hidden, nf_plan* out) {
     if (!out) return NF_ERR_INVALID_ARG;
-    if (!hidden_ok(hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
+    if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return NF_ERR_INVALID_ARG;
+    if (!hidden_supported(op, hidden)) return NF_ERR_UNSUPPORTED_HIDDEN;
     if (rows < 0) return NF_ERR_INVALID_ARG;
     return plan_for_call(op, rows, hidden, out);
 }
 
 nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int64_t rows,
                                int64_t hidden, float eps, nf_stream stream) {
-    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (nf_status st = common_checks(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!x || !residual || !weight) return NF_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16)) return NF_ERR_MISALIGNED;
@@ -267,6 +319,18 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
+    if (pl.path == NF_PATH_DYNAMIC) {
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(x);
+        a.out1 = static_cast<uint16_t*>(residual);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.in1 = static_cast<const uint16_t*>(residual);
+        a.p0 = static_cast<const uint16_t*>(weight);
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        return from_cuda(launch_dyn(NF_OP_FUSED_ADD_RMSNORM, a, pl.grid, s));
+    }
     if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
@@ -277,7 +341,7 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
 
 nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t rows, int64_t hidden,
                          float eps, nf_stream stream) {
-    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (nf_status st = common_checks(NF_OP_RMSNORM_FWD, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!y || !x || !weight) return NF_ERR_INVALID_ARG;
     if (!aligned(y, 16) || !aligned(x, 16) || !aligned(weight, 16)) return NF_ERR_MISALIGNED;
@@ -289,6 +353,16 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
+    if (pl.path == NF_PATH_DYNAMIC) {
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(y);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.p0 = static_cast<const uint16_t*>(weight);
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        return from_cuda(launch_dyn(NF_OP_RMSNORM_FWD, a, pl.grid, s));
+    }
     if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
@@ -300,7 +374,7 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
 nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                            const void* beta, int64_t rows, int64_t hidden, float eps,
                            nf_stream stream) {
-    if (nf_status st = common_checks(rows, hidden, eps, true)) return st;
+    if (nf_status st = common_checks(NF_OP_LAYERNORM_FWD, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!y || !x || !gamma || !beta) return NF_ERR_INVALID_ARG;
     if (!aligned(y, 16) || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(beta, 16))
@@ -320,6 +394,19 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
     if (pl.path == NF_PATH_CLUSTER)
         return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
                                                pl.grid, s));
+    if (pl.path == NF_PATH_DYNAMIC) {
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(y);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.p0 = static_cast<const uint16_t*>(gamma);
+        a.p1 = static_cast<const uint16_t*>(beta);
+        a.mean = mean;
+        a.rstd = rstd;
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        return from_cuda(launch_dyn(NF_OP_LAYERNORM_FWD, a, pl.grid, s));
+    }
     if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
@@ -330,26 +417,14 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
 }
 
 size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
-    if (!hidden_ok(hidden) || rows <= 0) return 0;
-    int sms;
-    if (device_sm_count(&sms) != NF_OK) return 0;
-    // enough for every backward path, so a later nf_set_path cannot make a
-    // previously sized workspace too small
-    size_t most = 0;
-    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK}) {
-        nf_plan pl;
-        if (nf_plan_compute(NF_OP_LAYERNORM_BWD, rows, hidden, sms, p, &pl) != NF_OK) continue;
-        const size_t b = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
-        if (b > most) most = b;
-    }
-    return most;
+    return bwd_workspace_bytes(NF_OP_LAYERNORM_BWD, rows, hidden);
 }
 
 nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                            const float* mean, const float* rstd, const void* gamma, int64_t rows,
                            int64_t hidden, void* workspace, size_t workspace_bytes,
                            nf_stream stream) {
-    if (nf_status st = common_checks(rows, hidden, 0.f, false)) return st;
+    if (nf_status st = common_checks(NF_OP_LAYERNORM_BWD, rows, hidden, 0.f, false)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (rows == 0) {
         // an empty sum: dgamma = dbeta = 0
@@ -383,7 +458,19 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
             return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_BULK) {
+    if (pl.path == NF_PATH_DYNAMIC) {
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(dx);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.in1 = static_cast<const uint16_t*>(dy);
+        a.p0 = static_cast<const uint16_t*>(gamma);
+        a.mean = const_cast<float*>(mean);
+        a.rstd = const_cast<float*>(rstd);
+        a.ws = ws;
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        if (cudaError_t e = launch_dyn(NF_OP_LAYERNORM_BWD, a, pl.grid, s)) return from_cuda(e);
+    } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
         if (cudaError_t e = launch_ln_bwd_bulk(hidden, dx, ws, dy, x, mean, rstd, gamma, rows,
@@ -394,6 +481,64 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         return from_cuda(e);
     }
     return from_cuda(launch_column_reduce(ws, dgamma, dbeta, pl.partials, hidden, s));
+}
+
+size_t nf_rmsnorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
+    return bwd_workspace_bytes(NF_OP_RMSNORM_BWD, rows, hidden);
+}
+
+nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, const void* weight,
+                         int64_t rows, int64_t hidden, float eps, void* workspace,
+                         size_t workspace_bytes, nf_stream stream) {
+    if (nf_status st = common_checks(NF_OP_RMSNORM_BWD, rows, hidden, eps, true)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {
+        // an empty sum: dw = 0
+        if (dw && !aligned(dw, 16)) return NF_ERR_MISALIGNED;
+        if (dw && cudaMemsetAsync(dw, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
+        return NF_OK;
+    }
+    if (!dx || !dw || !dy || !x || !weight || !workspace) return NF_ERR_INVALID_ARG;
+    if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
+        !aligned(workspace, 16) || !aligned(dw, 16))
+        return NF_ERR_MISALIGNED;
+    nf_plan pl;
+    if (nf_status st = plan_for_call(NF_OP_RMSNORM_BWD, rows, hidden, &pl)) return st;
+    const size_t need = static_cast<size_t>(pl.partials) * static_cast<size_t>(hidden) * sizeof(float);
+    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t act = rows * hidden * 2, par = hidden * 2, grad = hidden * 4;
+    const Span sdx{dx, act}, sdw{dw, grad}, sws{workspace, static_cast<int64_t>(need)};
+    const Span ins[] = {{dy, act}, {x, act}, {weight, par}};
+    if (overlap(sdx, sdw) || overlap(sws, sdx) || overlap(sws, sdw)) return NF_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i) {
+        const Span& in = ins[i];
+        // dx may be exactly dy or x (each row is read before it is written)
+        const bool dx_clash = i < 2 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
+        if (dx_clash || overlap(sdw, in) || overlap(sws, in)) return NF_ERR_INVALID_ARG;
+    }
+    float* ws = static_cast<float*>(workspace);
+    if (pl.path == NF_PATH_DYNAMIC) {
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(dx);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.in1 = static_cast<const uint16_t*>(dy);
+        a.p0 = static_cast<const uint16_t*>(weight);
+        a.ws = ws;
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        if (cudaError_t e = launch_dyn(NF_OP_RMSNORM_BWD, a, pl.grid, s)) return from_cuda(e);
+    } else if (pl.path == NF_PATH_BULK) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        if (cudaError_t e = launch_rms_bwd_bulk(hidden, dx, ws, dy, x, weight, rows, eps, pl.grid,
+                                                status, s))
+            return from_cuda(e);
+    } else if (cudaError_t e = launch_rms_bwd_reg(hidden, dx, ws, dy, x, weight, rows, eps,
+                                                  pl.grid, s)) {
+        return from_cuda(e);
+    }
+    return from_cuda(launch_column_reduce1(ws, dw, pl.partials, hidden, s));
 }
 
 nf_status nf_get_device_status(nf_stream stream) {

@@ -13,7 +13,7 @@
 // stage's barrier phases and the group's row sequence move in lockstep and
 // a parity wait can never match a phase from an earlier use).  A group
 // waits on its row's "full" barrier, reads the row from shared memory with
-// 128-bit loads into registers (4 vectors of 8 bf16 per thread), releases the
+// 128-bit loads into registers (4 or 5 vectors of 8 bf16 per thread), releases the
 // stage on its
 // "empty" mbarrier at once (so the next copy starts while it computes),
 // reduces the row within the group (warp shuffles, then a named barrier
@@ -37,16 +37,25 @@
 
 namespace nf {
 
-enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3 };
+enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3, kRmsBwd = 4 };
 
-// Row-group shape: GW warps per row (so each thread holds 4 vectors of its
-// row) and NG concurrent row groups per CTA.
+// Row-group shape: GW warps per row and NG concurrent row groups per CTA.
+// Every shape makes the consumer warps a whole number of warp groups (the
+// CTA is then 128 * k threads), which setmaxnreg requires: it is executed
+// by all four warps of a warp group together, so a partial warp group
+// would wait forever.
+template <int H> struct BulkRow;                        // GW, fwd NG, bwd NG
+template <> struct BulkRow<1024>  { static constexpr int GW = 1,  NGF = 16, NGB = 8; };
+template <> struct BulkRow<2048>  { static constexpr int GW = 2,  NGF = 8,  NGB = 4; };
+template <> struct BulkRow<4096>  { static constexpr int GW = 4,  NGF = 4,  NGB = 2; };
+template <> struct BulkRow<5120>  { static constexpr int GW = 4,  NGF = 4,  NGB = 2; };  // 5 vectors/thread
+template <> struct BulkRow<8192>  { static constexpr int GW = 8,  NGF = 2,  NGB = 1; };
+template <> struct BulkRow<12288> { static constexpr int GW = 12, NGF = 1,  NGB = 1; };
+
 template <int OP, int H>
 struct BulkShape {
-    static constexpr int GW = H / kVec / 4 / 32;
-    static constexpr int NG_FWD = (H >= 12288) ? 1 : (16 / GW > 0 ? 16 / GW : 1);
-    static constexpr int NG_BWD = (GW >= 5) ? 1 : 8 / GW;
-    static constexpr int NG = OP == 3 ? NG_BWD : NG_FWD;
+    static constexpr int GW = BulkRow<H>::GW;
+    static constexpr int NG = (OP == 3 || OP == 4) ? BulkRow<H>::NGB : BulkRow<H>::NGF;
 };
 
 constexpr int kSmemBudget = 200 * 1024;  // ring + barriers + reduction scratch
@@ -54,7 +63,7 @@ constexpr int kMaxStagesPerGroup = 8;
 constexpr int kProducerRegs = 40;
 
 template <int OP> struct OpIO {
-    static constexpr int NIN = (OP == kFused || OP == kLnBwd) ? 2 : 1;  // staged tensors per row
+    static constexpr int NIN = (OP == kFused || OP == kLnBwd || OP == kRmsBwd) ? 2 : 1;  // staged tensors per row
 };
 
 template <int OP, int H>
@@ -66,8 +75,9 @@ struct BGeo {
     static constexpr int THREADS = 128 + NCT;
     static constexpr int NV = H / kVec;
     static constexpr int VPT = NV / GT;
-    static_assert(NV % GT == 0 && VPT == 4, "four vectors per consumer thread");
+    static_assert(NV % GT == 0 && VPT >= 1, "whole vectors per consumer thread");
     static_assert(THREADS <= 1024, "CTA size");
+    static_assert(THREADS % 128 == 0, "whole warp groups (setmaxnreg)");
     static_assert(GW == 1 || NG <= 15, "named barriers 1..NG");
     static constexpr int ROW_BYTES = H * 2;
     static constexpr int STAGE_BYTES = ROW_BYTES * OpIO<OP>::NIN;
@@ -133,12 +143,12 @@ struct BulkArgs {
     uint16_t* out0;          // fused: x (in place); rms/ln fwd: y; ln bwd: dx
     uint16_t* out1;          // fused: residual (in place)
     const uint16_t* in0;     // fused: x; rms/ln: x; ln bwd: x
-    const uint16_t* in1;     // fused: residual; ln bwd: dy
+    const uint16_t* in1;     // fused: residual; ln/rms bwd: dy
     const uint16_t* p0;      // weight / gamma
     const uint16_t* p1;      // beta
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
-    float* ws;               // ln bwd column partials [grid * NG][2][H]
+    float* ws;               // bwd column partials [grid * NG][planes][H]
     int* status;
     int64_t rows;
     float eps;
@@ -212,12 +222,19 @@ norm_bulk_kernel(BulkArgs a) {
     for (int k = 0; k < G::VPT; ++k) {
         prm0[k] = ld_param(a.p0 + (k * G::GT + gt) * kVec);
     }
-    float acc_g[OP == kLnBwd ? G::VPT : 1][8], acc_b[OP == kLnBwd ? G::VPT : 1][8];
+    constexpr bool kBwd = OP == kLnBwd || OP == kRmsBwd;
+    float acc_g[kBwd ? G::VPT : 1][8], acc_b[OP == kLnBwd ? G::VPT : 1][8];
+    if constexpr (kBwd) {
+#pragma unroll
+        for (int k = 0; k < G::VPT; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc_g[k][e] = 0.f;
+    }
     if constexpr (OP == kLnBwd) {
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) { acc_g[k][e] = 0.f; acc_b[k][e] = 0.f; }
+            for (int e = 0; e < 8; ++e) acc_b[k][e] = 0.f;
     }
     // saved statistics of the group's next row, fetched one row ahead
     float nmu = 0.f, nrs = 0.f;
@@ -317,6 +334,39 @@ norm_bulk_kernel(BulkArgs a) {
                 if (a.mean) a.mean[row] = mean;
                 if (a.rstd) a.rstd[row] = rstd;
             }
+        } else if constexpr (OP == kRmsBwd) {
+            // rstd recomputed from the row: rs = rsqrt(sum x^2 / H + eps),
+            // dx = rs * g - x * rs^3 * sum(g x) / H with g = dy * w
+            float v[3] = {0.f, 0.f, fail};
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], wf[8];
+                unpack8(v0[k], xf);
+                unpack8(v1[k], df);
+                unpack8(prm0[k], wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    v[0] += xf[e] * xf[e];
+                    v[1] += df[e] * wf[e] * xf[e];
+                }
+            }
+            group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
+            if (v[2] != 0.f) { failed = true; break; }
+            const float rs = rsqrtf(v[0] * (1.0f / H) + a.eps);
+            const float c = rs * rs * rs * v[1] * (1.0f / H);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], wf[8], o[8];
+                unpack8(v0[k], xf);
+                unpack8(v1[k], df);
+                unpack8(prm0[k], wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    o[e] = rs * df[e] * wf[e] - xf[e] * c;
+                    acc_g[k][e] += df[e] * xf[e] * rs;
+                }
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
+            }
         } else {  // kLnBwd
             const float mu = nmu, rs = nrs;
             if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
@@ -356,6 +406,16 @@ norm_bulk_kernel(BulkArgs a) {
         if (gt == 0) record_status(a.status, kStatusTimeout);
         return;
     }
+    if constexpr (OP == kRmsBwd) {
+        const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::NG + gid;
+        float* wg = a.ws + slot * H;
+#pragma unroll
+        for (int k = 0; k < G::VPT; ++k) {
+            const int jj = (k * G::GT + gt) * kVec;
+            reinterpret_cast<float4*>(wg + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
+            reinterpret_cast<float4*>(wg + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+        }
+    }
     if constexpr (OP == kLnBwd) {
         const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::NG + gid;
         float* wg = a.ws + slot * 2 * H;
@@ -388,7 +448,8 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
         if (cudaFuncGetAttributes(&fa, norm_bulk_kernel<OP, H, true>) == cudaSuccess) {
             const long pool = static_cast<long>(fa.numRegs) * G::THREADS;
             const long need = 128L * kProducerRegs + static_cast<long>(G::NCT) * G::CONS_REGS;
-            ok = (fa.numRegs >= kProducerRegs && fa.numRegs < G::CONS_REGS && pool >= need) ? 1 : 0;
+            ok = (G::THREADS % 128 == 0 && fa.numRegs >= kProducerRegs &&
+                  fa.numRegs < G::CONS_REGS && pool >= need) ? 1 : 0;
         }
         share_ok = ok;
     }
@@ -438,6 +499,7 @@ bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_byt
         case kRms: return shape_of<kRms>(hidden, threads, stages, smem_bytes, groups);
         case kLnFwd: return shape_of<kLnFwd>(hidden, threads, stages, smem_bytes, groups);
         case kLnBwd: return shape_of<kLnBwd>(hidden, threads, stages, smem_bytes, groups);
+        case kRmsBwd: return shape_of<kRmsBwd>(hidden, threads, stages, smem_bytes, groups);
         default: return false;
     }
 }
@@ -498,6 +560,21 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* 
     a.status = status;
     a.rows = rows;
     return launch_bulk_op<kLnBwd>(hidden, a, grid, st);
+}
+
+cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                                const void* w, int64_t rows, float eps, int grid, int* status,
+                                cudaStream_t st) {
+    BulkArgs a{};
+    a.out0 = static_cast<uint16_t*>(dx);
+    a.in0 = static_cast<const uint16_t*>(x);
+    a.in1 = static_cast<const uint16_t*>(dy);
+    a.p0 = static_cast<const uint16_t*>(w);
+    a.ws = ws;
+    a.status = status;
+    a.rows = rows;
+    a.eps = eps;
+    return launch_bulk_op<kRmsBwd>(hidden, a, grid, st);
 }
 
 }  // namespace nf

@@ -120,19 +120,102 @@ layernorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, cons
     }
 }
 
-// dgamma[j] = sum_{slot} ws[slot][0][j], dbeta[j] = sum_{slot} ws[slot][1][j],
-// in a fixed order: thread row ty sums slots ty, ty+8, ty+16, ... and the 8
-// row sums are then added in ty order.  Each thread owns 4 adjacent columns
-// of the [2][H] plane (float4 loads, coalesced across the warp).
+// RMSNorm backward, stage 1 (register path), same stripes and slots as the
+// LayerNorm kernel above.  rstd is recomputed from the resident row (one
+// more sum in the same reduction), so the forward need not save it:
+//     rstd = rsqrt(sum_j x_j^2 / H + eps),  g = dy * w,  P = sum_j g_j x_j
+//     dx_j = rstd * g_j - x_j * rstd^3 * P / H     (= rstd * (g_j - xhat_j * mean(g * xhat)))
+//     acc_w_j += dy_j * x_j * rstd                  -> ws[slot][0][:]
+template <int H>
+__global__ void __launch_bounds__(BGeo<H>::TPR * BGeo<H>::RPC)
+rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const uint16_t* x,
+                const uint16_t* __restrict__ w, int64_t rows, float eps) {
+    using G = BGeo<H>;
+    __shared__ float red[2][G::RPC * G::W * 2];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    const int64_t nslots = static_cast<int64_t>(gridDim.x) * G::RPC;
+    const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::RPC + group;
+    const int64_t r0 = rows * slot / nslots;
+    const int64_t r1 = rows * (slot + 1) / nslots;
+    const int64_t maxlen = (rows + nslots - 1) / nslots;
+
+    uint4 wv[G::VPT];
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k) wv[k] = ld_param(w + (k * G::TPR + t) * kVec);
+    float acc[G::VPT][8];
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+
+    for (int64_t it = 0; it < maxlen; ++it) {
+        const int64_t r = r0 + it;
+        const bool active = r < r1;
+        uint4 xv[G::VPT], dv[G::VPT];
+        float v[2] = {0.f, 0.f};
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int vi = k * G::TPR + t;
+                xv[k] = ld_stream(x + r * H + vi * kVec);
+                dv[k] = ld_stream(dy + r * H + vi * kVec);
+            }
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], wf[8];
+                unpack8(xv[k], xf);
+                unpack8(dv[k], df);
+                unpack8(wv[k], wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    v[0] += xf[e] * xf[e];
+                    v[1] += df[e] * wf[e] * xf[e];
+                }
+            }
+        }
+        group_sum<G::TPR, 2>(v, red[it & 1], group, t);
+        if (active) {
+            const float rs = rsqrtf(v[0] * (1.0f / H) + eps);
+            const float c = rs * rs * rs * v[1] * (1.0f / H);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float xf[8], df[8], wf[8], o[8];
+                unpack8(xv[k], xf);
+                unpack8(dv[k], df);
+                unpack8(wv[k], wf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    o[e] = rs * df[e] * wf[e] - xf[e] * c;
+                    acc[k][e] += df[e] * xf[e] * rs;
+                }
+                st_stream(dx + r * H + (k * G::TPR + t) * kVec, pack8(o));
+            }
+        }
+    }
+
+    float* wp = ws + slot * H;
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k) {
+        const int j = (k * G::TPR + t) * kVec;
+        reinterpret_cast<float4*>(wp + j)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+        reinterpret_cast<float4*>(wp + j)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+}
+
+// out0[j] = sum_{slot} ws[slot][0][j] and, with two planes,
+// out1[j] = sum_{slot} ws[slot][1][j], in a fixed order: thread row ty sums
+// slots ty, ty+8, ty+16, ... and the 8 row sums are then added in ty order.
+// Each thread owns 4 adjacent columns of the [planes][H] block (float4
+// loads, coalesced across the warp).
 constexpr int kColThreadsX = 32, kColThreadsY = 8;
 
 __global__ void __launch_bounds__(kColThreadsX * kColThreadsY)
 column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
-              float* __restrict__ dbeta, int nslots, int hidden) {
+              float* __restrict__ dbeta, int nslots, int hidden, int planes) {
     __shared__ float4 part[kColThreadsY][kColThreadsX];
     const int tx = threadIdx.x % kColThreadsX, ty = threadIdx.x / kColThreadsX;
-    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColThreadsX + tx;  // float4 index in [2][H]
-    const bool ok = c4 * 4 < 2 * static_cast<int64_t>(hidden);
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColThreadsX + tx;  // float4 index in [planes][H]
+    const bool ok = c4 * 4 < planes * static_cast<int64_t>(hidden);
     const int which = ok ? static_cast<int>((c4 * 4) / hidden) : 0;
     const int64_t j = ok ? (c4 * 4) % hidden : 0;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -140,7 +223,7 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
 #pragma unroll 4
         for (int p = ty; p < nslots; p += kColThreadsY) {
             const float4 v = __ldcs(reinterpret_cast<const float4*>(
-                ws + (static_cast<int64_t>(p) * 2 + which) * hidden + j));
+                ws + (static_cast<int64_t>(p) * planes + which) * hidden + j));
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
     }
@@ -176,8 +259,27 @@ cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, i
     const int64_t cols4 = 2 * hidden / 4;
     const int grid = static_cast<int>((cols4 + kColThreadsX - 1) / kColThreadsX);
     column_reduce<<<grid, kColThreadsX * kColThreadsY, 0, st>>>(ws, dgamma, dbeta, nslots,
-                                                                 static_cast<int>(hidden));
+                                                                 static_cast<int>(hidden), 2);
     return cudaGetLastError();
+}
+
+cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64_t hidden,
+                                  cudaStream_t st) {
+    const int64_t cols4 = hidden / 4;
+    const int grid = static_cast<int>((cols4 + kColThreadsX - 1) / kColThreadsX);
+    column_reduce<<<grid, kColThreadsX * kColThreadsY, 0, st>>>(ws, out, nullptr, nslots,
+                                                                 static_cast<int>(hidden), 1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                               const void* w, int64_t rows, float eps, int grid, cudaStream_t st) {
+    NF_HIDDEN_SWITCH(hidden, {
+        rmsnorm_bwd_reg<H><<<grid, BGeo<H>::TPR * BGeo<H>::RPC, 0, st>>>(
+            static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
+            static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), rows, eps);
+        return cudaGetLastError();
+    })
 }
 
 }  // namespace nf

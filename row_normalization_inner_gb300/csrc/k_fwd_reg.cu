@@ -6,7 +6,8 @@
 // loops are all static ("optimize inner persistent scheduler for static
 // fusion", description item 2(1): static bdimx when the hidden size is
 // fixed; bdimx a multiple of the warp size).  Each thread loads its VPT
-// 128-bit vectors once, keeps the row in registers as fp32, and reduces it
+// 128-bit vectors once, keeps the row in registers (the fused kernel as the
+// fp32 sum, the others as packed bf16 widened on each pass), and reduces it
 // in the same pass that loads it (the page's compute-with-first-consumer
 // change): sum of squares for RMSNorm; for LayerNorm the sum, then the
 // centered sum of squares over the resident values (two passes, no reload).
@@ -93,17 +94,18 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
         const bool active = row < rows;
-        float f[G::VPT][8];
+        // the row stays packed (bf16) in registers and is widened per pass
+        uint4 xv[G::VPT];
         float ss[1] = {0.f};
         if (active) {
-            uint4 xv[G::VPT];
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(xv[k], f[k]);
+                float f[8];
+                unpack8(xv[k], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss[0] += f[k][e] * f[k][e];
+                for (int e = 0; e < 8; ++e) ss[0] += f[e] * f[e];
             }
         }
         group_sum<G::TPR, 1>(ss, red, group, t);
@@ -112,10 +114,11 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float wf[8], o[8];
+                float f[8], wf[8], o[8];
+                unpack8(xv[k], f);
                 unpack8(ld_param(w + v * kVec), wf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = f[k][e] * rstd * wf[e];
+                for (int e = 0; e < 8; ++e) o[e] = f[e] * rstd * wf[e];
                 st_stream(y + row * H + v * kVec, pack8(o));
             }
         }
@@ -138,17 +141,18 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
         const bool active = row < rows;
-        float f[G::VPT][8];
+        // the row stays packed (bf16) in registers and is widened per pass
+        uint4 xv[G::VPT];
         float acc[1] = {0.f};
         if (active) {
-            uint4 xv[G::VPT];
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(xv[k], f[k]);
+                float f[8];
+                unpack8(xv[k], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[0] += f[k][e];
+                for (int e = 0; e < 8; ++e) acc[0] += f[e];
             }
         }
         group_sum<G::TPR, 1>(acc, red1, group, t);
@@ -156,12 +160,15 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
         float sq[1] = {0.f};
         if (active) {
 #pragma unroll
-            for (int k = 0; k < G::VPT; ++k)
+            for (int k = 0; k < G::VPT; ++k) {
+                float f[8];
+                unpack8(xv[k], f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = f[k][e] - mean;
+                    const float d = f[e] - mean;
                     sq[0] += d * d;
                 }
+            }
         }
         group_sum<G::TPR, 1>(sq, red2, group, t);
         if (active) {
@@ -169,11 +176,12 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float gf[8], bf[8], o[8];
+                float f[8], gf[8], bf[8], o[8];
+                unpack8(xv[k], f);
                 unpack8(ld_param(gamma + v * kVec), gf);
                 unpack8(ld_param(beta + v * kVec), bf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (f[k][e] - mean) * rstd * gf[e] + bf[e];
+                for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gf[e] + bf[e];
                 st_stream(y + row * H + v * kVec, pack8(o));
             }
             if (t == 0) {

@@ -16,7 +16,7 @@ bool reg_shape(int64_t hidden, int* tpr, int* rpc);
 bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);
 // Bulk path: threads per CTA (one producer warp group + consumer row
 // groups), ring stages, dynamic shared memory and consumer row groups for
-// `op` (0 fused, 1 rms, 2 ln fwd, 3 ln bwd).  False if no bulk kernel
+// `op` (0 fused, 1 rms, 2 ln fwd, 3 ln bwd, 4 rms bwd).  False if no bulk kernel
 // exists for (op, hidden).
 bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups);
 
@@ -47,6 +47,13 @@ cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* d
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
                                  int64_t hidden, cudaStream_t st);
 
+// One-plane variant: out[j] = fixed-order sum over the slots of ws[slot][hidden].
+cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64_t hidden,
+                                  cudaStream_t st);
+// RMSNorm backward, stage 1 (register path): RPC slots per CTA, ws[slot][hidden].
+cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                               const void* w, int64_t rows, float eps, int grid, cudaStream_t st);
+
 // Bulk-copy staged path: `grid` persistent CTAs (one per SM), each over a
 // contiguous row stripe; `status` is the device status word.
 cudaError_t launch_fused_bulk(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
@@ -61,6 +68,31 @@ cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd
 cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st);
+
+// RMSNorm backward, stage 1 on the bulk path (grid * groups slots of ws[slot][hidden]).
+cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                                const void* w, int64_t rows, float eps, int grid, int* status,
+                                cudaStream_t st);
+
+// Runtime-hidden path (any hidden that is a multiple of 8 up to
+// dyn_max_hidden(op)).  op: 0 fused, 1 rms fwd, 2 ln fwd, 3 ln bwd, 4 rms bwd.
+struct DynArgs {
+    uint16_t* out0;          // fused: x; rms/ln fwd: y; bwd: dx
+    uint16_t* out1;          // fused: residual
+    const uint16_t* in0;     // x
+    const uint16_t* in1;     // fused: residual; bwd: dy
+    const uint16_t* p0;      // weight / gamma
+    const uint16_t* p1;      // beta
+    float* mean;             // ln fwd out / ln bwd in
+    float* rstd;
+    float* ws;               // bwd partials [grid][planes][hidden]
+    int64_t rows;
+    int hidden;
+    float eps;
+};
+bool dyn_shape(int op, int64_t hidden, int* threads);
+int64_t dyn_max_hidden(int op);
+cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st);
 
 // Bounded-wait self test (see nf_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -63,7 +63,7 @@ def test_status_strings_and_version():
 
 # ---------------------------------------------------------------- validation
 
-@pytest.mark.parametrize("hidden", [0, 1, 8, 1000, 3072, 4095, 16384, -4096])
+@pytest.mark.parametrize("hidden", [0, 1, 4, 12, 1002, 4095, 32776, 65536, -4096])
 def test_unsupported_hidden(hidden):
     assert nf.nf_fused_add_rmsnorm(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_rmsnorm_fwd(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
@@ -71,6 +71,46 @@ def test_unsupported_hidden(hidden):
     assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, hidden, A, 1 << 30, None) == \
         nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_layernorm_bwd_workspace_size(4, hidden) == 0
+
+
+def test_backward_hidden_limit():
+    # the runtime-hidden backward kernels stop at 16384; the forward ones at 32768
+    for h in (16392, 24576, 32768):
+        assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, h, A, 1 << 30, None) == \
+            nf.NF_ERR_UNSUPPORTED_HIDDEN
+        assert nf.nf_rmsnorm_bwd(A, B, C, D, A, 4, h, 1e-6, B, 1 << 30, None) == \
+            nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32768, 152)[1]["path"] == "dynamic"
+
+
+@pytest.mark.parametrize("hidden", [8, 24, 264, 768, 1000, 3072, 6144, 14336, 16384, 32768])
+def test_dynamic_plans(hidden):
+    for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
+        bwd = op.endswith("_bwd")
+        if bwd and hidden > nf.DYN_MAX_HIDDEN_BWD:
+            assert nf.nf_plan_compute(op, 16, hidden, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
+            continue
+        for rows in (1, 77, 16384):
+            st, p = nf.nf_plan_compute(op, rows, hidden, 152)
+            assert st == nf.NF_OK and p["path"] == "dynamic"
+            assert p["block"] % 32 == 0 and 32 <= p["block"] <= (512 if bwd else 1024)
+            assert p["block"] * 4 * 8 >= hidden          # four vectors per thread cover the row
+            assert p["block"] == 32 or (p["block"] - 32) * 4 * 8 < hidden   # no spare warp
+            if bwd:
+                assert p["launches"] == 2 and p["partials"] == p["grid"] >= 1
+                assert p["grid"] <= min(rows, 152 * max(1, 1024 // p["block"]))
+            else:
+                assert p["launches"] == 1 and p["grid"] == rows
+        for path in ("reg", "cluster", "bulk"):
+            assert nf.nf_plan_compute(op, 16, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
+
+
+def test_compiled_sizes_can_be_forced_dynamic():
+    for h in nf.HIDDEN_SET:
+        st, p = nf.nf_plan_compute("layernorm_fwd", 100, h, 152, "dynamic")
+        assert st == nf.NF_OK and p["path"] == "dynamic"
+        st, p = nf.nf_plan_compute("layernorm_bwd", 100, h, 152, "dynamic")
+        assert st == nf.NF_OK and p["path"] == "dynamic"
 
 
 def test_negative_rows_and_bad_eps():
@@ -147,8 +187,22 @@ def test_exact_alias_passes_validation_without_gpu():
     assert nf.nf_layernorm_bwd_workspace_size(16, 4096) == 0
 
 
+def test_rmsnorm_bwd_validation():
+    assert nf.nf_rmsnorm_bwd(A, B, C, D, A, 4, 4004, 1e-6, B, 1 << 30, None) == \
+        nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert nf.nf_rmsnorm_bwd(A, B, C, D, A, -1, 4096, 1e-6, B, 1 << 30, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_rmsnorm_bwd(A, B, C, D, A, 4, 4096, 0.0, B, 1 << 30, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_rmsnorm_bwd(None, None, None, None, None, 0, 4096, 1e-6, None, 0, None) == nf.NF_OK
+    assert nf.nf_rmsnorm_bwd(A, None, C, D, A, 4, 4096, 1e-6, B, 1 << 30, None) == \
+        nf.NF_ERR_INVALID_ARG
+    assert nf.nf_rmsnorm_bwd(A + 8, B, C, D, A + 0x1000000, 4, 4096, 1e-6, B + 0x1000000, 1 << 30,
+                             None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_rmsnorm_bwd_workspace_size(0, 4096) == 0
+
+
 def test_set_path_rejects_unknown():
     assert nf.nf_set_path(17) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(5) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(-1) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
 
@@ -179,9 +233,12 @@ def test_forward_plans(hidden, rows):
         assert bk["grid"] == min(rows, sms) and bk["block"] % 32 == 0
         groups = bk["rows_per_cta"]                        # consumer row groups
         assert 1 <= groups <= 16 and (bk["block"] - 128) % groups == 0
-        # each consumer thread of a group holds exactly 4 vectors of the row
-        assert hidden // 8 == 4 * ((bk["block"] - 128) // groups)
+        # each consumer thread of a group holds a whole number (4 or 5) of vectors of the row
+        per_group = (bk["block"] - 128) // groups
+        assert (hidden // 8) % per_group == 0 and (hidden // 8) // per_group in (4, 5)
         assert bk["block"] <= 1024 and bk["smem_bytes"] <= 227 * 1024
+        # whole warp groups: setmaxnreg is executed by all four warps of a warp group
+        assert bk["block"] % 128 == 0
         st, auto = nf.nf_plan_compute(op, rows, hidden, sms)
         assert st == nf.NF_OK
         want = "cluster" if -(-rows // reg["rows_per_cta"]) * 2 < sms else "reg"
@@ -192,7 +249,7 @@ def test_forward_plans(hidden, rows):
 @pytest.mark.parametrize("rows", [1, 3, 151, 152, 153, 16384, 65537])
 def test_backward_plans(hidden, rows):
     for sms in (1, 148, 152):
-        st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms)
+        st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "reg")
         assert st == nf.NF_OK
         assert p["path"] == "reg" and p["launches"] == 2
         blocks = -(-rows // p["rows_per_cta"])
@@ -206,11 +263,19 @@ def test_backward_plans(hidden, rows):
         assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) <= -(-rows // n)
     assert nf.nf_plan_compute("layernorm_bwd", 16, hidden, 152, "cluster")[0] == \
         nf.NF_ERR_UNSUPPORTED_PATH
+    assert nf.nf_plan_compute("rmsnorm_bwd", 16, hidden, 152, "cluster")[0] == \
+        nf.NF_ERR_UNSUPPORTED_PATH
+    for path in ("reg", "bulk"):
+        a = nf.nf_plan_compute("rmsnorm_bwd", rows, hidden, 152, path)[1]
+        b = nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152, path)[1]
+        assert a == b    # same stripes and slots; only the planes per slot differ
+    assert nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152)[1]["path"] == "bulk"
     for sms in (1, 152):
         st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "bulk")
         assert st == nf.NF_OK and p["path"] == "bulk" and p["launches"] == 2
         assert p["grid"] == min(rows, sms)
         assert p["partials"] == p["grid"] * p["rows_per_cta"]
+        assert p["block"] % 128 == 0 and p["block"] <= 1024
 
 
 def test_plan_invalid_arguments():

@@ -1,0 +1,99 @@
+"""GPU parity of the runtime-hidden (dynamic) kernels against the fp64
+oracle: hidden sizes outside the compiled set (any multiple of 8), and the
+compiled sizes forced onto the dynamic kernels."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import row_normalization_inner_gb300 as nf
+import workloads
+from gpu_helpers import check_bf16, check_f32, ulp_diff_bf16
+
+pytestmark = pytest.mark.gpu
+
+FWD_HIDDEN = (8, 264, 768, 1000, 3072, 6144, 14336, 32768)
+BWD_HIDDEN = (8, 264, 768, 1000, 3072, 6144, 16384)
+ROWS = (1, 37, 300)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from row_normalization_inner_gb300 import build
+    build.build()
+    nf.set_path("auto")
+    yield
+    nf.set_path("auto")
+
+
+def _path_for(hidden):
+    return "dynamic" if hidden in nf.HIDDEN_SET else "auto"
+
+
+@pytest.mark.parametrize("hidden", FWD_HIDDEN + (1024, 8192))
+@pytest.mark.parametrize("rows", ROWS)
+def test_dynamic_fused(rows, hidden):
+    x, r, w = workloads.fused_inputs(rows, hidden, seed=rows + hidden, residual_scale=4.0)
+    s_ref, y_ref, _ = oracle.fused_add_rmsnorm(x, r, w, 1e-5)
+    xd, rd = x.cuda(), r.cuda()
+    with nf.forced_path(_path_for(hidden)):
+        assert nf.nf_plan_query("fused_add_rmsnorm", rows, hidden)["path"] == "dynamic"
+        nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    check_bf16(xd, y_ref, f"dyn fused {rows}x{hidden}")
+    d = ulp_diff_bf16(rd, oracle.to_bf16(s_ref))
+    assert d.max() <= 1 and (d > 0).mean() < 1e-3
+
+
+@pytest.mark.parametrize("hidden", FWD_HIDDEN + (1024, 8192))
+@pytest.mark.parametrize("rows", ROWS)
+def test_dynamic_rmsnorm_fwd(rows, hidden):
+    x, w = workloads.rms_inputs(rows, hidden, seed=rows + hidden)
+    y_ref, _ = oracle.rmsnorm_fwd(x, w, 1e-6)
+    with nf.forced_path(_path_for(hidden)):
+        y = nf.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(y, y_ref, f"dyn rms {rows}x{hidden}")
+
+
+@pytest.mark.parametrize("hidden", FWD_HIDDEN + (1024, 8192))
+@pytest.mark.parametrize("rows", ROWS)
+def test_dynamic_layernorm_fwd(rows, hidden):
+    x, g, b = workloads.layernorm_fwd_inputs(rows, hidden, seed=rows + hidden)
+    y_ref, m_ref, r_ref = oracle.layernorm_fwd(x, g, b, 1e-5)
+    with nf.forced_path(_path_for(hidden)):
+        y, mean, rstd = nf.layernorm_fwd(x.cuda(), g.cuda(), b.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    check_bf16(y, y_ref, f"dyn ln {rows}x{hidden}")
+    check_f32(mean, m_ref, f"dyn ln mean {rows}x{hidden}")
+    check_f32(rstd, r_ref, f"dyn ln rstd {rows}x{hidden}", rtol=1e-4)
+
+
+@pytest.mark.parametrize("hidden", BWD_HIDDEN + (1024, 8192))
+@pytest.mark.parametrize("rows", ROWS + (2000,))
+def test_dynamic_layernorm_bwd(rows, hidden):
+    x, dy, g = workloads.layernorm_bwd_inputs(rows, hidden, seed=rows + hidden)
+    _, m, r = oracle.layernorm_fwd(x, np.ones(hidden), np.zeros(hidden), 1e-5)
+    mean, rstd = torch.from_numpy(m.astype(np.float32)), torch.from_numpy(r.astype(np.float32))
+    dx_ref, dg_ref, db_ref = oracle.layernorm_bwd(dy, x, mean, rstd, g)
+    with nf.forced_path(_path_for(hidden)):
+        dx, dg, db = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+        dx2, dg2, db2 = nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda())
+    torch.cuda.synchronize()
+    check_bf16(dx, dx_ref, f"dyn ln bwd dx {rows}x{hidden}")
+    check_f32(dg, dg_ref, f"dyn ln bwd dgamma {rows}x{hidden}")
+    check_f32(db, db_ref, f"dyn ln bwd dbeta {rows}x{hidden}")
+    assert torch.equal(dg, dg2) and torch.equal(db, db2) and torch.equal(dx, dx2)
+
+
+@pytest.mark.parametrize("hidden", BWD_HIDDEN + (1024, 8192))
+@pytest.mark.parametrize("rows", ROWS + (2000,))
+def test_dynamic_rmsnorm_bwd(rows, hidden):
+    x, dy, w = workloads.rms_bwd_inputs(rows, hidden, seed=rows + hidden)
+    _, rstd = oracle.rmsnorm_fwd(x, w, 1e-6)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(dy, x, rstd, w)
+    with nf.forced_path(_path_for(hidden)):
+        dx, dw = nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(dx, dx_ref, f"dyn rms bwd dx {rows}x{hidden}")
+    check_f32(dw, dw_ref, f"dyn rms bwd dw {rows}x{hidden}")

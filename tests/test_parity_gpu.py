@@ -291,6 +291,77 @@ def test_layernorm_bwd_zero_rows_zeroes_grads():
     assert torch.count_nonzero(dg) == 0 and torch.count_nonzero(db) == 0
 
 
+# ---------------------------------------------------------------- RMSNorm backward
+
+def _rms_bwd_ref(dy, x, w, eps, chunk=2048):
+    """fp64 oracle: rstd from the oracle forward, then the oracle backward."""
+    hidden = x.shape[1]
+    dxs, dws = [], np.zeros(hidden)
+    for i in range(0, x.shape[0], chunk):
+        _, rstd = oracle.rmsnorm_fwd(x[i:i + chunk], w, eps)
+        dx, dw = oracle.rmsnorm_bwd(dy[i:i + chunk], x[i:i + chunk], rstd, w)
+        dxs.append(dx)
+        dws += dw
+    return np.concatenate(dxs), dws
+
+
+@pytest.mark.parametrize("path", BWD_PATHS)
+@pytest.mark.parametrize("hidden", workloads.HIDDEN_SET)
+@pytest.mark.parametrize("rows", (1, 3, 37, 152, 301, 1000))
+def test_rmsnorm_bwd_all_sizes(rows, hidden, path):
+    x, dy, w = workloads.rms_bwd_inputs(rows, hidden, seed=rows)
+    dx_ref, dw_ref = _rms_bwd_ref(dy, x, w, 1e-6)
+    with nf.forced_path(path):
+        dx, dw = nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(dx, dx_ref, f"rms bwd dx {rows}x{hidden}/{path}")
+    check_f32(dw, dw_ref, f"rms bwd dw {rows}x{hidden}/{path}")
+
+
+@pytest.mark.parametrize("path", ("auto",) + BWD_PATHS)
+@pytest.mark.parametrize("hidden", (4096, 8192))
+def test_rmsnorm_bwd_full_size(hidden, path):
+    rows = 16384
+    x, dy, w = workloads.rms_bwd_inputs(rows, hidden)
+    with nf.forced_path(path):
+        dx, dw = nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    dx_ref, dw_ref = _rms_bwd_ref(dy, x, w, 1e-5)
+    check_f32(dw, dw_ref, f"rms bwd full dw {hidden}/{path}")
+    idx = _sample_rows(rows, seed=hidden)
+    check_bf16(dx.cpu()[torch.from_numpy(idx)], dx_ref[idx], f"rms bwd full dx {hidden}/{path}")
+
+
+@pytest.mark.parametrize("path", BWD_PATHS)
+def test_rmsnorm_bwd_in_place_and_deterministic(path):
+    rows, hidden = 640, 8192
+    x, dy, w = workloads.rms_bwd_inputs(rows, hidden, seed=9)
+    dx_ref, dw_ref = _rms_bwd_ref(dy, x, w, 1e-6)
+    with nf.forced_path(path):
+        dyd = dy.cuda()
+        _, dw1 = nf.rmsnorm_bwd(dyd, x.cuda(), w.cuda(), 1e-6, out=dyd)
+        _, dw2 = nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(dyd, dx_ref, f"rms bwd dx written over dy/{path}")
+    check_f32(dw1, dw_ref, f"rms bwd dw/{path}")
+    assert torch.equal(dw1, dw2)
+
+
+def test_rmsnorm_bwd_zero_rows_and_small_workspace():
+    hidden = 2048
+    dw = torch.full((hidden,), 3.0, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert nf.nf_rmsnorm_bwd(0, dw.data_ptr(), 0, 0, 0, 0, hidden, 1e-6, 0, 0, s) == nf.NF_OK
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dw) == 0
+    x, dy, w = workloads.rms_bwd_inputs(64, hidden)
+    need = nf.nf_rmsnorm_bwd_workspace_size(64, hidden)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nf.NFError) as e:
+        nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-6, workspace=ws)
+    assert e.value.status == nf.NF_ERR_WORKSPACE_TOO_SMALL
+
+
 # ---------------------------------------------------------------- determinism, empty, status
 
 @pytest.mark.parametrize("path", FWD_PATHS)
