@@ -189,6 +189,35 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
                          int64_t rows, int64_t hidden, float eps, void* workspace,
                          size_t workspace_bytes, nf_stream stream);
 
+/* Size of the fixed scratch area nf_layernorm_bwd_noalloc uses. */
+#define NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* LayerNorm backward that allocates nothing and takes no workspace.  The
+ * source pages have no counterpart to this call; it is an addition of this
+ * library for callers that cannot call cudaMalloc where they run the
+ * backward pass (code inside a region where the framework's caching
+ * allocator must not be entered, plugins that only receive pre-allocated
+ * buffers, latency-critical paths that cannot take cudaMalloc's implicit
+ * synchronization).  Same arguments, results and rules as nf_layernorm_bwd
+ * minus the workspace: the column partials go to a fixed
+ * NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES area of static device memory
+ * inside the library (held by every GPU that loads the library until the
+ * process exits).  A size whose partials need more than that area under
+ * the plan the call runs (nf_plan_query(NF_OP_LAYERNORM_BWD, ...).partials
+ * * 2 * hidden * 4 bytes; about 10 MB at the compiled sizes on a 152-SM
+ * GPU) returns NF_ERR_WORKSPACE_TOO_SMALL before anything is launched; argument
+ * errors return what nf_layernorm_bwd would.  The first call on
+ * each device looks up the area's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream
+ * capture.  Every call shares the one area, which keeps the last call's
+ * contents (nothing needs clearing: every partial is written before it is
+ * read); calls that overlap on the GPU -- on different streams or from
+ * different host threads -- race on it, so serialize them. */
+nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const void* dy,
+                                   const void* x, const float* mean, const float* rstd,
+                                   const void* gamma, int64_t rows, int64_t hidden,
+                                   nf_stream stream);
+
 /* Force a kernel family for every later call in this process (NF_PATH_AUTO
  * restores the library's choice).  A call whose op/size has no kernel of the
  * forced family returns NF_ERR_UNSUPPORTED_PATH.  Not thread-safe with

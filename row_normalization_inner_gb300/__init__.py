@@ -49,7 +49,7 @@ DYN_MAX_HIDDEN_BWD = 16384
 EXPORTS = (
     "nf_fused_add_rmsnorm", "nf_rmsnorm_fwd", "nf_layernorm_fwd",
     "nf_layernorm_bwd_workspace_size", "nf_layernorm_bwd",
-    "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd",
+    "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd", "nf_layernorm_bwd_noalloc",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
     "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
 )
@@ -91,6 +91,7 @@ def _bind(lib):
         "nf_layernorm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
         "nf_rmsnorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
         "nf_rmsnorm_bwd": (_S, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
+        "nf_layernorm_bwd_noalloc": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
         "nf_set_path": (_S, [_S]),
         "nf_plan_query": (_S, [_S, _I64, _I64, ctypes.POINTER(Plan)]),
         "nf_plan_compute": (_S, [_S, _I64, _I64, ctypes.c_int32, _S, ctypes.POINTER(Plan)]),
@@ -159,6 +160,15 @@ def nf_rmsnorm_bwd(dx, dw, dy, x, weight, rows, hidden, eps, workspace, workspac
                    stream) -> int:
     return lib().nf_rmsnorm_bwd(dx, dw, dy, x, weight, rows, hidden, eps, workspace,
                                 workspace_bytes, stream)
+
+
+def nf_layernorm_bwd_noalloc(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                             stream) -> int:
+    return lib().nf_layernorm_bwd_noalloc(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows,
+                                          hidden, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES
 
 
 def nf_set_path(path) -> int:

@@ -1,0 +1,76 @@
+// LayerNorm backward without a caller-provided workspace.
+//
+// nf_layernorm_bwd needs a scratch buffer for its per-CTA column partials,
+// and its caller has to allocate it.  Some callers cannot allocate device
+// memory at the point where they run the backward pass: code that runs
+// while an allocator is forbidden or unavailable (inside a region where the
+// framework's caching allocator must not be entered, in a plugin that only
+// receives pre-allocated tensors, in a real-time path where cudaMalloc's
+// implicit synchronization is not acceptable).  For them this file keeps a
+// fixed scratch area in the library's own static device memory and
+// forwards to the ordinary entry point with it.
+//
+// The area is a file-scope __device__ array: every GPU that loads the
+// library holds kNoAllocScratchBytes of it until the process exits.  In
+// host code its name only stands in for the device object, so the device
+// address is looked up once per device with cudaGetSymbolAddress (with that
+// device current) and cached; that first call on a device should come
+// before any stream capture.  Calls that overlap on the GPU (different
+// streams, or different host threads) share the one area and race.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "../../include/nf.h"
+
+namespace nf {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES;  // 16 MiB
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_scratch_addr[kMaxDevices];
+
+nf_status scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NF_ERR_CUDA;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_noalloc_scratch) != cudaSuccess || !q) return NF_ERR_CUDA;
+        g_scratch_addr[dev].store(q, std::memory_order_release);
+        p = q;
+    }
+    *out = p;
+    return NF_OK;
+}
+
+}  // namespace
+}  // namespace nf
+
+extern "C" {
+
+nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const void* dy,
+                                   const void* x, const float* mean, const float* rstd,
+                                   const void* gamma, int64_t rows, int64_t hidden,
+                                   nf_stream stream) {
+    if (rows == 0)  // no scratch is touched; same result as the ordinary entry point
+        return nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                                nullptr, 0, stream);
+    // Sizes whose partials (for the plan this call will run) exceed the
+    // fixed area are refused up front, before anything is launched.
+    nf_plan pl;
+    if (nf_status st = nf_plan_query(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
+    const size_t need = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+    if (need > nf::kNoAllocScratchBytes) return NF_ERR_WORKSPACE_TOO_SMALL;
+    void* scratch = nullptr;
+    if (nf_status st = nf::scratch_address(&scratch)) return st;
+    // Stage 1 writes every partial slot before stage 2 reads it, so the
+    // area needs no clearing between calls.
+    return nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, scratch,
+                            nf::kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"
