@@ -49,32 +49,32 @@ int bwd_ctas_per_sm(int64_t hidden) {
     return 1;
 }
 
-// Automatic choice between the register and the cluster forward paths: a
-// row goes to a cluster when one-CTA-per-row-group would occupy fewer than
-// half of the SMs.
-bool prefer_cluster(int64_t rows, int rpc, int sms) {
-    const int64_t ctas = (rows + rpc - 1) / rpc;
-    return ctas * 2 < sms;
-}
-
-// The library's own path choice.  Forward ops: a row goes to a cluster
-// when one CTA per row group would occupy fewer than half of the SMs;
-// otherwise the register path.  Backward ops: the bulk path, whose ring
-// keeps many rows in flight while the consumers hold the column
-// accumulators in registers.
+// The library's own path choice, from the per-path timings on GB300 (CUDA
+// graphs of back-to-back launches over L2-cold inputs, every op x size x
+// path):
+//  - forward ops: the register path is fastest at every row count, from 1
+//    row (about 2-3 us per launch, where a cluster split only adds its
+//    barrier latency) to 65536 rows (1.0x the measured copy bandwidth);
+//    the one exception is hidden 12288 RMSNorm / LayerNorm forward with
+//    many rows, where the bulk ring keeps more bytes in flight than 384
+//    threads per row can;
+//  - backward ops: the bulk path, except for small problems (rows x hidden
+//    up to 4 Mi elements), where the register path's lower start-up wins.
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
-    (void)hidden;
+    (void)rpc;
+    (void)sms;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    if (!fwd) return NF_PATH_BULK;
-    if (prefer_cluster(rows, rpc, sms)) return NF_PATH_CLUSTER;
+    if (!fwd) return rows * hidden <= (int64_t{4} << 20) ? NF_PATH_REG : NF_PATH_BULK;
+    if (hidden >= 12288 && ((op == NF_OP_RMSNORM_FWD && rows >= 1024) ||
+                            (op == NF_OP_LAYERNORM_FWD && rows >= 4096)))
+        return NF_PATH_BULK;
     return NF_PATH_REG;
 }
 
 // Column-partial planes a backward op keeps per slot (LayerNorm: dgamma and
 // dbeta; RMSNorm: dw).
 int bwd_planes(nf_op op) { return op == NF_OP_LAYERNORM_BWD ? 2 : 1; }
-
 
 std::atomic<int> g_forced_path{NF_PATH_AUTO};
 
@@ -273,7 +273,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.rows_per_cta = groups;  // rows being computed at once per CTA
         pl.smem_bytes = smem;
         pl.launches = fwd ? 1 : 2;
-        pl.partials = fwd ? 0 : static_cast<int32_t>(g * groups);
+        pl.partials = fwd ? 0 : static_cast<int32_t>(g);  // groups fold into one slot per CTA
     } else {  // register-path backward: persistent stage 1 + column reduce
         const int64_t blocks = (rows + rpc - 1) / rpc;
         const int64_t resident = static_cast<int64_t>(sm_count) * bwd_ctas_per_sm(hidden);

@@ -61,6 +61,7 @@ struct BulkShape {
 constexpr int kSmemBudget = 200 * 1024;  // ring + barriers + reduction scratch
 constexpr int kMaxStagesPerGroup = 8;
 constexpr int kProducerRegs = 40;
+constexpr int kConsumersBarrier = 15;  // named barrier of all consumer threads (groups use 1..NG)
 
 template <int OP> struct OpIO {
     static constexpr int NIN = (OP == kFused || OP == kLnBwd || OP == kRmsBwd) ? 2 : 1;  // staged tensors per row
@@ -148,7 +149,7 @@ struct BulkArgs {
     const uint16_t* p1;      // beta
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
-    float* ws;               // bwd column partials [grid * NG][planes][H]
+    float* ws;               // bwd column partials [grid][planes][H], one slot per CTA
     int* status;
     int64_t rows;
     float eps;
@@ -402,33 +403,39 @@ norm_bulk_kernel(BulkArgs a) {
             }
         }
     }
-    if (failed) {
-        if (gt == 0) record_status(a.status, kStatusTimeout);
-        return;
-    }
-    if constexpr (OP == kRmsBwd) {
-        const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::NG + gid;
-        float* wg = a.ws + slot * H;
+    if constexpr (kBwd) {
+        // Fold the NG groups' column partials into one slot per CTA, in
+        // group order: each group parks its partials in its own ring slice
+        // (all of its rows are consumed, so no copy targets that slice any
+        // more), every consumer thread meets at a consumer-wide barrier --
+        // failed groups too, so nobody waits on a missing warp -- and the
+        // consumers then sum the slices column by column.
+        constexpr int NP = OP == kLnBwd ? 2 : 1;
+        static_assert(G::SG * G::STAGE_BYTES >= NP * H * 4, "ring slice holds a group's partials");
+        float* mine = reinterpret_cast<float*>(smem + gid * G::SG * G::STAGE_BYTES);
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) {
             const int jj = (k * G::GT + gt) * kVec;
-            reinterpret_cast<float4*>(wg + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
-            reinterpret_cast<float4*>(wg + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+            reinterpret_cast<float4*>(mine + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
+            reinterpret_cast<float4*>(mine + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+            if constexpr (NP == 2) {
+                reinterpret_cast<float4*>(mine + H + jj)[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
+                reinterpret_cast<float4*>(mine + H + jj)[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
+            }
         }
-    }
-    if constexpr (OP == kLnBwd) {
-        const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::NG + gid;
-        float* wg = a.ws + slot * 2 * H;
-        float* wb = wg + H;
+        named_sync(kConsumersBarrier, G::NCT);
+        float4* out = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(blockIdx.x) * NP * H);
+        for (int c4 = ct; c4 < NP * H / 4; c4 += G::NCT) {
+            float4 acc = reinterpret_cast<const float4*>(smem)[c4];
 #pragma unroll
-        for (int k = 0; k < G::VPT; ++k) {
-            const int jj = (k * G::GT + gt) * kVec;
-            reinterpret_cast<float4*>(wg + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
-            reinterpret_cast<float4*>(wg + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
-            reinterpret_cast<float4*>(wb + jj)[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
-            reinterpret_cast<float4*>(wb + jj)[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
+            for (int g = 1; g < G::NG; ++g) {
+                const float4 v = reinterpret_cast<const float4*>(smem + g * G::SG * G::STAGE_BYTES)[c4];
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            out[c4] = acc;
         }
     }
+    if (failed && gt == 0) record_status(a.status, kStatusTimeout);
 }
 
 namespace {

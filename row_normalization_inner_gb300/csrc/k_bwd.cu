@@ -204,24 +204,25 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
 
 // out0[j] = sum_{slot} ws[slot][0][j] and, with two planes,
 // out1[j] = sum_{slot} ws[slot][1][j], in a fixed order: thread row ty sums
-// slots ty, ty+8, ty+16, ... and the 8 row sums are then added in ty order.
-// Each thread owns 4 adjacent columns of the [planes][H] block (float4
-// loads, coalesced across the warp).
-constexpr int kColThreadsX = 32, kColThreadsY = 8;
+// slots ty, ty+32, ty+64, ... and the 32 row sums are then added in ty
+// order.  A CTA covers 32 columns: 8 column lanes of one float4 each, so a
+// warp reads 4 slots x 128 contiguous bytes.  Many small CTAs keep every SM
+// busy even at hidden 1024 (64 CTAs for two planes).
+constexpr int kColX = 8, kColY = 32;
 
-__global__ void __launch_bounds__(kColThreadsX * kColThreadsY)
+__global__ void __launch_bounds__(kColX * kColY)
 column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
               float* __restrict__ dbeta, int nslots, int hidden, int planes) {
-    __shared__ float4 part[kColThreadsY][kColThreadsX];
-    const int tx = threadIdx.x % kColThreadsX, ty = threadIdx.x / kColThreadsX;
-    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColThreadsX + tx;  // float4 index in [planes][H]
+    __shared__ float4 part[kColY][kColX];
+    const int tx = threadIdx.x % kColX, ty = threadIdx.x / kColX;
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColX + tx;  // float4 index in [planes][H]
     const bool ok = c4 * 4 < planes * static_cast<int64_t>(hidden);
     const int which = ok ? static_cast<int>((c4 * 4) / hidden) : 0;
     const int64_t j = ok ? (c4 * 4) % hidden : 0;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
 #pragma unroll 4
-        for (int p = ty; p < nslots; p += kColThreadsY) {
+        for (int p = ty; p < nslots; p += kColY) {
             const float4 v = __ldcs(reinterpret_cast<const float4*>(
                 ws + (static_cast<int64_t>(p) * planes + which) * hidden + j));
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
@@ -232,7 +233,7 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     if (ty == 0 && ok) {
         float4 tot = part[0][tx];
 #pragma unroll
-        for (int y = 1; y < kColThreadsY; ++y) {
+        for (int y = 1; y < kColY; ++y) {
             const float4 v = part[y][tx];
             tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
         }
@@ -257,18 +258,18 @@ cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* d
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
                                  int64_t hidden, cudaStream_t st) {
     const int64_t cols4 = 2 * hidden / 4;
-    const int grid = static_cast<int>((cols4 + kColThreadsX - 1) / kColThreadsX);
-    column_reduce<<<grid, kColThreadsX * kColThreadsY, 0, st>>>(ws, dgamma, dbeta, nslots,
-                                                                 static_cast<int>(hidden), 2);
+    const int grid = static_cast<int>((cols4 + kColX - 1) / kColX);
+    column_reduce<<<grid, kColX * kColY, 0, st>>>(ws, dgamma, dbeta, nslots,
+                                                 static_cast<int>(hidden), 2);
     return cudaGetLastError();
 }
 
 cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64_t hidden,
                                   cudaStream_t st) {
     const int64_t cols4 = hidden / 4;
-    const int grid = static_cast<int>((cols4 + kColThreadsX - 1) / kColThreadsX);
-    column_reduce<<<grid, kColThreadsX * kColThreadsY, 0, st>>>(ws, out, nullptr, nslots,
-                                                                 static_cast<int>(hidden), 1);
+    const int grid = static_cast<int>((cols4 + kColX - 1) / kColX);
+    column_reduce<<<grid, kColX * kColY, 0, st>>>(ws, out, nullptr, nslots,
+                                                 static_cast<int>(hidden), 1);
     return cudaGetLastError();
 }
 

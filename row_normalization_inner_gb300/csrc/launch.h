@@ -64,12 +64,12 @@ cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd
                                const void* gamma, const void* beta, int64_t rows, float eps,
                                int grid, int* status, cudaStream_t st);
 // Stage 1 of LayerNorm backward on the bulk path: one column-partial slot
-// per consumer row group (grid * groups slots).
+// per CTA (the row groups fold theirs inside the CTA).
 cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st);
 
-// RMSNorm backward, stage 1 on the bulk path (grid * groups slots of ws[slot][hidden]).
+// RMSNorm backward, stage 1 on the bulk path (one slot of ws[slot][hidden] per CTA).
 cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                 const void* w, int64_t rows, float eps, int grid, int* status,
                                 cudaStream_t st);
