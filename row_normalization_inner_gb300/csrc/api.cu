@@ -58,14 +58,14 @@ int bwd_ctas_per_sm(int64_t hidden) {
 //    the one exception is hidden 12288 RMSNorm / LayerNorm forward with
 //    many rows, where the bulk ring keeps more bytes in flight than 384
 //    threads per row can;
-//  - backward ops: the bulk path, except for small problems (rows x hidden
-//    up to 4 Mi elements), where the register path's lower start-up wins.
+//  - backward ops: the bulk path, at every size (its row groups fold their
+//    column partials inside the CTA, so stage 2 stays small).
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
     (void)rpc;
     (void)sms;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    if (!fwd) return rows * hidden <= (int64_t{4} << 20) ? NF_PATH_REG : NF_PATH_BULK;
+    if (!fwd) return NF_PATH_BULK;
     if (hidden >= 12288 && ((op == NF_OP_RMSNORM_FWD && rows >= 1024) ||
                             (op == NF_OP_LAYERNORM_FWD && rows >= 4096)))
         return NF_PATH_BULK;

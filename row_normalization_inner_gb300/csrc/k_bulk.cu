@@ -7,7 +7,8 @@
 // is the producer: one elected thread issues, per row, one 1-D bulk
 // asynchronous copy (cp.async.bulk, global -> this CTA's shared memory) per
 // input tensor into a ring of S stages, each completing on the stage's
-// "full" mbarrier.  The consumers are NG independent row groups of GW warps
+// "full" mbarrier (one issuing thread per producer warp, each serving its
+// own row groups).  The consumers are NG independent row groups of GW warps
 // each; row i of the stripe belongs to group i % NG, and every group owns a
 // private slice of SG ring stages which it consumes strictly in order (so a
 // stage's barrier phases and the group's row sequence move in lockstep and
@@ -180,30 +181,47 @@ norm_bulk_kernel(BulkArgs a) {
     if (threadIdx.x < 128) {
         // ---------------- producer warp group
         if constexpr (SHARE) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-        if (threadIdx.x == 0) {
-            int issued = 0;
+        // One producer thread per producer warp (lane 0 of warps
+        // 0..NPROD-1); warp w serves the row groups g with g % NPROD == w.
+        // Groups own private ring slices, so two producers never touch the
+        // same stage, and each group's rows are issued in order.
+        constexpr int NPROD = G::NG < 4 ? G::NG : 4;
+        constexpr int GPP = G::NG / NPROD;  // groups per producer
+        const int pw = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0 && pw < NPROD) {
+            int issued[GPP];
+#pragma unroll
+            for (int k = 0; k < GPP; ++k) issued[k] = 0;
             bool ok = true;
-            for (int i = 0; i < n; ++i) {
-                const int q = i / G::NG;  // row index within its group
-                const int s = (i % G::NG) * G::SG + q % G::SG;
-                const uint32_t par = ((q / G::SG) & 1) ^ 1;
-                if (!mbar_wait(&empty[s], par, kWaitLimitNs)) { ok = false; break; }
-                mbar_arrive_expect_tx(&full[s], G::STAGE_BYTES);
-                const int64_t row = r0 + i;
-                uint8_t* st = smem + s * G::STAGE_BYTES;
-                bulk_g2s(smem_addr(st), a.in0 + row * H, G::ROW_BYTES, &full[s]);
-                if constexpr (OpIO<OP>::NIN == 2)
-                    bulk_g2s(smem_addr(st + G::ROW_BYTES), a.in1 + row * H, G::ROW_BYTES, &full[s]);
-                issued = i + 1;
+            const int qmax = (n + G::NG - 1) / G::NG;
+            for (int q = 0; q < qmax && ok; ++q) {
+#pragma unroll
+                for (int k = 0; k < GPP; ++k) {
+                    const int g = pw + k * NPROD;
+                    const int i = g + q * G::NG;
+                    if (!ok || i >= n) continue;
+                    const int s = g * G::SG + q % G::SG;
+                    const uint32_t par = ((q / G::SG) & 1) ^ 1;
+                    if (!mbar_wait(&empty[s], par, kWaitLimitNs)) { ok = false; continue; }
+                    mbar_arrive_expect_tx(&full[s], G::STAGE_BYTES);
+                    const int64_t row = r0 + i;
+                    uint8_t* st = smem + s * G::STAGE_BYTES;
+                    bulk_g2s(smem_addr(st), a.in0 + row * H, G::ROW_BYTES, &full[s]);
+                    if constexpr (OpIO<OP>::NIN == 2)
+                        bulk_g2s(smem_addr(st + G::ROW_BYTES), a.in1 + row * H, G::ROW_BYTES, &full[s]);
+                    issued[k] = q + 1;
+                }
             }
             if (!ok) {
                 record_status(a.status, kStatusTimeout);
                 // let the copies already issued land before the CTA can exit
-                // (the last S issued rows cover every stage exactly once)
-                const int first = issued > G::S ? issued - G::S : 0;
-                for (int i = first; i < issued; ++i) {
-                    const int q = i / G::NG;
-                    mbar_wait(&full[(i % G::NG) * G::SG + q % G::SG], (q / G::SG) & 1, kWaitLimitNs / 4);
+                // (a group's last SG issued rows cover each of its stages once)
+#pragma unroll
+                for (int k = 0; k < GPP; ++k) {
+                    const int g = pw + k * NPROD;
+                    const int first = issued[k] > G::SG ? issued[k] - G::SG : 0;
+                    for (int q = first; q < issued[k]; ++q)
+                        mbar_wait(&full[g * G::SG + q % G::SG], (q / G::SG) & 1, kWaitLimitNs / 4);
                 }
             }
         }
@@ -403,6 +421,10 @@ norm_bulk_kernel(BulkArgs a) {
             }
         }
     }
+    // This CTA's rows are done: let a programmatically dependent launch
+    // (the column reduction of the backward ops) start scheduling.  It still
+    // waits for this grid to finish before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (kBwd) {
         // Fold the NG groups' column partials into one slot per CTA, in
         // group order: each group parks its partials in its own ring slice

@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(kColX * kColY)
 column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
               float* __restrict__ dbeta, int nslots, int hidden, int planes) {
     __shared__ float4 part[kColY][kColX];
+    // Launched as a programmatic dependent of stage 1: wait until stage 1
+    // has finished and its partials are visible (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tx = threadIdx.x % kColX, ty = threadIdx.x / kColX;
     const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColX + tx;  // float4 index in [planes][H]
     const bool ok = c4 * 4 < planes * static_cast<int64_t>(hidden);
@@ -255,22 +258,33 @@ cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* d
     })
 }
 
+// Stage 2 is launched with programmatic stream serialization: its launch
+// overlaps the tail of stage 1, and the kernel's griddepcontrol.wait keeps
+// every read after stage 1 has completed.
+cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out1, int nslots,
+                                        int64_t hidden, int planes, cudaStream_t st) {
+    const int64_t cols4 = planes * hidden / 4;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((cols4 + kColX - 1) / kColX), 1, 1);
+    cfg.blockDim = dim3(kColX * kColY, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, column_reduce, ws, out0, out1, nslots,
+                              static_cast<int>(hidden), planes);
+}
+
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
                                  int64_t hidden, cudaStream_t st) {
-    const int64_t cols4 = 2 * hidden / 4;
-    const int grid = static_cast<int>((cols4 + kColX - 1) / kColX);
-    column_reduce<<<grid, kColX * kColY, 0, st>>>(ws, dgamma, dbeta, nslots,
-                                                 static_cast<int>(hidden), 2);
-    return cudaGetLastError();
+    return launch_column_reduce_planes(ws, dgamma, dbeta, nslots, hidden, 2, st);
 }
 
 cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64_t hidden,
                                   cudaStream_t st) {
-    const int64_t cols4 = hidden / 4;
-    const int grid = static_cast<int>((cols4 + kColX - 1) / kColX);
-    column_reduce<<<grid, kColX * kColY, 0, st>>>(ws, out, nullptr, nslots,
-                                                 static_cast<int>(hidden), 1);
-    return cudaGetLastError();
+    return launch_column_reduce_planes(ws, out, nullptr, nslots, hidden, 1, st);
 }
 
 cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,

@@ -273,8 +273,7 @@ def test_backward_plans(hidden, rows):
         b = nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152, path)[1]
         assert a == b    # same stripes and slots; only the planes per slot differ
     for op in ("layernorm_bwd", "rmsnorm_bwd"):
-        want = "reg" if rows * hidden <= 4 << 20 else "bulk"
-        assert nf.nf_plan_compute(op, rows, hidden, 152)[1]["path"] == want
+        assert nf.nf_plan_compute(op, rows, hidden, 152)[1]["path"] == "bulk"
     for sms in (1, 152):
         st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "bulk")
         assert st == nf.NF_OK and p["path"] == "bulk" and p["launches"] == 2
