@@ -30,7 +30,10 @@
  * hidden.   The compiled sizes 1024, 2048, 4096, 5120, 8192, 12288 get
  *           kernels specialized per size.  Any other multiple of 8 up to
  *           32768 (forward ops) or 16384 (backward ops) runs on the
- *           runtime-hidden kernels (NF_PATH_DYNAMIC).  Other values return
+ *           runtime-hidden kernels (NF_PATH_DYNAMIC); longer rows, up to
+ *           262144 (forward) or 131072 (backward), run on the grid-parallel
+ *           cluster kernels (NF_PATH_CLUSTER), which split one row over a
+ *           cluster of 2, 4 or 8 CTAs.  Other values return
  *           NF_ERR_UNSUPPORTED_HIDDEN.
  * rows.     Any value >= 0; rows == 0 returns NF_OK without launching.
  * eps.      Finite and > 0.
@@ -79,8 +82,11 @@ typedef struct CUstream_st* nf_stream;
  *              of threads ("optimize inner persistent scheduler for static
  *              fusion": static hidden size, warp-multiple block size).
  *   CLUSTER -- one row split across a thread-block cluster, partial sums
- *              exchanged through distributed shared memory (the small-batch
- *              case of the same page: use more SMs when rows are few).
+ *              exchanged through distributed shared memory: the small-batch
+ *              idea of the same page (more SMs per row), and the
+ *              grid-parallel inner normalization "Llu/ln bwd" lists as
+ *              missing (rows longer than one CTA holds; any hidden, forward
+ *              and backward).
  *   BULK    -- a producer warp stages rows into a shared-memory ring with
  *              bulk asynchronous copies; consumer warps read 128-bit vectors
  *              from shared memory; registers move from producer to

@@ -44,6 +44,8 @@ OPS = {"fused_add_rmsnorm": 0, "rmsnorm_fwd": 1, "layernorm_fwd": 2, "layernorm_
 HIDDEN_SET = (1024, 2048, 4096, 5120, 8192, 12288)   # compiled sizes
 DYN_MAX_HIDDEN_FWD = 32768    # runtime-hidden path: any multiple of 8 up to these
 DYN_MAX_HIDDEN_BWD = 16384
+LONG_MAX_HIDDEN_FWD = 262144  # grid-parallel cluster path for longer rows
+LONG_MAX_HIDDEN_BWD = 131072
 
 # Every symbol include/nf.h declares.
 EXPORTS = (

@@ -121,10 +121,11 @@ bool hidden_ok(int64_t h) {
     return reg_shape(h, &a, &b);
 }
 
-// A size some kernel of `op` handles (compiled, or the runtime-hidden path).
+// A size some kernel of `op` handles (compiled, the runtime-hidden path, or
+// the grid-parallel cluster path for long rows).
 bool hidden_supported(nf_op op, int64_t h) {
-    int t;
-    return hidden_ok(h) || dyn_shape(op, h, &t);
+    int t, c, sl;
+    return hidden_ok(h) || dyn_shape(op, h, &t) || long_shape(op, h, &c, &t, &sl);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -171,7 +172,7 @@ size_t bwd_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
     // enough for every backward path, so a later nf_set_path cannot make a
     // previously sized workspace too small
     size_t most = 0;
-    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC}) {
+    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER}) {
         nf_plan pl;
         if (nf_plan_compute(op, rows, hidden, sms, p, &pl) != NF_OK) continue;
         const size_t b = static_cast<size_t>(pl.partials) * bwd_planes(op) *
@@ -214,16 +215,22 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
     if (path < NF_PATH_AUTO || path > NF_PATH_DYNAMIC) return NF_ERR_INVALID_ARG;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    int tpr = 0, rpc = 1, dyn_threads = 0;
+    int tpr = 0, rpc = 1, dyn_threads = 0, long_c = 0, long_t = 0, long_slice = 0;
     const bool compiled = reg_shape(hidden, &tpr, &rpc);
     const bool dyn_ok = dyn_shape(op, hidden, &dyn_threads);
-    if (!compiled && !dyn_ok) return NF_ERR_UNSUPPORTED_HIDDEN;
+    const bool long_ok = long_shape(op, hidden, &long_c, &long_t, &long_slice);
+    if (!compiled && !dyn_ok && !long_ok) return NF_ERR_UNSUPPORTED_HIDDEN;
 
     nf_path p = path;
-    if (p == NF_PATH_AUTO) p = compiled ? auto_path(op, rows, hidden, rpc, sm_count) : NF_PATH_DYNAMIC;
-    if (p != NF_PATH_DYNAMIC && !compiled) return NF_ERR_UNSUPPORTED_PATH;
+    if (p == NF_PATH_AUTO)
+        p = compiled ? auto_path(op, rows, hidden, rpc, sm_count)
+                     : (dyn_ok ? NF_PATH_DYNAMIC : NF_PATH_CLUSTER);
+    if ((p == NF_PATH_REG || p == NF_PATH_BULK) && !compiled) return NF_ERR_UNSUPPORTED_PATH;
     if (p == NF_PATH_DYNAMIC && !dyn_ok) return NF_ERR_UNSUPPORTED_PATH;
-    if (p == NF_PATH_CLUSTER && !fwd) return NF_ERR_UNSUPPORTED_PATH;
+    // the cluster family: the static kernels for compiled forward sizes,
+    // the long-row (runtime hidden) kernels otherwise and for backward ops
+    const bool long_cluster = p == NF_PATH_CLUSTER && !(fwd && compiled);
+    if (long_cluster && !long_ok) return NF_ERR_UNSUPPORTED_PATH;
 
     nf_plan pl;
     std::memset(&pl, 0, sizeof pl);
@@ -236,6 +243,23 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.cluster = 1;
         pl.rows_per_cta = rpc;
         pl.launches = 1;
+    } else if (long_cluster) {
+        pl.block = long_t;
+        pl.cluster = long_c;
+        pl.rows_per_cta = 1;
+        if (fwd) {
+            const int64_t max_clusters = kMaxGrid / long_c;
+            const int64_t clusters = rows < max_clusters ? rows : max_clusters;
+            pl.grid = static_cast<int32_t>(clusters * long_c);
+            pl.launches = 1;
+        } else {
+            int64_t clusters = sm_count / long_c;
+            if (clusters > rows) clusters = rows;
+            if (clusters < 1) clusters = 1;
+            pl.grid = static_cast<int32_t>(clusters * long_c);
+            pl.launches = 2;
+            pl.partials = static_cast<int32_t>(clusters);
+        }
     } else if (p == NF_PATH_CLUSTER) {
         int c, t;
         if (!cluster_shape(hidden, &c, &t)) return NF_ERR_UNSUPPORTED_HIDDEN;
@@ -317,9 +341,9 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, &pl)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_CLUSTER)
+    if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
-    if (pl.path == NF_PATH_DYNAMIC) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(x);
         a.out1 = static_cast<uint16_t*>(residual);
@@ -329,6 +353,7 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
+        if (pl.path == NF_PATH_CLUSTER) return from_cuda(launch_long(NF_OP_FUSED_ADD_RMSNORM, a, pl.grid, s));
         return from_cuda(launch_dyn(NF_OP_FUSED_ADD_RMSNORM, a, pl.grid, s));
     }
     if (pl.path == NF_PATH_BULK) {
@@ -351,9 +376,9 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_RMSNORM_FWD, rows, hidden, &pl)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_CLUSTER)
+    if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
-    if (pl.path == NF_PATH_DYNAMIC) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(y);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -361,6 +386,7 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
+        if (pl.path == NF_PATH_CLUSTER) return from_cuda(launch_long(NF_OP_RMSNORM_FWD, a, pl.grid, s));
         return from_cuda(launch_dyn(NF_OP_RMSNORM_FWD, a, pl.grid, s));
     }
     if (pl.path == NF_PATH_BULK) {
@@ -391,10 +417,10 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_LAYERNORM_FWD, rows, hidden, &pl)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_CLUSTER)
+    if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
                                                pl.grid, s));
-    if (pl.path == NF_PATH_DYNAMIC) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(y);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -405,6 +431,7 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
+        if (pl.path == NF_PATH_CLUSTER) return from_cuda(launch_long(NF_OP_LAYERNORM_FWD, a, pl.grid, s));
         return from_cuda(launch_dyn(NF_OP_LAYERNORM_FWD, a, pl.grid, s));
     }
     if (pl.path == NF_PATH_BULK) {
@@ -458,7 +485,7 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
             return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -469,7 +496,9 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         a.ws = ws;
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
-        if (cudaError_t e = launch_dyn(NF_OP_LAYERNORM_BWD, a, pl.grid, s)) return from_cuda(e);
+        const cudaError_t e = pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_LAYERNORM_BWD, a, pl.grid, s)
+                                                         : launch_dyn(NF_OP_LAYERNORM_BWD, a, pl.grid, s);
+        if (e != cudaSuccess) return from_cuda(e);
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
@@ -517,7 +546,7 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
         if (dx_clash || overlap(sdw, in) || overlap(sws, in)) return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -527,7 +556,9 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
-        if (cudaError_t e = launch_dyn(NF_OP_RMSNORM_BWD, a, pl.grid, s)) return from_cuda(e);
+        const cudaError_t e = pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_RMSNORM_BWD, a, pl.grid, s)
+                                                         : launch_dyn(NF_OP_RMSNORM_BWD, a, pl.grid, s);
+        if (e != cudaSuccess) return from_cuda(e);
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;

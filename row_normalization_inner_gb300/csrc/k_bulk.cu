@@ -242,6 +242,13 @@ norm_bulk_kernel(BulkArgs a) {
         prm0[k] = ld_param(a.p0 + (k * G::GT + gt) * kVec);
     }
     constexpr bool kBwd = OP == kLnBwd || OP == kRmsBwd;
+    // Backward consumers keep gamma / w widened to fp32 for the whole stripe
+    // (they run with the larger register share), so no row re-widens it.
+    float wf[kBwd ? G::VPT : 1][8];
+    if constexpr (kBwd) {
+#pragma unroll
+        for (int k = 0; k < G::VPT; ++k) unpack8(prm0[k], wf[k]);
+    }
     float acc_g[kBwd ? G::VPT : 1][8], acc_b[OP == kLnBwd ? G::VPT : 1][8];
     if constexpr (kBwd) {
 #pragma unroll
@@ -313,40 +320,34 @@ norm_bulk_kernel(BulkArgs a) {
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
         } else if constexpr (OP == kLnFwd) {
-            // the row stays packed (bf16) in registers and is widened on each
-            // of the three passes: fewer live registers, same values
+            float f[G::VPT][8];
             float v[2] = {0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float f[8];
-                unpack8(v0[k], f);
+                unpack8(v0[k], f[k]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[0] += f[e];
+                for (int e = 0; e < 8; ++e) v[0] += f[k][e];
             }
             group_reduce<G::GW, 2>(v, rb0, gwarp, lane, gid);
             if (v[1] != 0.f) { failed = true; break; }
             const float mean = v[0] * (1.0f / H);
             float sq[1] = {0.f};
 #pragma unroll
-            for (int k = 0; k < G::VPT; ++k) {
-                float f[8];
-                unpack8(v0[k], f);
+            for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = f[e] - mean;
-                    sq[0] += d * d;
+                    f[k][e] -= mean;  // the row, centered in place
+                    sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
                 }
-            }
             group_reduce<G::GW, 1>(sq, rb1, gwarp, lane, gid);
             const float rstd = rsqrtf(sq[0] * (1.0f / H) + a.eps);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float f[8], g[8], b[8], o[8];
-                unpack8(v0[k], f);
+                float g[8], b[8], o[8];
                 unpack8(prm0[k], g);
                 unpack8(ld_param(a.p1 + (k * G::GT + gt) * kVec), b);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * g[e] + b[e];
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(f[k][e], rstd * g[e], b[e]);
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
             if (gt == 0) {
@@ -355,18 +356,17 @@ norm_bulk_kernel(BulkArgs a) {
             }
         } else if constexpr (OP == kRmsBwd) {
             // rstd recomputed from the row: rs = rsqrt(sum x^2 / H + eps),
-            // dx = rs * g - x * rs^3 * sum(g x) / H with g = dy * w
+            // dx = rs * g - x * (rs^3 * sum(g x) / H) with g = dy * w
+            float xf[G::VPT][8], df[G::VPT][8];
             float v[3] = {0.f, 0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xf[8], df[8], wf[8];
-                unpack8(v0[k], xf);
-                unpack8(v1[k], df);
-                unpack8(prm0[k], wf);
+                unpack8(v0[k], xf[k]);
+                unpack8(v1[k], df[k]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    v[0] += xf[e] * xf[e];
-                    v[1] += df[e] * wf[e] * xf[e];
+                    v[0] = fmaf(xf[k][e], xf[k][e], v[0]);
+                    v[1] = fmaf(df[k][e] * wf[k][e], xf[k][e], v[1]);
                 }
             }
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
@@ -375,48 +375,47 @@ norm_bulk_kernel(BulkArgs a) {
             const float c = rs * rs * rs * v[1] * (1.0f / H);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xf[8], df[8], wf[8], o[8];
-                unpack8(v0[k], xf);
-                unpack8(v1[k], df);
-                unpack8(prm0[k], wf);
+                float o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    o[e] = rs * df[e] * wf[e] - xf[e] * c;
-                    acc_g[k][e] += df[e] * xf[e] * rs;
+                    o[e] = fmaf(-xf[k][e], c, rs * (df[k][e] * wf[k][e]));
+                    acc_g[k][e] = fmaf(df[k][e] * xf[k][e], rs, acc_g[k][e]);
                 }
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
         } else {  // kLnBwd
+            // xhat = x * rstd - mean * rstd (one fma), g = dy * gamma;
+            // dx = rstd * g - rstd * A - xhat * (rstd * B)
             const float mu = nmu, rs = nrs;
             if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
+            const float nmr = -mu * rs;
+            float xf[G::VPT][8], df[G::VPT][8];
             float v[3] = {0.f, 0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xf[8], df[8], gf[8];
-                unpack8(v0[k], xf);
-                unpack8(v1[k], df);
-                unpack8(prm0[k], gf);
+                unpack8(v0[k], xf[k]);
+                unpack8(v1[k], df[k]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float xh = (xf[e] - mu) * rs;
-                    const float g = df[e] * gf[e];
+                    const float xh = fmaf(xf[k][e], rs, nmr);
+                    const float g = df[k][e] * wf[k][e];
                     v[0] += g;
-                    v[1] += g * xh;
-                    acc_g[k][e] += df[e] * xh;
-                    acc_b[k][e] += df[e];
+                    v[1] = fmaf(g, xh, v[1]);
+                    acc_g[k][e] = fmaf(df[k][e], xh, acc_g[k][e]);
+                    acc_b[k][e] += df[k][e];
                 }
             }
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
             if (v[2] != 0.f) { failed = true; break; }
-            const float A = v[0] * (1.0f / H), B = v[1] * (1.0f / H);
+            const float rsA = rs * v[0] * (1.0f / H), rsB = rs * v[1] * (1.0f / H);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xf[8], df[8], gf[8], o[8];
-                unpack8(v0[k], xf);
-                unpack8(v1[k], df);
-                unpack8(prm0[k], gf);
+                float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = rs * (df[e] * gf[e] - A - (xf[e] - mu) * rs * B);
+                for (int e = 0; e < 8; ++e) {
+                    const float xh = fmaf(xf[k][e], rs, nmr);
+                    o[e] = fmaf(-xh, rsB, fmaf(rs, df[k][e] * wf[k][e], -rsA));
+                }
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
         }

@@ -6,8 +6,8 @@
 // loops are all static ("optimize inner persistent scheduler for static
 // fusion", description item 2(1): static bdimx when the hidden size is
 // fixed; bdimx a multiple of the warp size).  Each thread loads its VPT
-// 128-bit vectors once, keeps the row in registers (the fused kernel as the
-// fp32 sum, the others as packed bf16 widened on each pass), and reduces it
+// 128-bit vectors once, keeps the row in registers (fp32 for the fused and
+// LayerNorm kernels, packed bf16 widened per pass for RMSNorm), and reduces it
 // in the same pass that loads it (the page's compute-with-first-consumer
 // change): sum of squares for RMSNorm; for LayerNorm the sum, then the
 // centered sum of squares over the resident values (two passes, no reload).
@@ -141,18 +141,18 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
         const bool active = row < rows;
-        // the row stays packed (bf16) in registers and is widened per pass
-        uint4 xv[G::VPT];
+        // the row is widened once and centered in place; y = fma(x - mean, rstd * gamma, beta)
+        float f[G::VPT][8];
         float acc[1] = {0.f};
         if (active) {
+            uint4 xv[G::VPT];
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float f[8];
-                unpack8(xv[k], f);
+                unpack8(xv[k], f[k]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[0] += f[e];
+                for (int e = 0; e < 8; ++e) acc[0] += f[k][e];
             }
         }
         group_sum<G::TPR, 1>(acc, red1, group, t);
@@ -160,15 +160,12 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
         float sq[1] = {0.f};
         if (active) {
 #pragma unroll
-            for (int k = 0; k < G::VPT; ++k) {
-                float f[8];
-                unpack8(xv[k], f);
+            for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = f[e] - mean;
-                    sq[0] += d * d;
+                    f[k][e] -= mean;
+                    sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
                 }
-            }
         }
         group_sum<G::TPR, 1>(sq, red2, group, t);
         if (active) {
@@ -176,12 +173,11 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float f[8], gf[8], bf[8], o[8];
-                unpack8(xv[k], f);
+                float gf[8], bf[8], o[8];
                 unpack8(ld_param(gamma + v * kVec), gf);
                 unpack8(ld_param(beta + v * kVec), bf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gf[e] + bf[e];
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(f[k][e], rstd * gf[e], bf[e]);
                 st_stream(y + row * H + v * kVec, pack8(o));
             }
             if (t == 0) {

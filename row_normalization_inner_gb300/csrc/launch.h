@@ -94,6 +94,13 @@ bool dyn_shape(int op, int64_t hidden, int* threads);
 int64_t dyn_max_hidden(int op);
 cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st);
 
+// Grid-parallel inner normalization for long rows (runtime hidden, one row
+// per cluster of `ctas` CTAs).  Forward up to long_max_hidden(op) = 262144,
+// backward up to 131072.  op numbering as for the runtime-hidden path.
+bool long_shape(int op, int64_t hidden, int* ctas, int* threads, int* slice);
+int64_t long_max_hidden(int op);
+cudaError_t launch_long(int op, const DynArgs& a, int grid, cudaStream_t st);
+
 // Bounded-wait self test (see nf_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
 

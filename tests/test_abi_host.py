@@ -63,7 +63,7 @@ def test_status_strings_and_version():
 
 # ---------------------------------------------------------------- validation
 
-@pytest.mark.parametrize("hidden", [0, 1, 4, 12, 1002, 4095, 32776, 65536, -4096])
+@pytest.mark.parametrize("hidden", [0, 1, 4, 12, 1002, 4095, 262152, 1 << 20, -4096])
 def test_unsupported_hidden(hidden):
     assert nf.nf_fused_add_rmsnorm(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_rmsnorm_fwd(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
@@ -74,13 +74,49 @@ def test_unsupported_hidden(hidden):
 
 
 def test_backward_hidden_limit():
-    # the runtime-hidden backward kernels stop at 16384; the forward ones at 32768
-    for h in (16392, 24576, 32768):
+    # backward rows go up to 131072 (cluster path beyond 16384); forward to 262144
+    for h in (131080, 262144):
         assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, h, A, 1 << 30, None) == \
             nf.NF_ERR_UNSUPPORTED_HIDDEN
         assert nf.nf_rmsnorm_bwd(A, B, C, D, A, 4, h, 1e-6, B, 1 << 30, None) == \
             nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32768, 152)[1]["path"] == "dynamic"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32776, 152)[1]["path"] == "cluster"
+    assert nf.nf_plan_compute("layernorm_bwd", 4, 16392, 152)[1]["path"] == "cluster"
+
+
+@pytest.mark.parametrize("hidden", [32776, 40000, 65536, 131072, 200008, 262144])
+def test_long_row_plans(hidden):
+    for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
+        bwd = op.endswith("_bwd")
+        if bwd and hidden > nf.LONG_MAX_HIDDEN_BWD:
+            assert nf.nf_plan_compute(op, 16, hidden, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
+            continue
+        for rows in (1, 7, 5000):
+            st, p = nf.nf_plan_compute(op, rows, hidden, 152)
+            assert st == nf.NF_OK and p["path"] == "cluster", (op, hidden, p)
+            c, t = p["cluster"], p["block"]
+            assert c in (2, 4, 8) and t % 32 == 0 and t <= (512 if bwd else 1024)
+            assert p["grid"] % c == 0
+            # the C slices of 4 vectors per thread cover the row
+            assert c * t * 4 * 8 >= hidden
+            if bwd:
+                assert p["launches"] == 2 and p["partials"] == p["grid"] // c
+                assert p["partials"] == max(1, min(rows, 152 // c))
+            else:
+                assert p["launches"] == 1 and p["grid"] == rows * c
+        for path in ("reg", "bulk", "dynamic"):
+            assert nf.nf_plan_compute(op, 16, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
+
+
+def test_cluster_path_forced_for_any_hidden():
+    # non-compiled sizes run the long-row kernels when the cluster family is forced
+    for op in ("rmsnorm_fwd", "layernorm_bwd"):
+        st, p = nf.nf_plan_compute(op, 64, 3072, 152, "cluster")
+        assert st == nf.NF_OK and p["path"] == "cluster" and p["cluster"] == 2
+    # backward at a compiled size also uses the long-row cluster kernel
+    st, p = nf.nf_plan_compute("layernorm_bwd", 64, 4096, 152, "cluster")
+    assert st == nf.NF_OK and p["launches"] == 2 and p["partials"] >= 1
 
 
 @pytest.mark.parametrize("hidden", [8, 24, 264, 768, 1000, 3072, 6144, 14336, 16384, 32768])
@@ -88,7 +124,8 @@ def test_dynamic_plans(hidden):
     for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
         bwd = op.endswith("_bwd")
         if bwd and hidden > nf.DYN_MAX_HIDDEN_BWD:
-            assert nf.nf_plan_compute(op, 16, hidden, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
+            # beyond the runtime-hidden backward limit the long-row cluster path takes over
+            assert nf.nf_plan_compute(op, 16, hidden, 152)[1]["path"] == "cluster"
             continue
         for rows in (1, 77, 16384):
             st, p = nf.nf_plan_compute(op, rows, hidden, 152)
@@ -101,8 +138,9 @@ def test_dynamic_plans(hidden):
                 assert p["grid"] <= min(rows, 152 * max(1, 1024 // p["block"]))
             else:
                 assert p["launches"] == 1 and p["grid"] == rows
-        for path in ("reg", "cluster", "bulk"):
+        for path in ("reg", "bulk"):
             assert nf.nf_plan_compute(op, 16, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
+        assert nf.nf_plan_compute(op, 16, hidden, 152, "cluster")[1]["path"] == "cluster"
 
 
 def test_compiled_sizes_can_be_forced_dynamic():
@@ -264,10 +302,9 @@ def test_backward_plans(hidden, rows):
         assert bounds[0] == 0 and bounds[-1] == rows
         assert all(b1 >= b0 for b0, b1 in zip(bounds, bounds[1:]))
         assert max(b1 - b0 for b0, b1 in zip(bounds, bounds[1:])) <= -(-rows // n)
-    assert nf.nf_plan_compute("layernorm_bwd", 16, hidden, 152, "cluster")[0] == \
-        nf.NF_ERR_UNSUPPORTED_PATH
-    assert nf.nf_plan_compute("rmsnorm_bwd", 16, hidden, 152, "cluster")[0] == \
-        nf.NF_ERR_UNSUPPORTED_PATH
+    for op in ("layernorm_bwd", "rmsnorm_bwd"):
+        st, cp = nf.nf_plan_compute(op, 16, hidden, 152, "cluster")
+        assert st == nf.NF_OK and cp["path"] == "cluster" and cp["launches"] == 2
     for path in ("reg", "bulk"):
         a = nf.nf_plan_compute("rmsnorm_bwd", rows, hidden, 152, path)[1]
         b = nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152, path)[1]
