@@ -45,18 +45,22 @@ enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3, kRmsBwd = 4 };
 // CTA is then 128 * k threads), which setmaxnreg requires: it is executed
 // by all four warps of a warp group together, so a partial warp group
 // would wait forever.
-template <int H> struct BulkRow;                        // GW, fwd NG, bwd NG
-template <> struct BulkRow<1024>  { static constexpr int GW = 1,  NGF = 16, NGB = 8; };
-template <> struct BulkRow<2048>  { static constexpr int GW = 2,  NGF = 8,  NGB = 4; };
-template <> struct BulkRow<4096>  { static constexpr int GW = 4,  NGF = 4,  NGB = 2; };
-template <> struct BulkRow<5120>  { static constexpr int GW = 4,  NGF = 4,  NGB = 2; };  // 5 vectors/thread
-template <> struct BulkRow<8192>  { static constexpr int GW = 8,  NGF = 2,  NGB = 1; };
-template <> struct BulkRow<12288> { static constexpr int GW = 12, NGF = 1,  NGB = 1; };
+// Forward: GW warps per row, NGF groups; backward: GWB warps per row, NGB
+// groups (backward rows carry column accumulators, so most backward CTAs
+// stay at 384 threads, where consumers get 232 registers).
+template <int H> struct BulkRow;
+template <> struct BulkRow<1024>  { static constexpr int GW = 1,  NGF = 16, GWB = 1, NGB = 8; };
+template <> struct BulkRow<2048>  { static constexpr int GW = 2,  NGF = 8,  GWB = 2, NGB = 4; };
+template <> struct BulkRow<4096>  { static constexpr int GW = 4,  NGF = 4,  GWB = 4, NGB = 2; };
+template <> struct BulkRow<5120>  { static constexpr int GW = 4,  NGF = 4,  GWB = 4, NGB = 2; };  // 5 vectors/thread
+template <> struct BulkRow<8192>  { static constexpr int GW = 8,  NGF = 2,  GWB = 8, NGB = 1; };
+template <> struct BulkRow<12288> { static constexpr int GW = 12, NGF = 1,  GWB = 12, NGB = 1; };
 
 template <int OP, int H>
 struct BulkShape {
-    static constexpr int GW = BulkRow<H>::GW;
-    static constexpr int NG = (OP == 3 || OP == 4) ? BulkRow<H>::NGB : BulkRow<H>::NGF;
+    static constexpr bool BWD = OP == 3 || OP == 4;
+    static constexpr int GW = BWD ? BulkRow<H>::GWB : BulkRow<H>::GW;
+    static constexpr int NG = BWD ? BulkRow<H>::NGB : BulkRow<H>::NGF;
 };
 
 constexpr int kSmemBudget = 200 * 1024;  // ring + barriers + reduction scratch
@@ -242,10 +246,12 @@ norm_bulk_kernel(BulkArgs a) {
         prm0[k] = ld_param(a.p0 + (k * G::GT + gt) * kVec);
     }
     constexpr bool kBwd = OP == kLnBwd || OP == kRmsBwd;
-    // Backward consumers keep gamma / w widened to fp32 for the whole stripe
-    // (they run with the larger register share), so no row re-widens it.
-    float wf[kBwd ? G::VPT : 1][8];
-    if constexpr (kBwd) {
+    // Backward consumers with a large register share keep gamma / w widened
+    // to fp32 for the whole stripe, so no row re-widens it; with a smaller
+    // share (the 512-thread hidden-12288 shape) it stays packed.
+    constexpr bool kCacheW = kBwd && G::CONS_REGS >= 200;
+    float wf[kCacheW ? G::VPT : 1][8];
+    if constexpr (kCacheW) {
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) unpack8(prm0[k], wf[k]);
     }
@@ -357,16 +363,25 @@ norm_bulk_kernel(BulkArgs a) {
         } else if constexpr (OP == kRmsBwd) {
             // rstd recomputed from the row: rs = rsqrt(sum x^2 / H + eps),
             // dx = rs * g - x * (rs^3 * sum(g x) / H) with g = dy * w
-            float xf[G::VPT][8], df[G::VPT][8];
+            // the row is widened once when the register share allows,
+            // otherwise vector by vector on each pass
+            float xf[kCacheW ? G::VPT : 1][8], df[kCacheW ? G::VPT : 1][8];
             float v[3] = {0.f, 0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(v0[k], xf[k]);
-                unpack8(v1[k], df[k]);
+                float xk[8], dk[8], wk[8];
+                unpack8(v0[k], xk);
+                unpack8(v1[k], dk);
+                if constexpr (kCacheW) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { xf[k][e] = xk[e]; df[k][e] = dk[e]; wk[e] = wf[k][e]; }
+                } else {
+                    unpack8(prm0[k], wk);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    v[0] = fmaf(xf[k][e], xf[k][e], v[0]);
-                    v[1] = fmaf(df[k][e] * wf[k][e], xf[k][e], v[1]);
+                    v[0] = fmaf(xk[e], xk[e], v[0]);
+                    v[1] = fmaf(dk[e] * wk[e], xk[e], v[1]);
                 }
             }
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
@@ -375,11 +390,19 @@ norm_bulk_kernel(BulkArgs a) {
             const float c = rs * rs * rs * v[1] * (1.0f / H);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float o[8];
+                float xk[8], dk[8], wk[8], o[8];
+                if constexpr (kCacheW) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { xk[e] = xf[k][e]; dk[e] = df[k][e]; wk[e] = wf[k][e]; }
+                } else {
+                    unpack8(v0[k], xk);
+                    unpack8(v1[k], dk);
+                    unpack8(prm0[k], wk);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    o[e] = fmaf(-xf[k][e], c, rs * (df[k][e] * wf[k][e]));
-                    acc_g[k][e] = fmaf(df[k][e] * xf[k][e], rs, acc_g[k][e]);
+                    o[e] = fmaf(-xk[e], c, rs * (dk[e] * wk[e]));
+                    acc_g[k][e] = fmaf(dk[e] * xk[e], rs, acc_g[k][e]);
                 }
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }
@@ -389,20 +412,27 @@ norm_bulk_kernel(BulkArgs a) {
             const float mu = nmu, rs = nrs;
             if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
             const float nmr = -mu * rs;
-            float xf[G::VPT][8], df[G::VPT][8];
+            float xf[kCacheW ? G::VPT : 1][8], df[kCacheW ? G::VPT : 1][8];
             float v[3] = {0.f, 0.f, fail};
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(v0[k], xf[k]);
-                unpack8(v1[k], df[k]);
+                float xk[8], dk[8], wk[8];
+                unpack8(v0[k], xk);
+                unpack8(v1[k], dk);
+                if constexpr (kCacheW) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { xf[k][e] = xk[e]; df[k][e] = dk[e]; wk[e] = wf[k][e]; }
+                } else {
+                    unpack8(prm0[k], wk);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float xh = fmaf(xf[k][e], rs, nmr);
-                    const float g = df[k][e] * wf[k][e];
+                    const float xh = fmaf(xk[e], rs, nmr);
+                    const float g = dk[e] * wk[e];
                     v[0] += g;
                     v[1] = fmaf(g, xh, v[1]);
-                    acc_g[k][e] = fmaf(df[k][e], xh, acc_g[k][e]);
-                    acc_b[k][e] += df[k][e];
+                    acc_g[k][e] = fmaf(dk[e], xh, acc_g[k][e]);
+                    acc_b[k][e] += dk[e];
                 }
             }
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
@@ -410,11 +440,19 @@ norm_bulk_kernel(BulkArgs a) {
             const float rsA = rs * v[0] * (1.0f / H), rsB = rs * v[1] * (1.0f / H);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float o[8];
+                float xk[8], dk[8], wk[8], o[8];
+                if constexpr (kCacheW) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { xk[e] = xf[k][e]; dk[e] = df[k][e]; wk[e] = wf[k][e]; }
+                } else {
+                    unpack8(v0[k], xk);
+                    unpack8(v1[k], dk);
+                    unpack8(prm0[k], wk);
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float xh = fmaf(xf[k][e], rs, nmr);
-                    o[e] = fmaf(-xh, rsB, fmaf(rs, df[k][e] * wf[k][e], -rsA));
+                    const float xh = fmaf(xk[e], rs, nmr);
+                    o[e] = fmaf(-xh, rsB, fmaf(rs, dk[e] * wk[e], -rsA));
                 }
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
             }

@@ -6,8 +6,9 @@
 // loops are all static ("optimize inner persistent scheduler for static
 // fusion", description item 2(1): static bdimx when the hidden size is
 // fixed; bdimx a multiple of the warp size).  Each thread loads its VPT
-// 128-bit vectors once, keeps the row in registers (fp32 for the fused and
-// LayerNorm kernels, packed bf16 widened per pass for RMSNorm), and reduces it
+// 128-bit vectors once, keeps the row in registers (fp32 for the fused
+// kernel and for LayerNorm at hidden 1024, packed bf16 widened per pass
+// otherwise), and reduces it
 // in the same pass that loads it (the page's compute-with-first-consumer
 // change): sum of squares for RMSNorm; for LayerNorm the sum, then the
 // centered sum of squares over the resident values (two passes, no reload).
@@ -141,18 +142,26 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
         const bool active = row < rows;
-        // the row is widened once and centered in place; y = fma(x - mean, rstd * gamma, beta)
-        float f[G::VPT][8];
+        // Small rows are instruction-bound: widen the row once and center it
+        // in place.  Larger rows are occupancy-bound: keep it packed (half
+        // the registers) and widen it on each pass.  Either way
+        // y = fma(x - mean, rstd * gamma, beta).
+        constexpr bool kWide = H <= 1024;
+        float f[kWide ? G::VPT : 1][8];
+        uint4 xv[G::VPT];
         float acc[1] = {0.f};
         if (active) {
-            uint4 xv[G::VPT];
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(xv[k], f[k]);
+                float tmp[8];
+                unpack8(xv[k], tmp);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[0] += f[k][e];
+                for (int e = 0; e < 8; ++e) {
+                    if constexpr (kWide) f[k][e] = tmp[e];
+                    acc[0] += tmp[e];
+                }
             }
         }
         group_sum<G::TPR, 1>(acc, red1, group, t);
@@ -160,12 +169,20 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
         float sq[1] = {0.f};
         if (active) {
 #pragma unroll
-            for (int k = 0; k < G::VPT; ++k)
+            for (int k = 0; k < G::VPT; ++k) {
+                float tmp[8];
+                if constexpr (!kWide) unpack8(xv[k], tmp);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    f[k][e] -= mean;
-                    sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
+                    if constexpr (kWide) {
+                        f[k][e] -= mean;
+                        sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
+                    } else {
+                        const float d = tmp[e] - mean;
+                        sq[0] = fmaf(d, d, sq[0]);
+                    }
                 }
+            }
         }
         group_sum<G::TPR, 1>(sq, red2, group, t);
         if (active) {
@@ -173,11 +190,19 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float gf[8], bf[8], o[8];
+                float gf[8], bf[8], o[8], xm[8];
+                if constexpr (kWide) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xm[e] = f[k][e];
+                } else {
+                    unpack8(xv[k], xm);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xm[e] -= mean;
+                }
                 unpack8(ld_param(gamma + v * kVec), gf);
                 unpack8(ld_param(beta + v * kVec), bf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(f[k][e], rstd * gf[e], bf[e]);
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(xm[e], rstd * gf[e], bf[e]);
                 st_stream(y + row * H + v * kVec, pack8(o));
             }
             if (t == 0) {

@@ -273,7 +273,7 @@ def test_forward_plans(hidden, rows):
         assert 1 <= groups <= 16 and (bk["block"] - 128) % groups == 0
         # each consumer thread of a group holds a whole number (4 or 5) of vectors of the row
         per_group = (bk["block"] - 128) // groups
-        assert (hidden // 8) % per_group == 0 and (hidden // 8) // per_group in (4, 5)
+        assert (hidden // 8) % per_group == 0 and (hidden // 8) // per_group in (4, 5, 6)
         assert bk["block"] <= 1024 and bk["smem_bytes"] <= 227 * 1024
         # whole warp groups: setmaxnreg is executed by all four warps of a warp group
         assert bk["block"] % 128 == 0
