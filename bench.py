@@ -571,6 +571,23 @@ def run_gpu(args):
     return 0
 
 
+def _source_hash(sources, span=None):
+    """sha256 over the given files; for a file with a `[kernel-span NAME]`
+    marker pair and span == NAME, only the text between the markers (so
+    edits to other kernels of the same file do not invalidate it)."""
+    import hashlib
+    h = hashlib.sha256()
+    for fn in sources:
+        with open(os.path.join(ROOT, fn), "r") as fh:
+            text = fh.read()
+        if span:
+            b, e = f"// [kernel-span {span}]", f"// [end kernel-span {span}]"
+            if b in text and e in text:
+                text = text[text.index(b):text.index(e) + len(e)]
+        h.update(text.encode())
+    return h.hexdigest()
+
+
 def _profiled_traffic(op, path, rows, hidden):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the kernel source that is built now; else None."""
@@ -579,12 +596,7 @@ def _profiled_traffic(op, path, rows, hidden):
         with open(p) as f:
             d = json.load(f)
         ent = d[f"{op} {path} {rows}x{hidden}"]
-        import hashlib
-        h = hashlib.sha256()
-        for fn in ent["sources"]:
-            with open(os.path.join(ROOT, fn), "rb") as fh:
-                h.update(fh.read())
-        if h.hexdigest() != ent["sha256"]:
+        if _source_hash(ent["sources"], ent.get("span")) != ent["sha256"]:
             return None
         return ent["dram_bytes_per_launch"]
     except Exception:

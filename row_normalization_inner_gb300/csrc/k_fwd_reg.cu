@@ -30,6 +30,7 @@ struct Geo {
 };
 
 // residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
+// [kernel-span fused_add_rmsnorm_reg]
 template <int H>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
@@ -82,6 +83,7 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
         if constexpr (G::W > 1) __syncthreads();  // `red` is reused by the next row block
     }
 }
+// [end kernel-span fused_add_rmsnorm_reg]
 
 // y <- bf16(x * rsqrt(mean(x^2) + eps) * w)
 template <int H>
