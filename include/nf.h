@@ -164,14 +164,10 @@ size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden);
  * mean/rstd are the forward's saved values (eps is folded into rstd, so
  * none is passed).  dgamma/dbeta are overwritten, not accumulated.  The
  * column sums go through `workspace` in two stages -- per-CTA partials,
- * then a fixed-order sum -- so they are deterministic.  On the bulk path
- * (the default for the compiled sizes) both stages run in one cooperative
- * launch whose CTAs meet at a grid barrier; the call first clears the
- * barrier word at the start of the workspace with a 4-byte memset on
- * `stream`.  workspace is a caller-owned device buffer, 16-byte aligned,
- * of at least nf_layernorm_bwd_workspace_size(rows, hidden) bytes; its
- * contents on entry do not matter, and a call overwrites all of it that
- * it uses.  dx may be dy or x itself (exact alias).  With
+ * then a fixed-order sum -- so they are deterministic.  workspace is a
+ * caller-owned device buffer, 16-byte aligned, of at least
+ * nf_layernorm_bwd_workspace_size(rows, hidden) bytes; its contents on
+ * entry do not matter.  dx may be dy or x itself (exact alias).  With
  * rows == 0 nothing is read and dgamma/dbeta, where not NULL, are set to 0
  * (an empty column sum). */
 nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta,
@@ -212,11 +208,10 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
  * minus the workspace: the column partials go to a fixed
  * NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES area of static device memory
  * inside the library (held by every GPU that loads the library until the
- * process exits).  A size whose workspace needs more than that area under
+ * process exits).  A size whose partials need more than that area under
  * the plan the call runs (nf_plan_query(NF_OP_LAYERNORM_BWD, ...).partials
- * * 2 * hidden * 4 bytes, plus 256 on the bulk path; about 10 MB at the
- * compiled sizes on a 152-SM GPU) returns NF_ERR_WORKSPACE_TOO_SMALL before
- * anything is launched; argument
+ * * 2 * hidden * 4 bytes; about 10 MB at the compiled sizes on a 152-SM
+ * GPU) returns NF_ERR_WORKSPACE_TOO_SMALL before anything is launched; argument
  * errors return what nf_layernorm_bwd would.  The first call on
  * each device looks up the area's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream

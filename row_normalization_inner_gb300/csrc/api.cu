@@ -76,16 +76,6 @@ nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
 // dbeta; RMSNorm: dw).
 int bwd_planes(nf_op op) { return op == NF_OP_LAYERNORM_BWD ? 2 : 1; }
 
-}  // namespace
-
-size_t bwd_workspace_need(int op, int path, int partials, int64_t hidden) {
-    const size_t slots = static_cast<size_t>(partials) * bwd_planes(static_cast<nf_op>(op)) *
-                         static_cast<size_t>(hidden) * sizeof(float);
-    return (path == NF_PATH_BULK ? kBwdBarrierBytes : 0) + slots;
-}
-
-namespace {
-
 std::atomic<int> g_forced_path{NF_PATH_AUTO};
 
 constexpr int kMaxDevices = 64;
@@ -185,7 +175,8 @@ size_t bwd_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
     for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER}) {
         nf_plan pl;
         if (nf_plan_compute(op, rows, hidden, sms, p, &pl) != NF_OK) continue;
-        const size_t b = bwd_workspace_need(op, pl.path, pl.partials, hidden);
+        const size_t b = static_cast<size_t>(pl.partials) * bwd_planes(op) *
+                         static_cast<size_t>(hidden) * sizeof(float);
         if (b > most) most = b;
     }
     return most;
@@ -305,7 +296,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.cluster = 1;
         pl.rows_per_cta = groups;  // rows being computed at once per CTA
         pl.smem_bytes = smem;
-        pl.launches = 1;  // backward: both stages in one cooperative launch
+        pl.launches = fwd ? 1 : 2;
         pl.partials = fwd ? 0 : static_cast<int32_t>(g);  // groups fold into one slot per CTA
     } else {  // register-path backward: persistent stage 1 + column reduce
         const int64_t blocks = (rows + rpc - 1) / rpc;
@@ -478,7 +469,7 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
-    const size_t need = bwd_workspace_need(NF_OP_LAYERNORM_BWD, pl.path, pl.partials, hidden);
+    const size_t need = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
     if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
     const int64_t act = rows * hidden * 2, par = hidden * 2, stat = rows * 4, grad = hidden * 4;
     const Span sdx{dx, act}, sdg{dgamma, grad}, sdb{dbeta, grad}, sws{workspace, static_cast<int64_t>(need)};
@@ -511,11 +502,9 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
-        unsigned int* arrive = static_cast<unsigned int*>(workspace);
-        float* slots = reinterpret_cast<float*>(static_cast<char*>(workspace) + kBwdBarrierBytes);
-        if (cudaMemsetAsync(arrive, 0, sizeof(unsigned int), s) != cudaSuccess) return NF_ERR_CUDA;
-        return from_cuda(launch_ln_bwd_bulk(hidden, dx, dgamma, dbeta, slots, arrive, dy, x, mean,
-                                            rstd, gamma, rows, pl.grid, status, s));
+        if (cudaError_t e = launch_ln_bwd_bulk(hidden, dx, ws, dy, x, mean, rstd, gamma, rows,
+                                               pl.grid, status, s))
+            return from_cuda(e);
     } else if (cudaError_t e = launch_ln_bwd_reg(hidden, dx, ws, dy, x, mean, rstd, gamma, rows,
                                                  pl.grid, s)) {
         return from_cuda(e);
@@ -544,7 +533,7 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_RMSNORM_BWD, rows, hidden, &pl)) return st;
-    const size_t need = bwd_workspace_need(NF_OP_RMSNORM_BWD, pl.path, pl.partials, hidden);
+    const size_t need = static_cast<size_t>(pl.partials) * static_cast<size_t>(hidden) * sizeof(float);
     if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
     const int64_t act = rows * hidden * 2, par = hidden * 2, grad = hidden * 4;
     const Span sdx{dx, act}, sdw{dw, grad}, sws{workspace, static_cast<int64_t>(need)};
@@ -573,11 +562,9 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
-        unsigned int* arrive = static_cast<unsigned int*>(workspace);
-        float* slots = reinterpret_cast<float*>(static_cast<char*>(workspace) + kBwdBarrierBytes);
-        if (cudaMemsetAsync(arrive, 0, sizeof(unsigned int), s) != cudaSuccess) return NF_ERR_CUDA;
-        return from_cuda(launch_rms_bwd_bulk(hidden, dx, dw, slots, arrive, dy, x, weight, rows, eps,
-                                             pl.grid, status, s));
+        if (cudaError_t e = launch_rms_bwd_bulk(hidden, dx, ws, dy, x, weight, rows, eps, pl.grid,
+                                                status, s))
+            return from_cuda(e);
     } else if (cudaError_t e = launch_rms_bwd_reg(hidden, dx, ws, dy, x, weight, rows, eps,
                                                   pl.grid, s)) {
         return from_cuda(e);

@@ -103,8 +103,7 @@ struct BGeo {
     static constexpr int RING = S * STAGE_BYTES;
     static constexpr int BAR_OFF = RING;                     // full[S], empty[S]
     static constexpr int RED_OFF = BAR_OFF + 2 * S * 8;
-    static constexpr int FLAG_OFF = RED_OFF + NG * RED_PER_GROUP * 4;  // one int
-    static constexpr int SMEM = FLAG_OFF + 16;
+    static constexpr int SMEM = RED_OFF + NG * RED_PER_GROUP * 4;
 };
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -112,14 +111,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
-
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int lane_of(int t) { return t & 31; }
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -164,9 +155,6 @@ struct BulkArgs {
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
     float* ws;               // bwd column partials [grid][planes][H], one slot per CTA
-    float* grad0;            // bwd final column sums: dgamma / dw
-    float* grad1;            // dbeta
-    unsigned int* arrive;    // bwd grid barrier counter (zeroed before the launch)
     int* status;
     int64_t rows;
     float eps;
@@ -470,6 +458,10 @@ norm_bulk_kernel(BulkArgs a) {
             }
         }
     }
+    // This CTA's rows are done: let a programmatically dependent launch
+    // (the column reduction of the backward ops) start scheduling.  It still
+    // waits for this grid to finish before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if constexpr (kBwd) {
         // Fold the NG groups' column partials into one slot per CTA, in
         // group order: each group parks its partials in its own ring slice
@@ -501,81 +493,11 @@ norm_bulk_kernel(BulkArgs a) {
             }
             out[c4] = acc;
         }
-        // Every CTA now meets at a grid barrier (the launch is cooperative,
-        // so all CTAs are resident; the counter was zeroed by the host just
-        // before the launch, which keeps graph replays correct), then each
-        // warp reduces float4 columns over all slots in a fixed order: lane
-        // l sums slots l, l+32, ..., and the 32 lane sums meet in a fixed
-        // xor-shuffle tree.  A CTA that gives up on the barrier records
-        // NF_ERR_TIMEOUT and leaves the gradients unwritten.
-        volatile int* flag = reinterpret_cast<volatile int*>(smem + G::FLAG_OFF);
-        __threadfence();
-        named_sync(kConsumersBarrier, G::NCT);
-        if (ct == 0) {
-            atomicAdd(a.arrive, 1u);
-            const unsigned int want = gridDim.x;
-            bool ok = true;
-            if (ld_acquire_gpu(a.arrive) < want) {
-                const uint64_t t0 = global_ns();
-                while (ld_acquire_gpu(a.arrive) < want) {
-                    if (global_ns() - t0 > kWaitLimitNs) { ok = false; break; }
-                }
-            }
-            *flag = ok ? 1 : 0;
-        }
-        named_sync(kConsumersBarrier, G::NCT);
-        if (*flag == 0) {
-            if (ct == 0) record_status(a.status, kStatusTimeout);
-            return;
-        }
-        __threadfence();
-        const int warp = ct >> 5;
-        const int64_t total4 = static_cast<int64_t>(NP) * H / 4;
-        const int P = gridDim.x;
-        const float4* all = reinterpret_cast<const float4*>(a.ws);
-        for (int64_t c4 = static_cast<int64_t>(blockIdx.x) * (G::NCT / 32) + warp; c4 < total4;
-             c4 += static_cast<int64_t>(P) * (G::NCT / 32)) {
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = lane_of(ct); p < P; p += 32) {
-                const float4 v = __ldcg(all + static_cast<int64_t>(p) * total4 + c4);
-                t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                t.x += __shfl_xor_sync(0xFFFFFFFFu, t.x, off);
-                t.y += __shfl_xor_sync(0xFFFFFFFFu, t.y, off);
-                t.z += __shfl_xor_sync(0xFFFFFFFFu, t.z, off);
-                t.w += __shfl_xor_sync(0xFFFFFFFFu, t.w, off);
-            }
-            if (lane_of(ct) == 0) {
-                const int64_t col = c4 * 4;
-                float* dst = (col < H) ? a.grad0 + col : a.grad1 + (col - H);
-                *reinterpret_cast<float4*>(dst) = t;
-            }
-        }
     }
     if (failed && gt == 0) record_status(a.status, kStatusTimeout);
 }
 
 namespace {
-
-// Backward launches are cooperative (their CTAs meet at a grid barrier, so
-// all of them must be resident at once); forward launches are plain.
-template <typename Kernel>
-cudaError_t launch_bulk_kernel(Kernel k, const BulkArgs& a, int grid, int threads, int smem,
-                               cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = a.arrive ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, a);
-}
 
 template <int OP, int H>
 cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
@@ -604,7 +526,7 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             attr_set[1] = true;
         }
-        return launch_bulk_kernel(norm_bulk_kernel<OP, H, true>, a, grid, G::THREADS, G::SMEM, st);
+        norm_bulk_kernel<OP, H, true><<<grid, G::THREADS, G::SMEM, st>>>(a);
     } else {
         if (!attr_set[0]) {
             cudaError_t e = cudaFuncSetAttribute(norm_bulk_kernel<OP, H, false>,
@@ -612,8 +534,9 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             attr_set[0] = true;
         }
-        return launch_bulk_kernel(norm_bulk_kernel<OP, H, false>, a, grid, G::THREADS, G::SMEM, st);
+        norm_bulk_kernel<OP, H, false><<<grid, G::THREADS, G::SMEM, st>>>(a);
     }
+    return cudaGetLastError();
 }
 
 template <int OP>
@@ -689,14 +612,10 @@ cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd
     return launch_bulk_op<kLnFwd>(hidden, a, grid, st);
 }
 
-cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* dgamma, float* dbeta, float* ws,
-                               unsigned int* arrive, const void* dy, const void* x,
+cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st) {
     BulkArgs a{};
-    a.grad0 = dgamma;
-    a.grad1 = dbeta;
-    a.arrive = arrive;
     a.out0 = static_cast<uint16_t*>(dx);
     a.in0 = static_cast<const uint16_t*>(x);
     a.in1 = static_cast<const uint16_t*>(dy);
@@ -709,12 +628,10 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* dgamma, float* d
     return launch_bulk_op<kLnBwd>(hidden, a, grid, st);
 }
 
-cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* dw, float* ws, unsigned int* arrive,
-                                const void* dy, const void* x, const void* w, int64_t rows,
-                                float eps, int grid, int* status, cudaStream_t st) {
+cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                                const void* w, int64_t rows, float eps, int grid, int* status,
+                                cudaStream_t st) {
     BulkArgs a{};
-    a.grad0 = dw;
-    a.arrive = arrive;
     a.out0 = static_cast<uint16_t*>(dx);
     a.in0 = static_cast<const uint16_t*>(x);
     a.in1 = static_cast<const uint16_t*>(dy);

@@ -63,26 +63,16 @@ cudaError_t launch_rms_bulk(int64_t hidden, void* y, const void* x, const void* 
 cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                                const void* gamma, const void* beta, int64_t rows, float eps,
                                int grid, int* status, cudaStream_t st);
-// LayerNorm backward on the bulk path, both stages in one cooperative
-// launch: one column-partial slot per CTA (the row groups fold theirs
-// inside the CTA), a grid barrier on `*arrive` (which must be 0 at launch),
-// then a fixed-order reduction of the slots into dgamma / dbeta.
-cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* dgamma, float* dbeta, float* ws,
-                               unsigned int* arrive, const void* dy, const void* x,
+// Stage 1 of LayerNorm backward on the bulk path: one column-partial slot
+// per CTA (the row groups fold theirs inside the CTA).
+cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st);
 
-// RMSNorm backward on the bulk path, both stages in one cooperative launch
-// (as above; one plane, dw).
-cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* dw, float* ws, unsigned int* arrive,
-                                const void* dy, const void* x, const void* w, int64_t rows,
-                                float eps, int grid, int* status, cudaStream_t st);
-
-// Workspace bytes a backward call needs under `plan` (op 3 LayerNorm, 4
-// RMSNorm): the column-partial slots, plus, on the bulk path, a 256-byte
-// header holding the grid barrier counter in front of them.
-size_t bwd_workspace_need(int op, int path, int partials, int64_t hidden);
-constexpr size_t kBwdBarrierBytes = 256;
+// RMSNorm backward, stage 1 on the bulk path (one slot of ws[slot][hidden] per CTA).
+cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                                const void* w, int64_t rows, float eps, int grid, int* status,
+                                cudaStream_t st);
 
 // Runtime-hidden path (any hidden that is a multiple of 8 up to
 // dyn_max_hidden(op)).  op: 0 fused, 1 rms fwd, 2 ln fwd, 3 ln bwd, 4 rms bwd.

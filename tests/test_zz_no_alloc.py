@@ -28,10 +28,8 @@ def built():
 
 
 def _need(rows, hidden):
-    """Scratch bytes the plan of this call uses: partial slots x 2 planes x
-    hidden fp32, plus the 256-byte grid-barrier header on the bulk path."""
-    p = nf.nf_plan_query("layernorm_bwd", rows, hidden)
-    return p["partials"] * 2 * hidden * 4 + (256 if p["path"] == "bulk" else 0)
+    """Scratch bytes the plan of this call uses: partial slots x 2 planes x hidden fp32."""
+    return nf.nf_plan_query("layernorm_bwd", rows, hidden)["partials"] * 2 * hidden * 4
 
 
 def _case(rows, hidden, seed):
