@@ -23,6 +23,10 @@ Operations and where the pages name them:
   rmsnorm_bwd        -- the RMS norm counterpart of the same combined
                         reduction ("TMA inner persistent scheduler",
                         description: RMS norm with workspace support).
+  outer_norm_fwd,
+  outer_norm_bwd     -- outer normalization (statistics per column, over the
+                        rows), listed among the normalization variants in
+                        the "Llu/ln bwd" discussion.
 """
 from __future__ import annotations
 
@@ -65,9 +69,11 @@ def _bind(lib):
     lib.or_layernorm_fwd.argtypes = [_D, _D, _D, _I64, _I64, ctypes.c_double, _D, _D, _D]
     lib.or_layernorm_bwd.argtypes = [_D, _D, _D, _D, _D, _I64, _I64, _D, _D, _D]
     lib.or_rmsnorm_bwd.argtypes = [_D, _D, _D, _D, _I64, _I64, _D, _D]
+    lib.or_outer_norm_fwd.argtypes = [_D, _D, _D, _I64, _I64, ctypes.c_double, _D, _D, _D]
+    lib.or_outer_norm_bwd.argtypes = [_D, _D, _D, _D, _D, _I64, _I64, _D, _D, _D]
     for f in (lib.or_bf16_to_double_array, lib.or_double_to_bf16_array, lib.or_rmsnorm_fwd,
               lib.or_fused_add_rmsnorm, lib.or_layernorm_fwd, lib.or_layernorm_bwd,
-              lib.or_rmsnorm_bwd):
+              lib.or_rmsnorm_bwd, lib.or_outer_norm_fwd, lib.or_outer_norm_bwd):
         f.restype = None
     return lib
 
@@ -211,3 +217,37 @@ def rmsnorm_bwd(dy, x, rstd, w):
     dw = np.empty(hidden, dtype=np.float64)
     _load().or_rmsnorm_bwd(_dp(dy), _dp(x), _dp(rstd), _dp(w), rows, hidden, _dp(dx), _dp(dw))
     return dx, dw
+
+
+def outer_norm_fwd(x, gamma, beta, eps: float):
+    """Per-column normalization over the rows (biased variance).
+
+    Returns (y [rows, hidden], mean [hidden], rstd [hidden]) in float64."""
+    x = _f64(x)
+    rows, hidden = x.shape
+    g = _f64(gamma, (hidden,))
+    b = _f64(beta, (hidden,))
+    y = np.empty_like(x)
+    mean = np.empty(hidden, dtype=np.float64)
+    rstd = np.empty(hidden, dtype=np.float64)
+    _load().or_outer_norm_fwd(_dp(x), _dp(g), _dp(b), rows, hidden, float(eps),
+                              _dp(y), _dp(mean), _dp(rstd))
+    return y, mean, rstd
+
+
+def outer_norm_bwd(dy, x, mean, rstd, gamma):
+    """Gradients of sum(dy * OuterNorm(x)) given the saved per-column mean/rstd.
+
+    Returns (dx, dgamma, dbeta) in float64."""
+    x = _f64(x)
+    rows, hidden = x.shape
+    dy = _f64(dy, (rows, hidden))
+    mean = _f64(mean, (hidden,))
+    rstd = _f64(rstd, (hidden,))
+    g = _f64(gamma, (hidden,))
+    dx = np.empty_like(x)
+    dgamma = np.empty(hidden, dtype=np.float64)
+    dbeta = np.empty(hidden, dtype=np.float64)
+    _load().or_outer_norm_bwd(_dp(dy), _dp(x), _dp(mean), _dp(rstd), _dp(g), rows, hidden,
+                              _dp(dx), _dp(dgamma), _dp(dbeta))
+    return dx, dgamma, dbeta

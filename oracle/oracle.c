@@ -221,3 +221,60 @@ void or_rmsnorm_bwd(const double* dy, const double* x, const double* rstd, const
         for (int64_t j = 0; j < hidden; ++j)
             dw[j] += dy[r * hidden + j] * x[r * hidden + j] * rstd[r];
 }
+
+/* ---- outer normalization (per column, over the rows) -----------------------
+ * "Llu/ln bwd" lists block- and grid-parallel outer normalization among the
+ * normalization variants: the statistics run across the rows, one set per
+ * column (batch normalization of a [rows, hidden] matrix, training mode):
+ *   mean_j = (1/R) sum_r x[r][j] ; var_j = (1/R) sum_r (x[r][j] - mean_j)^2 (biased)
+ *   rstd_j = 1/sqrt(var_j + eps) ; y[r][j] = (x[r][j] - mean_j) * rstd_j * gamma[j] + beta[j] */
+void or_outer_norm_fwd(const double* x, const double* gamma, const double* beta,
+                       int64_t rows, int64_t hidden, double eps,
+                       double* y, double* mean_out, double* rstd_out) {
+    for (int64_t j = 0; j < hidden; ++j) {
+        double sum = 0.0;
+        for (int64_t r = 0; r < rows; ++r) sum += x[r * hidden + j];
+        double mean = sum / (double)rows;
+        double sq = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            double d = x[r * hidden + j] - mean;
+            sq += d * d;
+        }
+        double var = sq / (double)rows;
+        double rstd = 1.0 / sqrt(var + eps);
+        for (int64_t r = 0; r < rows; ++r)
+            y[r * hidden + j] = (x[r * hidden + j] - mean) * rstd * gamma[j] + beta[j];
+        if (mean_out) mean_out[j] = mean;
+        if (rstd_out) rstd_out[j] = rstd;
+    }
+}
+
+/* Gradient of L = sum dy * y for the outer normalization above, with the
+ * saved per-column mean/rstd treated as functions of x:
+ *   xhat = (x - mean_j) * rstd_j ; g = dy * gamma[j]
+ *   dx[r][j] = rstd_j * ( g - (1/R) sum_s g[s][j] - xhat * (1/R) sum_s g[s][j] * xhat[s][j] )
+ *   dgamma[j] = sum_r dy[r][j] * xhat[r][j] ; dbeta[j] = sum_r dy[r][j] */
+void or_outer_norm_bwd(const double* dy, const double* x, const double* mean, const double* rstd,
+                       const double* gamma, int64_t rows, int64_t hidden,
+                       double* dx, double* dgamma, double* dbeta) {
+    for (int64_t j = 0; j < hidden; ++j) {
+        double sum_g = 0.0, sum_gx = 0.0, sum_dy = 0.0, sum_dyx = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            double xhat = (x[r * hidden + j] - mean[j]) * rstd[j];
+            double g = dy[r * hidden + j] * gamma[j];
+            sum_g += g;
+            sum_gx += g * xhat;
+            sum_dy += dy[r * hidden + j];
+            sum_dyx += dy[r * hidden + j] * xhat;
+        }
+        double mean_g = sum_g / (double)rows;
+        double mean_gx = sum_gx / (double)rows;
+        for (int64_t r = 0; r < rows; ++r) {
+            double xhat = (x[r * hidden + j] - mean[j]) * rstd[j];
+            double g = dy[r * hidden + j] * gamma[j];
+            dx[r * hidden + j] = rstd[j] * (g - mean_g - xhat * mean_gx);
+        }
+        dgamma[j] = sum_dyx;
+        dbeta[j] = sum_dy;
+    }
+}

@@ -377,3 +377,73 @@ def test_rmsnorm_bwd_matches_torch_autograd_fp64():
     dx, dw = oracle.rmsnorm_bwd(dy, x.detach().numpy(), rstd, w.detach().numpy())
     np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-10, atol=1e-11)
     np.testing.assert_allclose(dw, w.grad.numpy(), rtol=1e-10, atol=1e-11)
+
+
+# ---------------------------------------------------------------- outer normalization pins
+
+def test_outer_norm_column_moments():
+    rng = np.random.default_rng(30)
+    x = rng.standard_normal((513, 64)) * rng.uniform(0.1, 5, 64) + rng.uniform(-3, 3, 64)
+    eps = 1e-5
+    y, mean, rstd = oracle.outer_norm_fwd(x, np.ones(64), np.zeros(64), eps)
+    var = x.var(axis=0)
+    assert np.max(np.abs(y.mean(axis=0))) < 1e-12
+    np.testing.assert_allclose(y.var(axis=0), var / (var + eps), rtol=1e-12)
+    np.testing.assert_allclose(mean, x.mean(axis=0), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(rstd, 1 / np.sqrt(var + eps), rtol=1e-12)
+
+
+def test_outer_norm_matches_torch_batch_norm_fp64():
+    rng = np.random.default_rng(31)
+    rows, hidden = 300, 48
+    x = torch.from_numpy(rng.standard_normal((rows, hidden)) * 2 + 0.5).requires_grad_()
+    g = torch.from_numpy(rng.standard_normal(hidden) * 0.1 + 1).requires_grad_()
+    b = torch.from_numpy(rng.standard_normal(hidden) * 0.1).requires_grad_()
+    dy = rng.standard_normal((rows, hidden))
+    y = torch.nn.functional.batch_norm(x, None, None, g, b, training=True, eps=1e-5)
+    y.backward(torch.from_numpy(dy))
+    yo, mean, rstd = oracle.outer_norm_fwd(x.detach().numpy(), g.detach().numpy(),
+                                           b.detach().numpy(), 1e-5)
+    np.testing.assert_allclose(yo, y.detach().numpy(), rtol=1e-11, atol=1e-12)
+    dx, dg, db = oracle.outer_norm_bwd(dy, x.detach().numpy(), mean, rstd, g.detach().numpy())
+    np.testing.assert_allclose(dx, x.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dg, g.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(db, b.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def _outer_loss(x, dy, g, b, eps):
+    y, _, _ = oracle.outer_norm_fwd(x, g, b, eps)
+    return float(np.sum(dy * y))
+
+
+def test_outer_norm_bwd_finite_differences():
+    rng = np.random.default_rng(32)
+    rows, hidden = 5, 3
+    x = rng.standard_normal((rows, hidden))
+    dy = rng.standard_normal((rows, hidden))
+    g = rng.standard_normal(hidden)
+    b = rng.standard_normal(hidden)
+    eps = 1e-5
+    _, mean, rstd = oracle.outer_norm_fwd(x, g, b, eps)
+    dx, dg, db = oracle.outer_norm_bwd(dy, x, mean, rstd, g)
+    h = 1e-6
+    for i in range(rows):
+        for j in range(hidden):
+            xp = x.copy(); xp[i, j] += h
+            xm = x.copy(); xm[i, j] -= h
+            fd = (_outer_loss(xp, dy, g, b, eps) - _outer_loss(xm, dy, g, b, eps)) / (2 * h)
+            assert dx[i, j] == pytest.approx(fd, rel=1e-6, abs=1e-8)
+    for j in range(hidden):
+        gp = g.copy(); gp[j] += h
+        gm = g.copy(); gm[j] -= h
+        fd = (_outer_loss(x, dy, gp, b, eps) - _outer_loss(x, dy, gm, b, eps)) / (2 * h)
+        assert dg[j] == pytest.approx(fd, rel=1e-6, abs=1e-8)
+        assert db[j] == pytest.approx(dy[:, j].sum(), rel=1e-12)
+
+
+def test_outer_norm_hand_case():
+    # one column (2, 4, 6): mean 4, var 8/3, rstd sqrt(3/8); eps = 0, gamma 2, beta 1
+    y, mean, rstd = oracle.outer_norm_fwd(np.array([[2.0], [4.0], [6.0]]), [2.0], [1.0], 0.0)
+    r = math.sqrt(3 / 8)
+    np.testing.assert_allclose(y[:, 0], [1 - 4 * r, 1.0, 1 + 4 * r], rtol=1e-14)
+    assert mean[0] == 4.0 and rstd[0] == pytest.approx(r, rel=1e-15)

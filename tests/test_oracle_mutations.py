@@ -28,6 +28,15 @@ MUTANTS = {
     "rms_bwd_sign": ("rstd[r] * (g - xhat * mean_gx);", "rstd[r] * (g + xhat * mean_gx);"),
     "rms_bwd_dw_no_rstd": ("dw[j] += dy[r * hidden + j] * x[r * hidden + j] * rstd[r];",
                            "dw[j] += dy[r * hidden + j] * x[r * hidden + j];"),
+    "outer_unbiased_var": ("double var = sq / (double)rows;", "double var = sq / (double)(rows - 1);"),
+    "outer_bwd_sign": ("dx[r * hidden + j] = rstd[j] * (g - mean_g - xhat * mean_gx);",
+                       "dx[r * hidden + j] = rstd[j] * (g - mean_g + xhat * mean_gx);"),
+    "outer_bwd_dropped_mean": ("dx[r * hidden + j] = rstd[j] * (g - mean_g - xhat * mean_gx);",
+                               "dx[r * hidden + j] = rstd[j] * (g - xhat * mean_gx);"),
+    "outer_dgamma_uses_dy": ("            sum_dyx += dy[r * hidden + j] * xhat;",
+                             "            sum_dyx += dy[r * hidden + j];"),
+    "outer_rows_transposed": ("        for (int64_t r = 0; r < rows; ++r) sum += x[r * hidden + j];",
+                              "        for (int64_t r = 0; r < rows; ++r) sum += x[j * rows + r];"),
     "bf16_ties_away": ("double r = nearbyint(d / q) * q;", "double r = round(d / q) * q;"),
     "bf16_one_bit_short": ("int qexp = e - 7;", "int qexp = e - 6;"),
     "bf16_truncate": ("double r = nearbyint(d / q) * q;", "double r = trunc(d / q) * q;"),
