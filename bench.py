@@ -81,6 +81,16 @@ def rms_bwd_bytes(rows, hidden):
     return 6 * hidden * rows + 6 * hidden
 
 
+def outer_fwd_bytes(rows, hidden):
+    # read x once, write y; gamma, beta in; mean, rstd (fp32) out
+    return 4 * hidden * rows + 12 * hidden
+
+
+def outer_bwd_bytes(rows, hidden):
+    # read x, dy once, write dx; mean, rstd, gamma in; dgamma, dbeta out
+    return 6 * hidden * rows + 26 * hidden
+
+
 # ---------------------------------------------------------------- environment helpers
 
 def measured_peaks():
@@ -306,6 +316,10 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         foot, nbytes = (4 * hidden + 8) * rows, ln_fwd_bytes(rows, hidden)
     elif op == "rmsnorm_bwd":
         foot, nbytes = 6 * hidden * rows, rms_bwd_bytes(rows, hidden)
+    elif op == "outer_norm_fwd":
+        foot, nbytes = 4 * hidden * rows, outer_fwd_bytes(rows, hidden)
+    elif op == "outer_norm_bwd":
+        foot, nbytes = 6 * hidden * rows, outer_bwd_bytes(rows, hidden)
     else:
         foot, nbytes = (6 * hidden + 8) * rows, ln_bwd_bytes(rows, hidden)
     sets = max(1, min(16384, -(-2 * l2_bytes // foot)))
@@ -344,6 +358,31 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         keep = (x, dy, w, dx, ws, dw)
         fn = lambda i, sh: lib.nf_rmsnorm_bwd(pdx + (i % sets) * a2, pdw, pdy + (i % sets) * a2,  # noqa: E731
                                                px + (i % sets) * a2, pw, rows, hidden, eps, pws, nws, sh)
+    elif op == "outer_norm_fwd":
+        # one [rows, hidden] problem per set; per-column statistics are per set
+        x, _, g, b = workloads.outer_inputs(tot, hidden, device=dev)
+        y = torch.empty_like(x)
+        m = torch.empty(hidden, device=dev)
+        rs = torch.empty(hidden, device=dev)
+        nws = max(nf.nf_outer_norm_workspace_size(rows, hidden), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        px, py, pg, pb, pm, pr, pws = (t.data_ptr() for t in (x, y, g, b, m, rs, ws))
+        keep = (x, y, g, b, m, rs, ws)
+        fn = lambda i, sh: lib.nf_outer_norm_fwd(py + (i % sets) * a2, pm, pr, px + (i % sets) * a2,  # noqa: E731
+                                                  pg, pb, rows, hidden, eps, pws, nws, sh)
+    elif op == "outer_norm_bwd":
+        x, dy, g, b = workloads.outer_inputs(tot, hidden, device=dev)
+        _, m, rs = nf.outer_norm_fwd(x[:rows], g, b, eps)
+        dx = torch.empty_like(x)
+        nws = max(nf.nf_outer_norm_workspace_size(rows, hidden), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        dg = torch.empty(hidden, device=dev)
+        db = torch.empty(hidden, device=dev)
+        px, pdy, pg, pm, pr, pdx, pws, pdg, pdb = (t.data_ptr() for t in (x, dy, g, m, rs, dx, ws, dg, db))
+        keep = (x, dy, g, m, rs, dx, ws, dg, db)
+        fn = lambda i, sh: lib.nf_outer_norm_bwd(pdx + (i % sets) * a2, pdg, pdb, pdy + (i % sets) * a2,  # noqa: E731
+                                                  px + (i % sets) * a2, pm, pr, pg, rows, hidden, pws,
+                                                  nws, sh)
     else:
         x, dy, g = workloads.layernorm_bwd_inputs(tot, hidden, device=dev)
         _, m, rs = nf.layernorm_fwd(x, g, torch.zeros_like(g), eps)
@@ -383,9 +422,9 @@ def ops_suite(nf, peak, stream, l2_bytes):
     def entry(op, rows, h, eps):
         ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        path = "outer" if op.startswith("outer") else nf.nf_plan_query(op, rows, h)["path"]
         out[f"{op} {rows}x{h}"] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                   "us": round(ms * 1e3, 3),
-                                   "path": nf.nf_plan_query(op, rows, h)["path"]}
+                                   "us": round(ms * 1e3, 3), "path": path}
 
     for h in (4096, 8192):
         for rows in (1, 2, 4, 8, 16, 32, 128):
@@ -401,6 +440,9 @@ def ops_suite(nf, peak, stream, l2_bytes):
         entry("layernorm_bwd", ROWS, h, EPS)
     for h in (4096, 8192):
         entry("rmsnorm_bwd", ROWS, h, EPS)
+    for rows, h in ((16384, 1024), (16384, 4096), (65536, 1024), (4096, 8192)):
+        entry("outer_norm_fwd", rows, h, EPS)
+        entry("outer_norm_bwd", rows, h, EPS)
     return out
 
 
@@ -606,7 +648,8 @@ def _profiled_traffic(op, path, rows, hidden):
 def run_profile_case(spec: str, reps: int):
     """Run `reps` launches of one operation at one size and exit: the small,
     self-contained command the ncu captures use.  spec = OP:ROWSxHIDDEN with
-    OP in fused_add_rmsnorm, rmsnorm_fwd, layernorm_fwd, layernorm_bwd."""
+    OP in fused_add_rmsnorm, rmsnorm_fwd, layernorm_fwd, layernorm_bwd,
+    outer_norm_fwd, outer_norm_bwd."""
     import row_normalization_inner_gb300 as nf
     from row_normalization_inner_gb300 import build as nf_build
     nf_build.build()
@@ -631,12 +674,23 @@ def run_profile_case(spec: str, reps: int):
                          dtype=torch.uint8, device=dev)
         dx = torch.empty_like(x)
         fn = lambda: nf.layernorm_bwd(dy, x, mean, rstd, g, workspace=ws, out=dx)  # noqa: E731
+    elif op in ("outer_norm_fwd", "outer_norm_bwd"):
+        x, dy, g, b = workloads.outer_inputs(rows, hidden, device=dev)
+        ws = torch.empty(max(nf.nf_outer_norm_workspace_size(rows, hidden), 16),
+                         dtype=torch.uint8, device=dev)
+        y = torch.empty_like(x)
+        _, mean, rstd = nf.outer_norm_fwd(x, g, b, EPS, workspace=ws, out=y)
+        if op == "outer_norm_fwd":
+            fn = lambda: nf.outer_norm_fwd(x, g, b, EPS, workspace=ws, out=y)  # noqa: E731
+        else:
+            fn = lambda: nf.outer_norm_bwd(dy, x, mean, rstd, g, workspace=ws, out=y)  # noqa: E731
     else:
         raise SystemExit(f"unknown op {op}")
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
-    print(f"profile case {spec}: {reps} call(s), plan {nf.nf_plan_query(op, rows, hidden)}")
+    plan = "outer" if op.startswith("outer") else nf.nf_plan_query(op, rows, hidden)
+    print(f"profile case {spec}: {reps} call(s), plan {plan}")
     return 0
 
 

@@ -224,6 +224,38 @@ nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const 
                                    const void* gamma, int64_t rows, int64_t hidden,
                                    nf_stream stream);
 
+/* Outer normalization: the statistics run down the columns, over the rows
+ * (batch normalization of a [rows, hidden] matrix in training mode; the
+ * "Llu/ln bwd" discussion lists block- and grid-parallel outer
+ * normalization among the normalization variants).  For each column j:
+ *     mean[j] = (1/R) sum_r x[r][j]
+ *     var_j   = (1/R) sum_r (x[r][j] - mean[j])^2          (biased)
+ *     rstd[j] = rsqrt(var_j + eps)
+ *     y[r][j] = bf16( (x[r][j] - mean[j]) * rstd[j] * gamma[j] + beta[j] )
+ * hidden: any multiple of 8 (no compiled-size restriction); rows >= 0
+ * (rows == 0 writes nothing).  mean/rstd ([hidden] fp32) may be NULL.  The
+ * per-column statistics are merged from row stripes in a fixed order
+ * (Chan's pairwise formula), so results are deterministic.  workspace:
+ * caller-owned, 16-byte aligned, at least
+ * nf_outer_norm_workspace_size(rows, hidden) bytes, contents irrelevant.
+ * y may be x itself. */
+size_t nf_outer_norm_workspace_size(int64_t rows, int64_t hidden);
+nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                            const void* beta, int64_t rows, int64_t hidden, float eps,
+                            void* workspace, size_t workspace_bytes, nf_stream stream);
+
+/* Outer normalization backward (saved per-column mean/rstd).  With
+ * xhat = (x - mean[j]) * rstd[j] and g = dy * gamma[j]:
+ *   dx[r][j]  = bf16( rstd[j] * ( g - (1/R) sum_s g[s][j] - xhat * (1/R) sum_s g[s][j] xhat[s][j] ) )
+ *   dgamma[j] = sum_r dy[r][j] * xhat[r][j],  dbeta[j] = sum_r dy[r][j]   (fp32, overwritten)
+ * The column sums go through `workspace` and the fixed-order column
+ * reduction.  dx may be dy or x itself.  rows == 0 sets dgamma/dbeta (if
+ * not NULL) to 0.  Same pointer and workspace rules as the forward. */
+nf_status nf_outer_norm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                            const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                            int64_t hidden, void* workspace, size_t workspace_bytes,
+                            nf_stream stream);
+
 /* Force a kernel family for every later call in this process (NF_PATH_AUTO
  * restores the library's choice).  A call whose op/size has no kernel of the
  * forced family returns NF_ERR_UNSUPPORTED_PATH.  Not thread-safe with

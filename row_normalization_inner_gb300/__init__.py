@@ -52,6 +52,7 @@ EXPORTS = (
     "nf_fused_add_rmsnorm", "nf_rmsnorm_fwd", "nf_layernorm_fwd",
     "nf_layernorm_bwd_workspace_size", "nf_layernorm_bwd",
     "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd", "nf_layernorm_bwd_noalloc",
+    "nf_outer_norm_workspace_size", "nf_outer_norm_fwd", "nf_outer_norm_bwd",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
     "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
 )
@@ -94,6 +95,9 @@ def _bind(lib):
         "nf_rmsnorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
         "nf_rmsnorm_bwd": (_S, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_layernorm_bwd_noalloc": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+        "nf_outer_norm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+        "nf_outer_norm_fwd": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
+        "nf_outer_norm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
         "nf_set_path": (_S, [_S]),
         "nf_plan_query": (_S, [_S, _I64, _I64, ctypes.POINTER(Plan)]),
         "nf_plan_compute": (_S, [_S, _I64, _I64, ctypes.c_int32, _S, ctypes.POINTER(Plan)]),
@@ -171,6 +175,22 @@ def nf_layernorm_bwd_noalloc(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, 
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20  # NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES
+
+
+def nf_outer_norm_workspace_size(rows, hidden) -> int:
+    return lib().nf_outer_norm_workspace_size(rows, hidden)
+
+
+def nf_outer_norm_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
+                      workspace_bytes, stream) -> int:
+    return lib().nf_outer_norm_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
+                                   workspace_bytes, stream)
+
+
+def nf_outer_norm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, workspace,
+                      workspace_bytes, stream) -> int:
+    return lib().nf_outer_norm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                                   workspace, workspace_bytes, stream)
 
 
 def nf_set_path(path) -> int:
@@ -317,6 +337,47 @@ def rmsnorm_bwd(dy, x, weight, eps: float = 1e-6, workspace=None, out=None, stre
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "nf_rmsnorm_bwd")
     return dx, dw
+
+
+def outer_norm_fwd(x, gamma, beta, eps: float = 1e-5, workspace=None, out=None, stream=None):
+    """Per-column normalization over the rows.  Returns (y, mean [hidden], rstd [hidden])."""
+    import torch
+    for t, n in ((x, "x"), (gamma, "gamma"), (beta, "beta")):
+        _need(t, torch.bfloat16, n)
+    rows, hidden = _rows_hidden(x)
+    y = torch.empty_like(x) if out is None else out
+    mean = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    rstd = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(nf_outer_norm_workspace_size(rows, hidden), 16),
+                                dtype=torch.uint8, device=x.device)
+    _check(nf_outer_norm_fwd(y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), x.data_ptr(),
+                             gamma.data_ptr(), beta.data_ptr(), rows, hidden, eps,
+                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                             _stream(stream)), "nf_outer_norm_fwd")
+    return y, mean, rstd
+
+
+def outer_norm_bwd(dy, x, mean, rstd, gamma, workspace=None, out=None, stream=None):
+    """Returns (dx bf16, dgamma fp32, dbeta fp32)."""
+    import torch
+    for t, n in ((dy, "dy"), (x, "x"), (gamma, "gamma")):
+        _need(t, torch.bfloat16, n)
+    _need(mean, torch.float32, "mean")
+    _need(rstd, torch.float32, "rstd")
+    rows, hidden = _rows_hidden(x)
+    dx = torch.empty_like(x) if out is None else out
+    dgamma = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    dbeta = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(max(nf_outer_norm_workspace_size(rows, hidden), 16),
+                                dtype=torch.uint8, device=x.device)
+    _check(nf_outer_norm_bwd(dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(), dy.data_ptr(),
+                             x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), gamma.data_ptr(),
+                             rows, hidden, workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream(stream)),
+           "nf_outer_norm_bwd")
+    return dx, dgamma, dbeta
 
 
 def set_path(path):

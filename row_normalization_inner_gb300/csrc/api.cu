@@ -572,6 +572,90 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
     return from_cuda(launch_column_reduce1(ws, dw, pl.partials, hidden, s));
 }
 
+size_t nf_outer_norm_workspace_size(int64_t rows, int64_t hidden) {
+    if (rows <= 0 || hidden < 8 || hidden % 8 != 0 || hidden > 0x7FFFFFFF) return 0;
+    int sms;
+    if (device_sm_count(&sms) != NF_OK) return 0;
+    return outer_workspace_bytes(rows, hidden, sms);
+}
+
+namespace {
+nf_status outer_checks(int64_t rows, int64_t hidden) {
+    if (hidden < 8 || hidden % 8 != 0 || hidden > 0x7FFFFFFF) return NF_ERR_UNSUPPORTED_HIDDEN;
+    if (rows < 0 || rows > (INT64_MAX / 8) / hidden) return NF_ERR_INVALID_ARG;
+    return NF_OK;
+}
+}  // namespace
+
+nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                            const void* beta, int64_t rows, int64_t hidden, float eps,
+                            void* workspace, size_t workspace_bytes, nf_stream stream) {
+    if (nf_status st = outer_checks(rows, hidden)) return st;
+    if (!(std::isfinite(eps) && eps > 0.f)) return NF_ERR_INVALID_ARG;
+    if (rows == 0) return NF_OK;
+    if (!y || !x || !gamma || !beta || !workspace) return NF_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(x, 16) || !aligned(gamma, 2) || !aligned(beta, 2) ||
+        !aligned(workspace, 16) || !aligned(mean, 4) || !aligned(rstd, 4))
+        return NF_ERR_MISALIGNED;
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    const size_t need = outer_workspace_bytes(rows, hidden, sms);
+    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t act = rows * hidden * 2, par = hidden * 2, stat = hidden * 4;
+    const Span sy{y, act}, sws{workspace, static_cast<int64_t>(need)};
+    const Span ins[] = {{x, act}, {gamma, par}, {beta, par}};
+    for (int i = 0; i < 3; ++i) {
+        const bool clash = i == 0 ? bad_overlap_except_alias(sy, ins[i]) : overlap(sy, ins[i]);
+        if (clash || overlap(sws, ins[i])) return NF_ERR_INVALID_ARG;
+    }
+    if (overlap(sws, sy) || overlap({mean, stat}, {rstd, stat})) return NF_ERR_INVALID_ARG;
+    for (Span o : {Span{mean, stat}, Span{rstd, stat}})
+        if (overlap(o, sy) || overlap(o, sws) || overlap(o, ins[0]) || overlap(o, ins[1]) ||
+            overlap(o, ins[2]))
+            return NF_ERR_INVALID_ARG;
+    return from_cuda(launch_outer_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
+                                      sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nf_status nf_outer_norm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                            const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                            int64_t hidden, void* workspace, size_t workspace_bytes,
+                            nf_stream stream) {
+    if (nf_status st = outer_checks(rows, hidden)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == 0) {
+        if (dgamma && !aligned(dgamma, 16)) return NF_ERR_MISALIGNED;
+        if (dbeta && !aligned(dbeta, 16)) return NF_ERR_MISALIGNED;
+        if (dgamma && cudaMemsetAsync(dgamma, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
+        if (dbeta && cudaMemsetAsync(dbeta, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
+        return NF_OK;
+    }
+    if (!dx || !dgamma || !dbeta || !dy || !x || !mean || !rstd || !gamma || !workspace)
+        return NF_ERR_INVALID_ARG;
+    if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(x, 16) || !aligned(gamma, 16) ||
+        !aligned(workspace, 16) || !aligned(dgamma, 16) || !aligned(dbeta, 16) ||
+        !aligned(mean, 4) || !aligned(rstd, 4))
+        return NF_ERR_MISALIGNED;
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    const size_t need = outer_workspace_bytes(rows, hidden, sms);
+    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t act = rows * hidden * 2, par = hidden * 2, stat = hidden * 4, grad = hidden * 4;
+    const Span sdx{dx, act}, sdg{dgamma, grad}, sdb{dbeta, grad}, sws{workspace, static_cast<int64_t>(need)};
+    const Span ins[] = {{dy, act}, {x, act}, {mean, stat}, {rstd, stat}, {gamma, par}};
+    if (overlap(sdg, sdb) || overlap(sdx, sdg) || overlap(sdx, sdb) || overlap(sws, sdx) ||
+        overlap(sws, sdg) || overlap(sws, sdb))
+        return NF_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i) {
+        const Span& in = ins[i];
+        const bool dx_clash = i < 2 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
+        if (dx_clash || overlap(sdg, in) || overlap(sdb, in) || overlap(sws, in))
+            return NF_ERR_INVALID_ARG;
+    }
+    return from_cuda(launch_outer_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                                      workspace, sms, s));
+}
+
 nf_status nf_get_device_status(nf_stream stream) {
     int* addr;
     if (nf_status st = device_status_addr(&addr)) return st;

@@ -101,6 +101,17 @@ bool long_shape(int op, int64_t hidden, int* ctas, int* threads, int* slice);
 int64_t long_max_hidden(int op);
 cudaError_t launch_long(int op, const DynArgs& a, int grid, cudaStream_t st);
 
+// Outer (per-column) normalization: row stripes per direction, workspace
+// bytes covering both directions, and the launch sequences.
+int outer_stripes(int64_t rows, int64_t hidden, int sms, bool bwd);
+size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms);
+cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                             const void* beta, int64_t rows, int64_t hidden, float eps,
+                             void* workspace, int sms, cudaStream_t st);
+cudaError_t launch_outer_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                             const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                             int64_t hidden, void* workspace, int sms, cudaStream_t st);
+
 // Bounded-wait self test (see nf_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
 

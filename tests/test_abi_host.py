@@ -325,3 +325,40 @@ def test_plan_invalid_arguments():
     assert nf.nf_plan_compute("fused_add_rmsnorm", 4, 4097, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_plan_compute(9, 4, 4096, 152)[0] == nf.NF_ERR_INVALID_ARG
     assert nf.nf_plan_compute(0, 4, 4096, 152, 9)[0] == nf.NF_ERR_INVALID_ARG
+
+
+def test_outer_norm_validation():
+    ws = 1 << 30
+    # hidden must be a positive multiple of 8; any size otherwise
+    for hidden in (0, 4, 12, 4100):
+        assert nf.nf_outer_norm_fwd(A, 0, 0, B, C, D, 4, hidden, 1e-5, A + 0x4000000, ws, None) == \
+            nf.NF_ERR_UNSUPPORTED_HIDDEN
+        assert nf.nf_outer_norm_bwd(A, B, C, D, A, B, C, D, 4, hidden, A, ws, None) == \
+            nf.NF_ERR_UNSUPPORTED_HIDDEN
+        assert nf.nf_outer_norm_workspace_size(4, hidden) == 0
+    assert nf.nf_outer_norm_fwd(A, 0, 0, B, C, D, -1, 64, 1e-5, A, ws, None) == nf.NF_ERR_INVALID_ARG
+    for eps in (0.0, -1.0, float("nan")):
+        assert nf.nf_outer_norm_fwd(A, 0, 0, B, C, D, 4, 64, eps, A, ws, None) == \
+            nf.NF_ERR_INVALID_ARG
+    # zero rows: nothing to do, null pointers allowed
+    assert nf.nf_outer_norm_fwd(None, None, None, None, None, None, 0, 64, 1e-5, None, 0,
+                                None) == nf.NF_OK
+    assert nf.nf_outer_norm_bwd(None, None, None, None, None, None, None, None, 0, 64, None, 0,
+                                None) == nf.NF_OK
+    assert nf.nf_outer_norm_workspace_size(0, 64) == 0
+    # null and misaligned pointers
+    assert nf.nf_outer_norm_fwd(A, 0, 0, None, C, D, 4, 64, 1e-5, B, ws, None) == \
+        nf.NF_ERR_INVALID_ARG
+    assert nf.nf_outer_norm_fwd(A, 0, 0, B, C, D, 4, 64, 1e-5, None, ws, None) == \
+        nf.NF_ERR_INVALID_ARG
+    assert nf.nf_outer_norm_fwd(A + 8, 0, 0, B, C, D, 4, 64, 1e-5, B + 0x100000, ws, None) == \
+        nf.NF_ERR_MISALIGNED
+    assert nf.nf_outer_norm_fwd(A, D + 2, 0, B, C, D + 0x1000, 4, 64, 1e-5, B + 0x100000, ws,
+                                None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_outer_norm_bwd(A, B, None, D, A, B, C, D, 4, 64, A, ws, None) == \
+        nf.NF_ERR_INVALID_ARG
+    assert nf.nf_outer_norm_bwd(A, B + 4, C, D, A + 0x100000, B + 0x100000, C + 0x100000,
+                                D + 0x100000, 4, 64, D + 0x200000, ws, None) == nf.NF_ERR_MISALIGNED
+    # gamma feeds 128-bit loads in the backward
+    assert nf.nf_outer_norm_bwd(A, B, C, D, A + 0x100000, B + 0x100000, C + 0x100000,
+                                D + 0x100002, 4, 64, D + 0x200000, ws, None) == nf.NF_ERR_MISALIGNED

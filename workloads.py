@@ -83,6 +83,17 @@ def rms_bwd_inputs(rows: int, hidden: int, seed: int = 0, device="cpu"):
     return layernorm_bwd_inputs(rows, hidden, seed, device)
 
 
+def outer_inputs(rows: int, hidden: int, seed: int = 0, device="cpu"):
+    """Per-column normalization inputs: x ~ N(0.5, 2), dy ~ N(0, 1),
+    gamma ~ N(1, 0.1), beta ~ N(0, 0.1), bf16."""
+    g = _gen(seed, device)
+    x = _draw(g, (rows, hidden), 0.5, 2.0, device)
+    dy = _draw(g, (rows, hidden), 0.0, 1.0, device)
+    gamma = _draw(g, (hidden,), 1.0, 0.1, device)
+    beta = _draw(g, (hidden,), 0.0, 0.1, device)
+    return x, dy, gamma, beta
+
+
 @dataclass(frozen=True)
 class Workload:
     name: str
