@@ -69,11 +69,13 @@ def _bind(lib):
     lib.or_layernorm_fwd.argtypes = [_D, _D, _D, _I64, _I64, ctypes.c_double, _D, _D, _D]
     lib.or_layernorm_bwd.argtypes = [_D, _D, _D, _D, _D, _I64, _I64, _D, _D, _D]
     lib.or_rmsnorm_bwd.argtypes = [_D, _D, _D, _D, _I64, _I64, _D, _D]
+    lib.or_fused_add_rmsnorm_bwd.argtypes = [_D, _D, _D, _D, _I64, _I64, ctypes.c_double, _D, _D]
     lib.or_outer_norm_fwd.argtypes = [_D, _D, _D, _I64, _I64, ctypes.c_double, _D, _D, _D]
     lib.or_outer_norm_bwd.argtypes = [_D, _D, _D, _D, _D, _I64, _I64, _D, _D, _D]
     for f in (lib.or_bf16_to_double_array, lib.or_double_to_bf16_array, lib.or_rmsnorm_fwd,
               lib.or_fused_add_rmsnorm, lib.or_layernorm_fwd, lib.or_layernorm_bwd,
-              lib.or_rmsnorm_bwd, lib.or_outer_norm_fwd, lib.or_outer_norm_bwd):
+              lib.or_rmsnorm_bwd, lib.or_fused_add_rmsnorm_bwd, lib.or_outer_norm_fwd,
+              lib.or_outer_norm_bwd):
         f.restype = None
     return lib
 
@@ -217,6 +219,26 @@ def rmsnorm_bwd(dy, x, rstd, w):
     dw = np.empty(hidden, dtype=np.float64)
     _load().or_rmsnorm_bwd(_dp(dy), _dp(x), _dp(rstd), _dp(w), rows, hidden, _dp(dx), _dp(dw))
     return dx, dw
+
+
+def fused_add_rmsnorm_bwd(dy, dres, s, w, eps: float):
+    """Backward of the fused residual add + RMSNorm, given the saved residual
+    output s and the gradients dy (normalized output) and dres (residual
+    stream, or None).  Returns (ds, dw) in float64: ds is the gradient of
+    both x and residual."""
+    s = _f64(s)
+    rows, hidden = s.shape
+    dy = _f64(dy, (rows, hidden))
+    w = _f64(w, (hidden,))
+    ds = np.empty_like(s)
+    dw = np.empty(hidden, dtype=np.float64)
+    pr = None
+    if dres is not None:
+        dres = _f64(dres, (rows, hidden))
+        pr = _dp(dres)
+    _load().or_fused_add_rmsnorm_bwd(_dp(dy), pr, _dp(s), _dp(w), rows, hidden, float(eps),
+                                     _dp(ds), _dp(dw))
+    return ds, dw
 
 
 def outer_norm_fwd(x, gamma, beta, eps: float):

@@ -35,6 +35,7 @@
  * autograd in fp64.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -220,6 +221,29 @@ void or_rmsnorm_bwd(const double* dy, const double* x, const double* rstd, const
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t j = 0; j < hidden; ++j)
             dw[j] += dy[r * hidden + j] * x[r * hidden + j] * rstd[r];
+}
+
+/* ---- fused add + RMSNorm backward ------------------------------------------
+ * The forward leaves s = x + residual in the residual buffer and overwrites x
+ * with y = s * rstd(s) * w, so the backward sees s (as saved) and two
+ * incoming gradients: dy for y and dres for the residual stream s.  Both
+ * inputs x and residual receive the same gradient
+ *   ds = rmsnorm_bwd(dy, s, w) + dres,   dw = sum_r dy * s * rstd(s),
+ * with rstd(s) = 1 / sqrt(mean(s^2) + eps) recomputed from s.  dres may be
+ * NULL (no residual-stream gradient). */
+void or_fused_add_rmsnorm_bwd(const double* dy, const double* dres, const double* s,
+                              const double* w, int64_t rows, int64_t hidden, double eps,
+                              double* ds, double* dw) {
+    double* rstd = (double*)malloc((size_t)(rows > 0 ? rows : 1) * sizeof(double));
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) ss += s[r * hidden + j] * s[r * hidden + j];
+        rstd[r] = 1.0 / sqrt(ss / (double)hidden + eps);
+    }
+    or_rmsnorm_bwd(dy, s, rstd, w, rows, hidden, ds, dw);
+    if (dres)
+        for (int64_t i = 0; i < rows * hidden; ++i) ds[i] += dres[i];
+    free(rstd);
 }
 
 /* ---- outer normalization (per column, over the rows) -----------------------

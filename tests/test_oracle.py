@@ -447,3 +447,70 @@ def test_outer_norm_hand_case():
     r = math.sqrt(3 / 8)
     np.testing.assert_allclose(y[:, 0], [1 - 4 * r, 1.0, 1 + 4 * r], rtol=1e-14)
     assert mean[0] == 4.0 and rstd[0] == pytest.approx(r, rel=1e-15)
+
+
+# ---------------------------------------------------------------- fused add + RMSNorm backward pins
+
+def _fused_loss(x, r, w, dy, dres, eps):
+    s, y, _ = oracle.fused_add_rmsnorm(x, r, w, eps)
+    return float(np.sum(dy * y) + np.sum(dres * s))
+
+
+def test_fused_add_rmsnorm_bwd_finite_differences():
+    rng = np.random.default_rng(40)
+    rows, hidden = 3, 6
+    x = rng.standard_normal((rows, hidden))
+    r = rng.standard_normal((rows, hidden)) * 2
+    w = rng.standard_normal(hidden) * 0.3 + 1
+    dy = rng.standard_normal((rows, hidden))
+    dres = rng.standard_normal((rows, hidden))
+    eps = 1e-3
+    ds, dw = oracle.fused_add_rmsnorm_bwd(dy, dres, x + r, w, eps)
+    h = 1e-6
+    for i in range(rows):
+        for j in range(hidden):
+            for which in (0, 1):  # both inputs get the same gradient
+                xp, xm, rp, rm = x.copy(), x.copy(), r.copy(), r.copy()
+                if which == 0:
+                    xp[i, j] += h; xm[i, j] -= h
+                else:
+                    rp[i, j] += h; rm[i, j] -= h
+                fd = (_fused_loss(xp, rp, w, dy, dres, eps) - _fused_loss(xm, rm, w, dy, dres, eps)) / (2 * h)
+                assert ds[i, j] == pytest.approx(fd, rel=1e-6, abs=1e-8)
+    for j in range(hidden):
+        wp, wm = w.copy(), w.copy()
+        wp[j] += h; wm[j] -= h
+        fd = (_fused_loss(x, r, wp, dy, dres, eps) - _fused_loss(x, r, wm, dy, dres, eps)) / (2 * h)
+        assert dw[j] == pytest.approx(fd, rel=1e-6, abs=1e-8)
+
+
+def test_fused_add_rmsnorm_bwd_matches_torch_autograd_fp64():
+    rng = np.random.default_rng(41)
+    rows, hidden, eps = 17, 40, 1e-5
+    x = torch.from_numpy(rng.standard_normal((rows, hidden))).requires_grad_()
+    r = torch.from_numpy(rng.standard_normal((rows, hidden)) * 4).requires_grad_()
+    w = torch.from_numpy(rng.standard_normal(hidden) * 0.1 + 1).requires_grad_()
+    dy = rng.standard_normal((rows, hidden))
+    dres = rng.standard_normal((rows, hidden))
+    s = x + r
+    y = s * torch.rsqrt((s * s).mean(dim=1, keepdim=True) + eps) * w
+    ((torch.from_numpy(dy) * y).sum() + (torch.from_numpy(dres) * s).sum()).backward()
+    ds, dw = oracle.fused_add_rmsnorm_bwd(dy, dres, (x + r).detach().numpy(), w.detach().numpy(), eps)
+    np.testing.assert_allclose(ds, x.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ds, r.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dw, w.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_fused_add_rmsnorm_bwd_without_residual_gradient_is_rmsnorm_bwd():
+    rng = np.random.default_rng(42)
+    s = rng.standard_normal((9, 24))
+    w = rng.standard_normal(24)
+    dy = rng.standard_normal((9, 24))
+    ds, dw = oracle.fused_add_rmsnorm_bwd(dy, None, s, w, 1e-6)
+    # closed form of the RMSNorm gradient: ds = rstd * (g - s_hat * mean(g * s_hat)), g = dy * w
+    rstd = 1 / np.sqrt((s * s).mean(axis=1) + 1e-6)
+    sh = s * rstd[:, None]
+    g = dy * w
+    expect = rstd[:, None] * (g - sh * (g * sh).mean(axis=1)[:, None])
+    np.testing.assert_allclose(ds, expect, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dw, (dy * sh).sum(axis=0), rtol=1e-12, atol=1e-13)

@@ -28,6 +28,10 @@ MUTANTS = {
     "rms_bwd_sign": ("rstd[r] * (g - xhat * mean_gx);", "rstd[r] * (g + xhat * mean_gx);"),
     "rms_bwd_dw_no_rstd": ("dw[j] += dy[r * hidden + j] * x[r * hidden + j] * rstd[r];",
                            "dw[j] += dy[r * hidden + j] * x[r * hidden + j];"),
+    "fused_bwd_dres_dropped": ("for (int64_t i = 0; i < rows * hidden; ++i) ds[i] += dres[i];",
+                               "for (int64_t i = 0; i < rows * hidden; ++i) ds[i] += 0.0 * dres[i];"),
+    "fused_bwd_rstd_no_eps": ("rstd[r] = 1.0 / sqrt(ss / (double)hidden + eps);",
+                              "rstd[r] = 1.0 / sqrt(ss / (double)hidden);"),
     "outer_unbiased_var": ("double var = sq / (double)rows;", "double var = sq / (double)(rows - 1);"),
     "outer_bwd_sign": ("dx[r * hidden + j] = rstd[j] * (g - mean_g - xhat * mean_gx);",
                        "dx[r * hidden + j] = rstd[j] * (g - mean_g + xhat * mean_gx);"),
