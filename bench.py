@@ -81,6 +81,11 @@ def rms_bwd_bytes(rows, hidden):
     return 6 * hidden * rows + 6 * hidden
 
 
+def fused_bwd_bytes(rows, hidden):
+    # read s, dy, dres; write dx; read w once; write dw (fp32) once
+    return 8 * hidden * rows + 6 * hidden
+
+
 def outer_fwd_bytes(rows, hidden):
     # read x once, write y; gamma, beta in; mean, rstd (fp32) out
     return 4 * hidden * rows + 12 * hidden
@@ -316,6 +321,8 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         foot, nbytes = (4 * hidden + 8) * rows, ln_fwd_bytes(rows, hidden)
     elif op == "rmsnorm_bwd":
         foot, nbytes = 6 * hidden * rows, rms_bwd_bytes(rows, hidden)
+    elif op == "fused_add_rmsnorm_bwd":
+        foot, nbytes = 8 * hidden * rows, fused_bwd_bytes(rows, hidden)
     elif op == "outer_norm_fwd":
         foot, nbytes = 4 * hidden * rows, outer_fwd_bytes(rows, hidden)
     elif op == "outer_norm_bwd":
@@ -358,6 +365,17 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         keep = (x, dy, w, dx, ws, dw)
         fn = lambda i, sh: lib.nf_rmsnorm_bwd(pdx + (i % sets) * a2, pdw, pdy + (i % sets) * a2,  # noqa: E731
                                                px + (i % sets) * a2, pw, rows, hidden, eps, pws, nws, sh)
+    elif op == "fused_add_rmsnorm_bwd":
+        sres, w, dy, dres = workloads.fused_bwd_inputs(tot, hidden, device=dev)
+        dx = torch.empty_like(sres)
+        nws = max(nf.nf_rmsnorm_bwd_workspace_size(rows, hidden), 16)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        dw = torch.empty(hidden, device=dev)
+        ps, pw, pdy, pdr, pdx, pws, pdw = (t.data_ptr() for t in (sres, w, dy, dres, dx, ws, dw))
+        keep = (sres, w, dy, dres, dx, ws, dw)
+        fn = lambda i, sh: lib.nf_fused_add_rmsnorm_bwd(  # noqa: E731
+            pdx + (i % sets) * a2, pdw, pdy + (i % sets) * a2, pdr + (i % sets) * a2,
+            ps + (i % sets) * a2, pw, rows, hidden, eps, pws, nws, sh)
     elif op == "outer_norm_fwd":
         # one [rows, hidden] problem per set; per-column statistics are per set
         x, _, g, b = workloads.outer_inputs(tot, hidden, device=dev)
@@ -422,7 +440,8 @@ def ops_suite(nf, peak, stream, l2_bytes):
     def entry(op, rows, h, eps):
         ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        path = "outer" if op.startswith("outer") else nf.nf_plan_query(op, rows, h)["path"]
+        plan_op = "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op
+        path = "outer" if op.startswith("outer") else nf.nf_plan_query(plan_op, rows, h)["path"]
         out[f"{op} {rows}x{h}"] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                                    "us": round(ms * 1e3, 3), "path": path}
 
@@ -440,6 +459,7 @@ def ops_suite(nf, peak, stream, l2_bytes):
         entry("layernorm_bwd", ROWS, h, EPS)
     for h in (4096, 8192):
         entry("rmsnorm_bwd", ROWS, h, EPS)
+        entry("fused_add_rmsnorm_bwd", ROWS, h, EPS)
     for rows, h in ((16384, 1024), (16384, 4096), (65536, 1024), (4096, 8192)):
         entry("outer_norm_fwd", rows, h, EPS)
         entry("outer_norm_bwd", rows, h, EPS)

@@ -195,6 +195,24 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
                          int64_t rows, int64_t hidden, float eps, void* workspace,
                          size_t workspace_bytes, nf_stream stream);
 
+/* Fused residual-add + RMSNorm backward ("optimize inner persistent
+ * scheduler for static fusion" pairs the fused add + RMSNorm forward with
+ * in-place residual semantics; this is its gradient).  The forward left
+ * s = x + residual in `residual` and y = s * rstd(s) * w in x.  Given the
+ * gradient dy of y and, optionally, dres of the residual stream s:
+ *   rstd   = rsqrt(mean_j(s_j^2) + eps)     (recomputed from the saved s)
+ *   dx     = bf16( rstd * (g - s * rstd^2 * mean_j(g * s)) + dres ),  g = dy * w
+ *   dw[j]  = sum_r dy[r][j] * s[r][j] * rstd[r]                      (fp32)
+ * dx is the gradient of both forward inputs (x and residual).  dres may be
+ * NULL (no residual-stream gradient); dx may be exactly dy, dres or
+ * residual (in place).  Same hidden sizes, workspace (see
+ * nf_rmsnorm_bwd_workspace_size), alignment and error rules as
+ * nf_rmsnorm_bwd; dres, if given, must be 16-byte aligned. */
+nf_status nf_fused_add_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* dres,
+                                   const void* residual, const void* weight, int64_t rows,
+                                   int64_t hidden, float eps, void* workspace,
+                                   size_t workspace_bytes, nf_stream stream);
+
 /* Size of the fixed scratch area nf_layernorm_bwd_noalloc uses. */
 #define NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -53,6 +53,7 @@ EXPORTS = (
     "nf_layernorm_bwd_workspace_size", "nf_layernorm_bwd",
     "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd", "nf_layernorm_bwd_noalloc",
     "nf_outer_norm_workspace_size", "nf_outer_norm_fwd", "nf_outer_norm_bwd",
+    "nf_fused_add_rmsnorm_bwd",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
     "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
 )
@@ -96,6 +97,7 @@ def _bind(lib):
         "nf_rmsnorm_bwd": (_S, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_layernorm_bwd_noalloc": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
         "nf_outer_norm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+        "nf_fused_add_rmsnorm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_outer_norm_fwd": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_outer_norm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
         "nf_set_path": (_S, [_S]),
@@ -175,6 +177,12 @@ def nf_layernorm_bwd_noalloc(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, 
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20  # NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES
+
+
+def nf_fused_add_rmsnorm_bwd(dx, dw, dy, dres, residual, weight, rows, hidden, eps, workspace,
+                             workspace_bytes, stream) -> int:
+    return lib().nf_fused_add_rmsnorm_bwd(dx, dw, dy, dres, residual, weight, rows, hidden, eps,
+                                          workspace, workspace_bytes, stream)
 
 
 def nf_outer_norm_workspace_size(rows, hidden) -> int:
@@ -336,6 +344,30 @@ def rmsnorm_bwd(dy, x, weight, eps: float = 1e-6, workspace=None, out=None, stre
                           weight.data_ptr(), rows, hidden, eps, workspace.data_ptr(),
                           workspace.numel() * workspace.element_size(), _stream(stream)),
            "nf_rmsnorm_bwd")
+    return dx, dw
+
+
+def fused_add_rmsnorm_bwd(dy, residual, weight, dres=None, eps: float = 1e-6, workspace=None,
+                         out=None, stream=None):
+    """Backward of fused_add_rmsnorm given the saved residual output.
+    Returns (dx bf16 -- the gradient of both x and residual --, dw fp32)."""
+    import torch
+    for t, n in ((dy, "dy"), (residual, "residual"), (weight, "weight")):
+        _need(t, torch.bfloat16, n)
+    if dres is not None:
+        _need(dres, torch.bfloat16, "dres")
+    rows, hidden = _rows_hidden(residual)
+    dx = torch.empty_like(residual) if out is None else out
+    dw = torch.empty(hidden, dtype=torch.float32, device=residual.device)
+    need = nf_rmsnorm_bwd_workspace_size(rows, hidden)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=residual.device)
+    _check(nf_fused_add_rmsnorm_bwd(dx.data_ptr(), dw.data_ptr(), dy.data_ptr(),
+                                    None if dres is None else dres.data_ptr(),
+                                    residual.data_ptr(), weight.data_ptr(), rows, hidden, eps,
+                                    workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "nf_fused_add_rmsnorm_bwd")
     return dx, dw
 
 

@@ -516,9 +516,12 @@ size_t nf_rmsnorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
     return bwd_workspace_bytes(NF_OP_RMSNORM_BWD, rows, hidden);
 }
 
-nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, const void* weight,
-                         int64_t rows, int64_t hidden, float eps, void* workspace,
-                         size_t workspace_bytes, nf_stream stream) {
+namespace {
+// RMSNorm backward, optionally with a residual-stream gradient `dres` added
+// to dx (the fused residual-add + RMSNorm backward).
+nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void* dres,
+                  const void* weight, int64_t rows, int64_t hidden, float eps, void* workspace,
+                  size_t workspace_bytes, nf_stream stream) {
     if (nf_status st = common_checks(NF_OP_RMSNORM_BWD, rows, hidden, eps, true)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (rows == 0) {
@@ -529,7 +532,7 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
     }
     if (!dx || !dw || !dy || !x || !weight || !workspace) return NF_ERR_INVALID_ARG;
     if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
-        !aligned(workspace, 16) || !aligned(dw, 16))
+        !aligned(workspace, 16) || !aligned(dw, 16) || !aligned(dres, 16))
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_RMSNORM_BWD, rows, hidden, &pl)) return st;
@@ -537,12 +540,12 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
     if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
     const int64_t act = rows * hidden * 2, par = hidden * 2, grad = hidden * 4;
     const Span sdx{dx, act}, sdw{dw, grad}, sws{workspace, static_cast<int64_t>(need)};
-    const Span ins[] = {{dy, act}, {x, act}, {weight, par}};
+    const Span ins[] = {{dy, act}, {x, act}, {dres, dres ? act : 0}, {weight, par}};
     if (overlap(sdx, sdw) || overlap(sws, sdx) || overlap(sws, sdw)) return NF_ERR_INVALID_ARG;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const Span& in = ins[i];
-        // dx may be exactly dy or x (each row is read before it is written)
-        const bool dx_clash = i < 2 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
+        // dx may be exactly dy, x or dres (each row is read before it is written)
+        const bool dx_clash = i < 3 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
         if (dx_clash || overlap(sdw, in) || overlap(sws, in)) return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
@@ -552,6 +555,7 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
         a.in0 = static_cast<const uint16_t*>(x);
         a.in1 = static_cast<const uint16_t*>(dy);
         a.p0 = static_cast<const uint16_t*>(weight);
+        a.add = static_cast<const uint16_t*>(dres);
         a.ws = ws;
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
@@ -562,14 +566,30 @@ nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, con
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
         if (nf_status st = device_status_addr(&status)) return st;
-        if (cudaError_t e = launch_rms_bwd_bulk(hidden, dx, ws, dy, x, weight, rows, eps, pl.grid,
-                                                status, s))
+        if (cudaError_t e = launch_rms_bwd_bulk(hidden, dx, ws, dy, x, dres, weight, rows, eps,
+                                                pl.grid, status, s))
             return from_cuda(e);
-    } else if (cudaError_t e = launch_rms_bwd_reg(hidden, dx, ws, dy, x, weight, rows, eps,
+    } else if (cudaError_t e = launch_rms_bwd_reg(hidden, dx, ws, dy, x, dres, weight, rows, eps,
                                                   pl.grid, s)) {
         return from_cuda(e);
     }
     return from_cuda(launch_column_reduce1(ws, dw, pl.partials, hidden, s));
+}
+}  // namespace
+
+nf_status nf_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* x, const void* weight,
+                         int64_t rows, int64_t hidden, float eps, void* workspace,
+                         size_t workspace_bytes, nf_stream stream) {
+    return rms_bwd(dx, dw, dy, x, nullptr, weight, rows, hidden, eps, workspace, workspace_bytes,
+                   stream);
+}
+
+nf_status nf_fused_add_rmsnorm_bwd(void* dx, float* dw, const void* dy, const void* dres,
+                                   const void* residual, const void* weight, int64_t rows,
+                                   int64_t hidden, float eps, void* workspace,
+                                   size_t workspace_bytes, nf_stream stream) {
+    return rms_bwd(dx, dw, dy, residual, dres, weight, rows, hidden, eps, workspace,
+                   workspace_bytes, stream);
 }
 
 size_t nf_outer_norm_workspace_size(int64_t rows, int64_t hidden) {

@@ -34,11 +34,14 @@
 // on giving up, waits (bounded) for the copies it already issued and
 // leaves.  Either records NF_ERR_TIMEOUT in the device status word.
 #include "common.cuh"
+#include "pairs.cuh"
 #include "launch.h"
 
 namespace nf {
 
-enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3, kRmsBwd = 4 };
+// kFusedBwd: the RMSNorm backward of the fused residual add, which also
+// stages the residual-stream gradient and adds it to dx.
+enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3, kRmsBwd = 4, kFusedBwd = 5 };
 
 // Row-group shape: GW warps per row and NG concurrent row groups per CTA.
 // Every shape makes the consumer warps a whole number of warp groups (the
@@ -58,7 +61,7 @@ template <> struct BulkRow<12288> { static constexpr int GW = 12, NGF = 1,  GWB 
 
 template <int OP, int H>
 struct BulkShape {
-    static constexpr bool BWD = OP == 3 || OP == 4;
+    static constexpr bool BWD = OP == 3 || OP == 4 || OP == 5;
     static constexpr int GW = BWD ? BulkRow<H>::GWB : BulkRow<H>::GW;
     static constexpr int NG = BWD ? BulkRow<H>::NGB : BulkRow<H>::NGF;
 };
@@ -69,7 +72,8 @@ constexpr int kProducerRegs = 40;
 constexpr int kConsumersBarrier = 15;  // named barrier of all consumer threads (groups use 1..NG)
 
 template <int OP> struct OpIO {
-    static constexpr int NIN = (OP == kFused || OP == kLnBwd || OP == kRmsBwd) ? 2 : 1;  // staged tensors per row
+    static constexpr int NIN = OP == kFusedBwd ? 3
+                               : (OP == kFused || OP == kLnBwd || OP == kRmsBwd) ? 2 : 1;  // staged tensors per row
 };
 
 template <int OP, int H>
@@ -152,6 +156,7 @@ struct BulkArgs {
     const uint16_t* in1;     // fused: residual; ln/rms bwd: dy
     const uint16_t* p0;      // weight / gamma
     const uint16_t* p1;      // beta
+    const uint16_t* add;     // rms bwd: gradient added to dx (fused-add backward), or null
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
     float* ws;               // bwd column partials [grid][planes][H], one slot per CTA
@@ -211,8 +216,10 @@ norm_bulk_kernel(BulkArgs a) {
                     const int64_t row = r0 + i;
                     uint8_t* st = smem + s * G::STAGE_BYTES;
                     bulk_g2s(smem_addr(st), a.in0 + row * H, G::ROW_BYTES, &full[s]);
-                    if constexpr (OpIO<OP>::NIN == 2)
+                    if constexpr (OpIO<OP>::NIN >= 2)
                         bulk_g2s(smem_addr(st + G::ROW_BYTES), a.in1 + row * H, G::ROW_BYTES, &full[s]);
+                    if constexpr (OpIO<OP>::NIN == 3)
+                        bulk_g2s(smem_addr(st + 2 * G::ROW_BYTES), a.add + row * H, G::ROW_BYTES, &full[s]);
                     issued[k] = q + 1;
                 }
             }
@@ -245,28 +252,30 @@ norm_bulk_kernel(BulkArgs a) {
     for (int k = 0; k < G::VPT; ++k) {
         prm0[k] = ld_param(a.p0 + (k * G::GT + gt) * kVec);
     }
-    constexpr bool kBwd = OP == kLnBwd || OP == kRmsBwd;
+    constexpr bool kRmsB = OP == kRmsBwd || OP == kFusedBwd;
+    constexpr bool kBwd = OP == kLnBwd || kRmsB;
     // Backward consumers with a large register share keep gamma / w widened
     // to fp32 for the whole stripe, so no row re-widens it; with a smaller
-    // share (the 512-thread hidden-12288 shape) it stays packed.
+    // share (the 512-thread hidden-12288 shape) it stays packed.  All the
+    // elementwise arithmetic runs on fp32 pairs (add / mul / fma .f32x2).
     constexpr bool kCacheW = kBwd && G::CONS_REGS >= 200;
-    float wf[kCacheW ? G::VPT : 1][8];
+    float2 wf[kCacheW ? G::VPT : 1][4];
     if constexpr (kCacheW) {
 #pragma unroll
-        for (int k = 0; k < G::VPT; ++k) unpack8(prm0[k], wf[k]);
+        for (int k = 0; k < G::VPT; ++k) unpack8x2(prm0[k], wf[k]);
     }
-    float acc_g[kBwd ? G::VPT : 1][8], acc_b[OP == kLnBwd ? G::VPT : 1][8];
+    float2 acc_g[kBwd ? G::VPT : 1][4], acc_b[OP == kLnBwd ? G::VPT : 1][4];
     if constexpr (kBwd) {
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc_g[k][e] = 0.f;
+            for (int q = 0; q < 4; ++q) acc_g[k][q] = make_float2(0.f, 0.f);
     }
     if constexpr (OP == kLnBwd) {
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc_b[k][e] = 0.f;
+            for (int q = 0; q < 4; ++q) acc_b[k][q] = make_float2(0.f, 0.f);
     }
     // saved statistics of the group's next row, fetched one row ahead
     float nmu = 0.f, nrs = 0.f;
@@ -283,11 +292,12 @@ norm_bulk_kernel(BulkArgs a) {
         const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&full[s], par, kWaitLimitNs));
         const float fail = ok ? 0.f : 1.f;
         const uint8_t* st = smem + s * G::STAGE_BYTES;
-        uint4 v0[G::VPT], v1[G::VPT];
+        uint4 v0[G::VPT], v1[G::VPT], v2[OpIO<OP>::NIN == 3 ? G::VPT : 1];
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) {
             v0[k] = lds128(st + (k * G::GT + gt) * 16);
-            if constexpr (OpIO<OP>::NIN == 2) v1[k] = lds128(st + G::ROW_BYTES + (k * G::GT + gt) * 16);
+            if constexpr (OpIO<OP>::NIN >= 2) v1[k] = lds128(st + G::ROW_BYTES + (k * G::GT + gt) * 16);
+            if constexpr (OpIO<OP>::NIN == 3) v2[k] = lds128(st + 2 * G::ROW_BYTES + (k * G::GT + gt) * 16);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled now
@@ -295,116 +305,130 @@ norm_bulk_kernel(BulkArgs a) {
         float* rb1 = red + ((j & 1) * 2 + 1) * G::GW * 3;
 
         if constexpr (OP == kFused || OP == kRms) {
-            float f[G::VPT][8];
-            float v[2] = {0.f, fail};
+            float2 f[G::VPT][4];
+            float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(v0[k], f[k]);
+                unpack8x2(v0[k], f[k]);
                 if constexpr (OP == kFused) {
-                    float b[8];
-                    unpack8(v1[k], b);
+                    float2 b[4];
+                    unpack8x2(v1[k], b);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[k][e] += b[e];
+                    for (int q = 0; q < 4; ++q) f[k][q] = __fadd2_rn(f[k][q], b[q]);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[0] += f[k][e] * f[k][e];
+                for (int q = 0; q < 4; ++q) ss = __ffma2_rn(f[k][q], f[k][q], ss);
             }
+            float v[2] = {ss.x + ss.y, fail};
             group_reduce<G::GW, 2>(v, rb0, gwarp, lane, gid);
             if (v[1] != 0.f) { failed = true; break; }
             if constexpr (OP == kFused) {
 #pragma unroll
                 for (int k = 0; k < G::VPT; ++k)
-                    st_stream(a.out1 + row * H + (k * G::GT + gt) * kVec, pack8(f[k]));
+                    st_stream(a.out1 + row * H + (k * G::GT + gt) * kVec, pack8x2(f[k]));
             }
             const float rstd = rsqrtf(v[0] * (1.0f / H) + a.eps);
+            const float2 rstd2 = make_float2(rstd, rstd);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float w[8], o[8];
-                unpack8(prm0[k], w);
+                float2 w[4], o[4];
+                unpack8x2(prm0[k], w);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = f[k][e] * rstd * w[e];
-                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
+                for (int q = 0; q < 4; ++q) o[q] = __fmul2_rn(__fmul2_rn(f[k][q], rstd2), w[q]);
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8x2(o));
             }
         } else if constexpr (OP == kLnFwd) {
-            float f[G::VPT][8];
-            float v[2] = {0.f, fail};
+            float2 f[G::VPT][4];
+            float2 s1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                unpack8(v0[k], f[k]);
+                unpack8x2(v0[k], f[k]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[0] += f[k][e];
+                for (int q = 0; q < 4; ++q) s1 = __fadd2_rn(s1, f[k][q]);
             }
+            float v[2] = {s1.x + s1.y, fail};
             group_reduce<G::GW, 2>(v, rb0, gwarp, lane, gid);
             if (v[1] != 0.f) { failed = true; break; }
             const float mean = v[0] * (1.0f / H);
-            float sq[1] = {0.f};
+            const float2 nmean2 = make_float2(-mean, -mean);
+            float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    f[k][e] -= mean;  // the row, centered in place
-                    sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
+                for (int q = 0; q < 4; ++q) {
+                    f[k][q] = __fadd2_rn(f[k][q], nmean2);  // the row, centered in place
+                    s2 = __ffma2_rn(f[k][q], f[k][q], s2);
                 }
+            float sq[1] = {s2.x + s2.y};
             group_reduce<G::GW, 1>(sq, rb1, gwarp, lane, gid);
             const float rstd = rsqrtf(sq[0] * (1.0f / H) + a.eps);
+            const float2 rstd2 = make_float2(rstd, rstd);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float g[8], b[8], o[8];
-                unpack8(prm0[k], g);
-                unpack8(ld_param(a.p1 + (k * G::GT + gt) * kVec), b);
+                float2 g[4], b[4], o[4];
+                unpack8x2(prm0[k], g);
+                unpack8x2(ld_param(a.p1 + (k * G::GT + gt) * kVec), b);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(f[k][e], rstd * g[e], b[e]);
-                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
+                for (int q = 0; q < 4; ++q) o[q] = __ffma2_rn(f[k][q], __fmul2_rn(rstd2, g[q]), b[q]);
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8x2(o));
             }
             if (gt == 0) {
                 if (a.mean) a.mean[row] = mean;
                 if (a.rstd) a.rstd[row] = rstd;
             }
-        } else if constexpr (OP == kRmsBwd) {
+        } else if constexpr (kRmsB) {
             // rstd recomputed from the row: rs = rsqrt(sum x^2 / H + eps),
             // dx = rs * g - x * (rs^3 * sum(g x) / H) with g = dy * w
             // the row is widened once when the register share allows,
             // otherwise vector by vector on each pass
-            float xf[kCacheW ? G::VPT : 1][8], df[kCacheW ? G::VPT : 1][8];
-            float v[3] = {0.f, 0.f, fail};
+            float2 xf[kCacheW ? G::VPT : 1][4], df[kCacheW ? G::VPT : 1][4];
+            float2 sxx = make_float2(0.f, 0.f), sgx = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xk[8], dk[8], wk[8];
-                unpack8(v0[k], xk);
-                unpack8(v1[k], dk);
+                float2 xk[4], dk[4], wk[4];
+                unpack8x2(v0[k], xk);
+                unpack8x2(v1[k], dk);
                 if constexpr (kCacheW) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) { xf[k][e] = xk[e]; df[k][e] = dk[e]; wk[e] = wf[k][e]; }
+                    for (int q = 0; q < 4; ++q) { xf[k][q] = xk[q]; df[k][q] = dk[q]; wk[q] = wf[k][q]; }
                 } else {
-                    unpack8(prm0[k], wk);
+                    unpack8x2(prm0[k], wk);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    v[0] = fmaf(xk[e], xk[e], v[0]);
-                    v[1] = fmaf(dk[e] * wk[e], xk[e], v[1]);
+                for (int q = 0; q < 4; ++q) {
+                    sxx = __ffma2_rn(xk[q], xk[q], sxx);
+                    sgx = __ffma2_rn(__fmul2_rn(dk[q], wk[q]), xk[q], sgx);
                 }
             }
+            float v[3] = {sxx.x + sxx.y, sgx.x + sgx.y, fail};
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
             if (v[2] != 0.f) { failed = true; break; }
             const float rs = rsqrtf(v[0] * (1.0f / H) + a.eps);
             const float c = rs * rs * rs * v[1] * (1.0f / H);
+            const float2 rs2 = make_float2(rs, rs), nc2 = make_float2(-c, -c);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xk[8], dk[8], wk[8], o[8];
+                float2 xk[4], dk[4], wk[4], o[4];
                 if constexpr (kCacheW) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) { xk[e] = xf[k][e]; dk[e] = df[k][e]; wk[e] = wf[k][e]; }
+                    for (int q = 0; q < 4; ++q) { xk[q] = xf[k][q]; dk[q] = df[k][q]; wk[q] = wf[k][q]; }
                 } else {
-                    unpack8(v0[k], xk);
-                    unpack8(v1[k], dk);
-                    unpack8(prm0[k], wk);
+                    unpack8x2(v0[k], xk);
+                    unpack8x2(v1[k], dk);
+                    unpack8x2(prm0[k], wk);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    o[e] = fmaf(-xk[e], c, rs * (dk[e] * wk[e]));
-                    acc_g[k][e] = fmaf(dk[e] * xk[e], rs, acc_g[k][e]);
+                for (int q = 0; q < 4; ++q) {
+                    o[q] = __ffma2_rn(xk[q], nc2, __fmul2_rn(rs2, __fmul2_rn(dk[q], wk[q])));
+                    acc_g[k][q] = __ffma2_rn(__fmul2_rn(dk[q], xk[q]), rs2, acc_g[k][q]);
                 }
-                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
+                if constexpr (OP == kFusedBwd) {  // + the residual-stream gradient
+                    float2 af[4];
+                    unpack8x2(v2[k], af);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) o[q] = __fadd2_rn(o[q], af[q]);
+                }
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8x2(o));
             }
         } else {  // kLnBwd
             // xhat = x * rstd - mean * rstd (one fma), g = dy * gamma;
@@ -412,49 +436,52 @@ norm_bulk_kernel(BulkArgs a) {
             const float mu = nmu, rs = nrs;
             if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
             const float nmr = -mu * rs;
-            float xf[kCacheW ? G::VPT : 1][8], df[kCacheW ? G::VPT : 1][8];
-            float v[3] = {0.f, 0.f, fail};
+            const float2 rs2 = make_float2(rs, rs), nmr2 = make_float2(nmr, nmr);
+            float2 xf[kCacheW ? G::VPT : 1][4], df[kCacheW ? G::VPT : 1][4];
+            float2 sg = make_float2(0.f, 0.f), sgx = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xk[8], dk[8], wk[8];
-                unpack8(v0[k], xk);
-                unpack8(v1[k], dk);
+                float2 xk[4], dk[4], wk[4];
+                unpack8x2(v0[k], xk);
+                unpack8x2(v1[k], dk);
                 if constexpr (kCacheW) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) { xf[k][e] = xk[e]; df[k][e] = dk[e]; wk[e] = wf[k][e]; }
+                    for (int q = 0; q < 4; ++q) { xf[k][q] = xk[q]; df[k][q] = dk[q]; wk[q] = wf[k][q]; }
                 } else {
-                    unpack8(prm0[k], wk);
+                    unpack8x2(prm0[k], wk);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xh = fmaf(xk[e], rs, nmr);
-                    const float g = dk[e] * wk[e];
-                    v[0] += g;
-                    v[1] = fmaf(g, xh, v[1]);
-                    acc_g[k][e] = fmaf(dk[e], xh, acc_g[k][e]);
-                    acc_b[k][e] += dk[e];
+                for (int q = 0; q < 4; ++q) {
+                    const float2 xh = __ffma2_rn(xk[q], rs2, nmr2);
+                    const float2 g = __fmul2_rn(dk[q], wk[q]);
+                    sg = __fadd2_rn(sg, g);
+                    sgx = __ffma2_rn(g, xh, sgx);
+                    acc_g[k][q] = __ffma2_rn(dk[q], xh, acc_g[k][q]);
+                    acc_b[k][q] = __fadd2_rn(acc_b[k][q], dk[q]);
                 }
             }
+            float v[3] = {sg.x + sg.y, sgx.x + sgx.y, fail};
             group_reduce<G::GW, 3>(v, rb0, gwarp, lane, gid);
             if (v[2] != 0.f) { failed = true; break; }
             const float rsA = rs * v[0] * (1.0f / H), rsB = rs * v[1] * (1.0f / H);
+            const float2 nrsA2 = make_float2(-rsA, -rsA), nrsB2 = make_float2(-rsB, -rsB);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float xk[8], dk[8], wk[8], o[8];
+                float2 xk[4], dk[4], wk[4], o[4];
                 if constexpr (kCacheW) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) { xk[e] = xf[k][e]; dk[e] = df[k][e]; wk[e] = wf[k][e]; }
+                    for (int q = 0; q < 4; ++q) { xk[q] = xf[k][q]; dk[q] = df[k][q]; wk[q] = wf[k][q]; }
                 } else {
-                    unpack8(v0[k], xk);
-                    unpack8(v1[k], dk);
-                    unpack8(prm0[k], wk);
+                    unpack8x2(v0[k], xk);
+                    unpack8x2(v1[k], dk);
+                    unpack8x2(prm0[k], wk);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xh = fmaf(xk[e], rs, nmr);
-                    o[e] = fmaf(-xh, rsB, fmaf(rs, dk[e] * wk[e], -rsA));
+                for (int q = 0; q < 4; ++q) {
+                    const float2 xh = __ffma2_rn(xk[q], rs2, nmr2);
+                    o[q] = __ffma2_rn(xh, nrsB2, __ffma2_rn(rs2, __fmul2_rn(dk[q], wk[q]), nrsA2));
                 }
-                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8(o));
+                st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8x2(o));
             }
         }
     }
@@ -475,11 +502,11 @@ norm_bulk_kernel(BulkArgs a) {
 #pragma unroll
         for (int k = 0; k < G::VPT; ++k) {
             const int jj = (k * G::GT + gt) * kVec;
-            reinterpret_cast<float4*>(mine + jj)[0] = make_float4(acc_g[k][0], acc_g[k][1], acc_g[k][2], acc_g[k][3]);
-            reinterpret_cast<float4*>(mine + jj)[1] = make_float4(acc_g[k][4], acc_g[k][5], acc_g[k][6], acc_g[k][7]);
+            reinterpret_cast<float4*>(mine + jj)[0] = make_float4(acc_g[k][0].x, acc_g[k][0].y, acc_g[k][1].x, acc_g[k][1].y);
+            reinterpret_cast<float4*>(mine + jj)[1] = make_float4(acc_g[k][2].x, acc_g[k][2].y, acc_g[k][3].x, acc_g[k][3].y);
             if constexpr (NP == 2) {
-                reinterpret_cast<float4*>(mine + H + jj)[0] = make_float4(acc_b[k][0], acc_b[k][1], acc_b[k][2], acc_b[k][3]);
-                reinterpret_cast<float4*>(mine + H + jj)[1] = make_float4(acc_b[k][4], acc_b[k][5], acc_b[k][6], acc_b[k][7]);
+                reinterpret_cast<float4*>(mine + H + jj)[0] = make_float4(acc_b[k][0].x, acc_b[k][0].y, acc_b[k][1].x, acc_b[k][1].y);
+                reinterpret_cast<float4*>(mine + H + jj)[1] = make_float4(acc_b[k][2].x, acc_b[k][2].y, acc_b[k][3].x, acc_b[k][3].y);
             }
         }
         named_sync(kConsumersBarrier, G::NCT);
@@ -629,18 +656,20 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* 
 }
 
 cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
-                                const void* w, int64_t rows, float eps, int grid, int* status,
-                                cudaStream_t st) {
+                                const void* dres, const void* w, int64_t rows, float eps, int grid,
+                                int* status, cudaStream_t st) {
     BulkArgs a{};
     a.out0 = static_cast<uint16_t*>(dx);
     a.in0 = static_cast<const uint16_t*>(x);
     a.in1 = static_cast<const uint16_t*>(dy);
+    a.add = static_cast<const uint16_t*>(dres);
     a.p0 = static_cast<const uint16_t*>(w);
     a.ws = ws;
     a.status = status;
     a.rows = rows;
     a.eps = eps;
-    return launch_bulk_op<kRmsBwd>(hidden, a, grid, st);
+    return dres ? launch_bulk_op<kFusedBwd>(hidden, a, grid, st)
+                : launch_bulk_op<kRmsBwd>(hidden, a, grid, st);
 }
 
 }  // namespace nf

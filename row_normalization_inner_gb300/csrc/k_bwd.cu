@@ -129,7 +129,7 @@ layernorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, cons
 template <int H>
 __global__ void __launch_bounds__(BGeo<H>::TPR * BGeo<H>::RPC)
 rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const uint16_t* x,
-                const uint16_t* __restrict__ w, int64_t rows, float eps) {
+                const uint16_t* dres, const uint16_t* __restrict__ w, int64_t rows, float eps) {
     using G = BGeo<H>;
     __shared__ float red[2][G::RPC * G::W * 2];
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
@@ -187,6 +187,12 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
                 for (int e = 0; e < 8; ++e) {
                     o[e] = rs * df[e] * wf[e] - xf[e] * c;
                     acc[k][e] += df[e] * xf[e] * rs;
+                }
+                if (dres) {  // fused-add backward: + the residual-stream gradient
+                    float af[8];
+                    unpack8(ld_stream(dres + r * H + (k * G::TPR + t) * kVec), af);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] += af[e];
                 }
                 st_stream(dx + r * H + (k * G::TPR + t) * kVec, pack8(o));
             }
@@ -288,11 +294,13 @@ cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64
 }
 
 cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
-                               const void* w, int64_t rows, float eps, int grid, cudaStream_t st) {
+                               const void* dres, const void* w, int64_t rows, float eps, int grid,
+                               cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
         rmsnorm_bwd_reg<H><<<grid, BGeo<H>::TPR * BGeo<H>::RPC, 0, st>>>(
             static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
-            static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), rows, eps);
+            static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dres),
+            static_cast<const uint16_t*>(w), rows, eps);
         return cudaGetLastError();
     })
 }

@@ -251,6 +251,12 @@ __global__ void __launch_bounds__(kLongBwdMaxT) norm_long_bwd(DynArgs a, int sli
                         acc0[k][e] += df[e] * xf[e] * rs;
                     }
                 }
+                if (OP == 4 && a.add) {  // fused-add backward: + the residual-stream gradient
+                    float af[8];
+                    unpack8(ld_stream(a.add + r * H + v * kVec), af);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] += af[e];
+                }
                 st_stream(a.out0 + r * H + v * kVec, pack8(o));
             }
         }

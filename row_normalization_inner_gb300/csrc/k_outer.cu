@@ -32,6 +32,7 @@
 // and starts with griddepcontrol.wait, so launch latency overlaps the tail
 // of the previous kernel while every read still follows its producer.
 #include "common.cuh"
+#include "pairs.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -123,16 +124,6 @@ __device__ __forceinline__ int thread_rows(int64_t len, int ty) {
 }
 
 // ---- packed fp32 pairs ------------------------------------------------------
-__device__ __forceinline__ void unpack8x2(uint4 v, float2 (&f)[4]) {
-    f[0] = make_float2(bf_lo(v.x), bf_hi(v.x));
-    f[1] = make_float2(bf_lo(v.y), bf_hi(v.y));
-    f[2] = make_float2(bf_lo(v.z), bf_hi(v.z));
-    f[3] = make_float2(bf_lo(v.w), bf_hi(v.w));
-}
-__device__ __forceinline__ uint4 pack8x2(const float2 (&o)[4]) {
-    return make_uint4(pack2(o[0].x, o[0].y), pack2(o[1].x, o[1].y), pack2(o[2].x, o[2].y),
-                      pack2(o[3].x, o[3].y));
-}
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
 __device__ __forceinline__ void load8x2(const float* p, float2 (&f)[4]) {  // p 4-byte aligned
 #pragma unroll

@@ -52,7 +52,8 @@ cudaError_t launch_column_reduce1(const float* ws, float* out, int nslots, int64
                                   cudaStream_t st);
 // RMSNorm backward, stage 1 (register path): RPC slots per CTA, ws[slot][hidden].
 cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
-                               const void* w, int64_t rows, float eps, int grid, cudaStream_t st);
+                               const void* dres, const void* w, int64_t rows, float eps, int grid,
+                               cudaStream_t st);
 
 // Bulk-copy staged path: `grid` persistent CTAs (one per SM), each over a
 // contiguous row stripe; `status` is the device status word.
@@ -71,8 +72,8 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* 
 
 // RMSNorm backward, stage 1 on the bulk path (one slot of ws[slot][hidden] per CTA).
 cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
-                                const void* w, int64_t rows, float eps, int grid, int* status,
-                                cudaStream_t st);
+                                const void* dres, const void* w, int64_t rows, float eps, int grid,
+                                int* status, cudaStream_t st);
 
 // Runtime-hidden path (any hidden that is a multiple of 8 up to
 // dyn_max_hidden(op)).  op: 0 fused, 1 rms fwd, 2 ln fwd, 3 ln bwd, 4 rms bwd.
@@ -83,6 +84,7 @@ struct DynArgs {
     const uint16_t* in1;     // fused: residual; bwd: dy
     const uint16_t* p0;      // weight / gamma
     const uint16_t* p1;      // beta
+    const uint16_t* add;     // rms bwd: gradient added to dx (fused-add backward), or null
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
     float* ws;               // bwd partials [grid][planes][hidden]

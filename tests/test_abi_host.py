@@ -362,3 +362,17 @@ def test_outer_norm_validation():
     # gamma feeds 128-bit loads in the backward
     assert nf.nf_outer_norm_bwd(A, B, C, D, A + 0x100000, B + 0x100000, C + 0x100000,
                                 D + 0x100002, 4, 64, D + 0x200000, ws, None) == nf.NF_ERR_MISALIGNED
+
+
+def test_fused_add_rmsnorm_bwd_validation():
+    ws = 1 << 30
+    f = nf.nf_fused_add_rmsnorm_bwd
+    assert f(A, B, C, None, D, A, 4, 4004, 1e-6, B, ws, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
+    assert f(A, B, C, None, D, A, -1, 4096, 1e-6, B, ws, None) == nf.NF_ERR_INVALID_ARG
+    assert f(A, B, C, None, D, A, 4, 4096, 0.0, B, ws, None) == nf.NF_ERR_INVALID_ARG
+    assert f(None, None, None, None, None, None, 0, 4096, 1e-6, None, 0, None) == nf.NF_OK
+    assert f(A, None, C, None, D, A, 4, 4096, 1e-6, B, ws, None) == nf.NF_ERR_INVALID_ARG
+    assert f(A, B, C, D, None, A, 4, 4096, 1e-6, B, ws, None) == nf.NF_ERR_INVALID_ARG
+    # dres is optional but, when given, 16-byte aligned like the activations
+    assert f(A, B + 0x1000000, C, D + 8, D + 0x1000000, A + 0x2000000, 4, 4096, 1e-6,
+             B + 0x2000000, ws, None) == nf.NF_ERR_MISALIGNED

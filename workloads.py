@@ -83,6 +83,18 @@ def rms_bwd_inputs(rows: int, hidden: int, seed: int = 0, device="cpu"):
     return layernorm_bwd_inputs(rows, hidden, seed, device)
 
 
+def fused_bwd_inputs(rows: int, hidden: int, seed: int = 0, device="cpu"):
+    """Fused add + RMSNorm backward: the saved residual stream s ~ N(0, 4.12)
+    (the spread of x + 4 N(0,1)), dy ~ N(0,1), dres ~ N(0,1), weight ~ N(1, 0.1),
+    all bf16.  Returns (s, weight, dy, dres)."""
+    g = _gen(seed, device)
+    s = _draw(g, (rows, hidden), 0.0, 4.12, device)
+    dy = _draw(g, (rows, hidden), 0.0, 1.0, device)
+    dres = _draw(g, (rows, hidden), 0.0, 1.0, device)
+    w = _draw(g, (hidden,), 1.0, 0.1, device)
+    return s, w, dy, dres
+
+
 def outer_inputs(rows: int, hidden: int, seed: int = 0, device="cpu"):
     """Per-column normalization inputs: x ~ N(0.5, 2), dy ~ N(0, 1),
     gamma ~ N(1, 0.1), beta ~ N(0, 0.1), bf16."""
