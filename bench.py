@@ -332,19 +332,26 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
     sets = max(1, min(16384, -(-2 * l2_bytes // foot)))
     tot = sets * rows
     a2 = rows * hidden * 2  # bytes per set of one bf16 activation
+    # forward calls take a workspace only on the split family (rows longer
+    # than a cluster holds); sized for every family by the library
+    fwd_ws = None
+    if op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd"):
+        fwd_ws = torch.empty(max(nf.nf_workspace_size(nf.OPS[op], rows, hidden), 16),
+                             dtype=torch.uint8, device=dev)
+        fwp, fwn = fwd_ws.data_ptr(), fwd_ws.numel()
     if op == "fused_add_rmsnorm":
         x, r, w = workloads.fused_inputs(tot, hidden, residual_scale=4.0, device=dev)
         px, pr, pw = x.data_ptr(), r.data_ptr(), w.data_ptr()
         keep = (x, r, w)
-        fn = lambda i, sh: lib.nf_fused_add_rmsnorm(px + (i % sets) * a2, pr + (i % sets) * a2, pw,  # noqa: E731
-                                                     rows, hidden, eps, sh)
+        fn = lambda i, sh: lib.nf_fused_add_rmsnorm_ws(px + (i % sets) * a2, pr + (i % sets) * a2, pw,  # noqa: E731
+                                                        rows, hidden, eps, fwp, fwn, sh)
     elif op == "rmsnorm_fwd":
         x, w = workloads.rms_inputs(tot, hidden, device=dev)
         y = torch.empty_like(x)
         px, py, pw = x.data_ptr(), y.data_ptr(), w.data_ptr()
         keep = (x, y, w)
-        fn = lambda i, sh: lib.nf_rmsnorm_fwd(py + (i % sets) * a2, px + (i % sets) * a2, pw,  # noqa: E731
-                                               rows, hidden, eps, sh)
+        fn = lambda i, sh: lib.nf_rmsnorm_fwd_ws(py + (i % sets) * a2, px + (i % sets) * a2, pw,  # noqa: E731
+                                                  rows, hidden, eps, fwp, fwn, sh)
     elif op == "layernorm_fwd":
         x, g, b = workloads.layernorm_fwd_inputs(tot, hidden, device=dev)
         y = torch.empty_like(x)
@@ -352,9 +359,9 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         rs = torch.empty(tot, device=dev)
         px, py, pg, pb, pm, pr = (t.data_ptr() for t in (x, y, g, b, m, rs))
         keep = (x, y, g, b, m, rs)
-        fn = lambda i, sh: lib.nf_layernorm_fwd(py + (i % sets) * a2, pm + (i % sets) * rows * 4,  # noqa: E731
-                                                 pr + (i % sets) * rows * 4, px + (i % sets) * a2,
-                                                 pg, pb, rows, hidden, eps, sh)
+        fn = lambda i, sh: lib.nf_layernorm_fwd_ws(py + (i % sets) * a2, pm + (i % sets) * rows * 4,  # noqa: E731
+                                                    pr + (i % sets) * rows * 4, px + (i % sets) * a2,
+                                                    pg, pb, rows, hidden, eps, fwp, fwn, sh)
     elif op == "rmsnorm_bwd":
         x, dy, w = workloads.rms_bwd_inputs(tot, hidden, device=dev)
         dx = torch.empty_like(x)
@@ -414,6 +421,8 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         fn = lambda i, sh: lib.nf_layernorm_bwd(pdx + (i % sets) * a2, pdg, pdb, pdy + (i % sets) * a2,  # noqa: E731
                                                  px + (i % sets) * a2, pm + (i % sets) * rows * 4,
                                                  pr + (i % sets) * rows * 4, pg, rows, hidden, pws, nws, sh)
+
+    keep = keep + (fwd_ws,)
 
     def launch(i, sh, _keep=keep):
         st = fn(i, sh)

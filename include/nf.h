@@ -33,7 +33,11 @@
  *           runtime-hidden kernels (NF_PATH_DYNAMIC); longer rows, up to
  *           262144 (forward) or 131072 (backward), run on the grid-parallel
  *           cluster kernels (NF_PATH_CLUSTER), which split one row over a
- *           cluster of 2, 4 or 8 CTAs.  Other values return
+ *           cluster of 2, 4 or 8 CTAs; longer still, up to
+ *           NF_SPLIT_MAX_HIDDEN, on the split kernels (NF_PATH_SPLIT), which
+ *           spread a row over any number of CTAs and need a workspace (the
+ *           forward ops then take the _ws entry points).  Other values
+ *           (not a positive multiple of 8, or longer) return
  *           NF_ERR_UNSUPPORTED_HIDDEN.
  * rows.     Any value >= 0; rows == 0 returns NF_OK without launching.
  * eps.      Finite and > 0.
@@ -95,14 +99,25 @@ typedef struct CUstream_st* nf_stream;
  *              to 32768 forward, 16384 backward); the row still sits in
  *              registers under a compile-time per-thread bound ("TMA inner
  *              persistent scheduler": dynamic block dimensions).  The only
- *              family for hidden sizes outside the compiled set.           */
+ *              family for hidden sizes outside the compiled set.
+ *   SPLIT   -- one row cut into 8192-element chunks, one CTA per (chunk,
+ *              row), the row statistics passed through a caller workspace
+ *              in global memory: grid-parallel inner normalization across
+ *              any number of CTAs ("Llu/ln bwd"), for rows longer than a
+ *              cluster holds (any multiple of 8 up to NF_SPLIT_MAX_HIDDEN).
+ *              Forward calls on this family need a workspace: use the _ws
+ *              entry points and nf_workspace_size.                          */
 typedef enum {
     NF_PATH_AUTO = 0,
     NF_PATH_REG = 1,
     NF_PATH_CLUSTER = 2,
     NF_PATH_BULK = 3,
-    NF_PATH_DYNAMIC = 4
+    NF_PATH_DYNAMIC = 4,
+    NF_PATH_SPLIT = 5
 } nf_path;
+
+/* Longest row any family handles (the split family). */
+#define NF_SPLIT_MAX_HIDDEN (1LL << 26)
 
 /* Operation ids for nf_plan_query. */
 typedef enum {
@@ -135,10 +150,35 @@ typedef struct {
 nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight,
                                int64_t rows, int64_t hidden, float eps, nf_stream stream);
 
+/* Bytes of workspace `op` needs for (rows, hidden) on the current device,
+ * enough under every kernel family (so nf_set_path cannot make it short).
+ * For the forward ops it is nonzero only because the split family (rows
+ * longer than a cluster holds, or forced) keeps per-row partial statistics
+ * there: rows * (8 * chunks + 8) bytes, chunks = ceil(hidden / 8192).  For
+ * the backward ops it equals nf_layernorm_bwd_workspace_size /
+ * nf_rmsnorm_bwd_workspace_size.  0 when rows == 0, hidden is unsupported,
+ * op is unknown or the device cannot be queried. */
+size_t nf_workspace_size(nf_op op, int64_t rows, int64_t hidden);
+
+/* The forward entry points with a caller workspace (16-byte aligned, at
+ * least nf_workspace_size(op, rows, hidden) bytes, contents irrelevant, not
+ * overlapping any argument).  They behave exactly as the plain calls; the
+ * workspace is used only when the plan is the split family (automatic
+ * beyond the runtime-hidden limits, or forced).  Without a workspace (the
+ * plain calls, or NULL here) an automatic split plan runs on the cluster
+ * family instead where that holds the row (hidden <= 262144); longer rows,
+ * or a forced split, return NF_ERR_WORKSPACE_TOO_SMALL. */
+nf_status nf_fused_add_rmsnorm_ws(void* x, void* residual, const void* weight, int64_t rows,
+                                  int64_t hidden, float eps, void* workspace,
+                                  size_t workspace_bytes, nf_stream stream);
+
 /* RMSNorm forward:  y[r][j] = bf16( x[r][j] * rsqrt(mean_k(x[r][k]^2) + eps) * weight[j] ).
  * y may be x itself (in place); any other overlap is rejected. */
 nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight,
                          int64_t rows, int64_t hidden, float eps, nf_stream stream);
+nf_status nf_rmsnorm_fwd_ws(void* y, const void* x, const void* weight, int64_t rows,
+                            int64_t hidden, float eps, void* workspace, size_t workspace_bytes,
+                            nf_stream stream);
 
 /* LayerNorm forward with biased variance:
  *     mean[r] = (1/H) sum_j x[r][j]
@@ -150,6 +190,10 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight,
 nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x,
                            const void* gamma, const void* beta,
                            int64_t rows, int64_t hidden, float eps, nf_stream stream);
+nf_status nf_layernorm_fwd_ws(void* y, float* mean, float* rstd, const void* x,
+                              const void* gamma, const void* beta, int64_t rows, int64_t hidden,
+                              float eps, void* workspace, size_t workspace_bytes,
+                              nf_stream stream);
 
 /* Bytes of workspace nf_layernorm_bwd needs for (rows, hidden) on the
  * current device, under any kernel family (0 when rows == 0 or hidden is

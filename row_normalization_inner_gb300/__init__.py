@@ -31,9 +31,10 @@ NF_ERR_CUDA = 5
 NF_ERR_TIMEOUT = 6
 NF_ERR_UNSUPPORTED_PATH = 7
 
-NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK, NF_PATH_DYNAMIC = 0, 1, 2, 3, 4
+NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_SPLIT = \
+    0, 1, 2, 3, 4, 5
 PATHS = {"auto": NF_PATH_AUTO, "reg": NF_PATH_REG, "cluster": NF_PATH_CLUSTER, "bulk": NF_PATH_BULK,
-         "dynamic": NF_PATH_DYNAMIC}
+         "dynamic": NF_PATH_DYNAMIC, "split": NF_PATH_SPLIT}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 NF_OP_FUSED_ADD_RMSNORM, NF_OP_RMSNORM_FWD, NF_OP_LAYERNORM_FWD, NF_OP_LAYERNORM_BWD, \
@@ -46,6 +47,7 @@ DYN_MAX_HIDDEN_FWD = 32768    # runtime-hidden path: any multiple of 8 up to the
 DYN_MAX_HIDDEN_BWD = 16384
 LONG_MAX_HIDDEN_FWD = 262144  # grid-parallel cluster path for longer rows
 LONG_MAX_HIDDEN_BWD = 131072
+SPLIT_MAX_HIDDEN = 1 << 26    # NF_SPLIT_MAX_HIDDEN: rows across any number of CTAs
 
 # Every symbol include/nf.h declares.
 EXPORTS = (
@@ -53,7 +55,8 @@ EXPORTS = (
     "nf_layernorm_bwd_workspace_size", "nf_layernorm_bwd",
     "nf_rmsnorm_bwd_workspace_size", "nf_rmsnorm_bwd", "nf_layernorm_bwd_noalloc",
     "nf_outer_norm_workspace_size", "nf_outer_norm_fwd", "nf_outer_norm_bwd",
-    "nf_fused_add_rmsnorm_bwd",
+    "nf_fused_add_rmsnorm_bwd", "nf_workspace_size", "nf_fused_add_rmsnorm_ws", "nf_rmsnorm_fwd_ws",
+    "nf_layernorm_fwd_ws",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
     "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
 )
@@ -91,6 +94,10 @@ def _bind(lib):
         "nf_fused_add_rmsnorm": (_S, [_P, _P, _P, _I64, _I64, _F, _P]),
         "nf_rmsnorm_fwd": (_S, [_P, _P, _P, _I64, _I64, _F, _P]),
         "nf_layernorm_fwd": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+        "nf_workspace_size": (ctypes.c_size_t, [ctypes.c_int, _I64, _I64]),
+        "nf_fused_add_rmsnorm_ws": (_S, [_P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
+        "nf_rmsnorm_fwd_ws": (_S, [_P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
+        "nf_layernorm_fwd_ws": (_S, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
         "nf_layernorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
         "nf_layernorm_bwd": (_S, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
         "nf_rmsnorm_bwd_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
@@ -144,6 +151,27 @@ def nf_fused_add_rmsnorm(x, residual, weight, rows, hidden, eps, stream) -> int:
 
 def nf_rmsnorm_fwd(y, x, weight, rows, hidden, eps, stream) -> int:
     return lib().nf_rmsnorm_fwd(y, x, weight, rows, hidden, eps, stream)
+
+
+def nf_workspace_size(op, rows, hidden) -> int:
+    return lib().nf_workspace_size(op, rows, hidden)
+
+
+def nf_fused_add_rmsnorm_ws(x, residual, weight, rows, hidden, eps, workspace, workspace_bytes,
+                            stream) -> int:
+    return lib().nf_fused_add_rmsnorm_ws(x, residual, weight, rows, hidden, eps, workspace,
+                                         workspace_bytes, stream)
+
+
+def nf_rmsnorm_fwd_ws(y, x, weight, rows, hidden, eps, workspace, workspace_bytes, stream) -> int:
+    return lib().nf_rmsnorm_fwd_ws(y, x, weight, rows, hidden, eps, workspace, workspace_bytes,
+                                   stream)
+
+
+def nf_layernorm_fwd_ws(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
+                        workspace_bytes, stream) -> int:
+    return lib().nf_layernorm_fwd_ws(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
+                                     workspace_bytes, stream)
 
 
 def nf_layernorm_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps, stream) -> int:
@@ -267,7 +295,23 @@ def _rows_hidden(x):
     return rows, hidden
 
 
-def fused_add_rmsnorm(x, residual, weight, eps: float = 1e-6, stream=None):
+def _fwd_workspace(op, rows, hidden, device, workspace):
+    """(pointer, bytes) of the workspace a forward call needs now: a caller
+    tensor if given, else one allocated here (by PyTorch) only when the
+    plan is the split family."""
+    import torch
+    if workspace is not None:
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if rows == 0 or nf_plan_query(op, rows, hidden)["path"] != "split":
+        return None, 0
+    n = nf_workspace_size(OPS[op], rows, hidden)
+    # freed right after the launch: PyTorch's allocator hands the block to
+    # later work on the same stream only, which runs after these kernels
+    t = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    return t.data_ptr(), n
+
+
+def fused_add_rmsnorm(x, residual, weight, eps: float = 1e-6, stream=None, workspace=None):
     """In place: residual += x; x = rmsnorm(residual) * weight.  Returns (x, residual)."""
     import torch
     for t, n in ((x, "x"), (residual, "residual"), (weight, "weight")):
@@ -275,24 +319,26 @@ def fused_add_rmsnorm(x, residual, weight, eps: float = 1e-6, stream=None):
     rows, hidden = _rows_hidden(x)
     if residual.shape != x.shape or weight.shape != (hidden,):
         raise ValueError("shape mismatch")
-    _check(nf_fused_add_rmsnorm(x.data_ptr(), residual.data_ptr(), weight.data_ptr(), rows, hidden,
-                                eps, _stream(stream)), "nf_fused_add_rmsnorm")
+    wp, wb = _fwd_workspace("fused_add_rmsnorm", rows, hidden, x.device, workspace)
+    _check(nf_fused_add_rmsnorm_ws(x.data_ptr(), residual.data_ptr(), weight.data_ptr(), rows,
+                                   hidden, eps, wp, wb, _stream(stream)), "nf_fused_add_rmsnorm_ws")
     return x, residual
 
 
-def rmsnorm_fwd(x, weight, eps: float = 1e-6, out=None, stream=None):
+def rmsnorm_fwd(x, weight, eps: float = 1e-6, out=None, stream=None, workspace=None):
     import torch
     _need(x, torch.bfloat16, "x")
     _need(weight, torch.bfloat16, "weight")
     rows, hidden = _rows_hidden(x)
     y = torch.empty_like(x) if out is None else out
     _need(y, torch.bfloat16, "out")
-    _check(nf_rmsnorm_fwd(y.data_ptr(), x.data_ptr(), weight.data_ptr(), rows, hidden, eps,
-                          _stream(stream)), "nf_rmsnorm_fwd")
+    wp, wb = _fwd_workspace("rmsnorm_fwd", rows, hidden, x.device, workspace)
+    _check(nf_rmsnorm_fwd_ws(y.data_ptr(), x.data_ptr(), weight.data_ptr(), rows, hidden, eps,
+                             wp, wb, _stream(stream)), "nf_rmsnorm_fwd_ws")
     return y
 
 
-def layernorm_fwd(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
+def layernorm_fwd(x, gamma, beta, eps: float = 1e-5, out=None, stream=None, workspace=None):
     """Returns (y bf16, mean fp32 [rows], rstd fp32 [rows])."""
     import torch
     for t, n in ((x, "x"), (gamma, "gamma"), (beta, "beta")):
@@ -301,9 +347,10 @@ def layernorm_fwd(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
     y = torch.empty_like(x) if out is None else out
     mean = torch.empty(rows, dtype=torch.float32, device=x.device)
     rstd = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _check(nf_layernorm_fwd(y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), x.data_ptr(),
-                            gamma.data_ptr(), beta.data_ptr(), rows, hidden, eps, _stream(stream)),
-           "nf_layernorm_fwd")
+    wp, wb = _fwd_workspace("layernorm_fwd", rows, hidden, x.device, workspace)
+    _check(nf_layernorm_fwd_ws(y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), x.data_ptr(),
+                               gamma.data_ptr(), beta.data_ptr(), rows, hidden, eps, wp, wb,
+                               _stream(stream)), "nf_layernorm_fwd_ws")
     return y, mean, rstd
 
 

@@ -123,9 +123,11 @@ bool hidden_ok(int64_t h) {
 
 // A size some kernel of `op` handles (compiled, the runtime-hidden path, or
 // the grid-parallel cluster path for long rows).
+bool split_ok(int64_t h) { return h >= kVec && h % kVec == 0 && h <= kSplitMaxHidden; }
+
 bool hidden_supported(nf_op op, int64_t h) {
     int t, c, sl;
-    return hidden_ok(h) || dyn_shape(op, h, &t) || long_shape(op, h, &c, &t, &sl);
+    return hidden_ok(h) || dyn_shape(op, h, &t) || long_shape(op, h, &c, &t, &sl) || split_ok(h);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -165,21 +167,53 @@ nf_status plan_for_call(nf_op op, int64_t rows, int64_t hidden, nf_plan* plan) {
                            static_cast<nf_path>(g_forced_path.load(std::memory_order_relaxed)), plan);
 }
 
-size_t bwd_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
+// The plan of a forward call.  Without a workspace, an automatic split plan
+// falls back to the cluster family where that holds the row, so the plain
+// forward entry points keep working up to the cluster limit.
+nf_status plan_for_fwd(nf_op op, int64_t rows, int64_t hidden, bool have_ws, nf_plan* plan) {
+    if (nf_status st = plan_for_call(op, rows, hidden, plan)) return st;
+    if (have_ws || plan->path != NF_PATH_SPLIT ||
+        g_forced_path.load(std::memory_order_relaxed) != NF_PATH_AUTO)
+        return NF_OK;
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    nf_plan alt;
+    if (nf_plan_compute(op, rows, hidden, sms, NF_PATH_CLUSTER, &alt) == NF_OK) *plan = alt;
+    return NF_OK;
+}
+
+// Workspace bytes for `op` enough for every kernel family, so a later
+// nf_set_path cannot make a previously sized workspace too small.
+size_t any_path_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
     if (!hidden_supported(op, hidden) || rows <= 0) return 0;
     int sms;
     if (device_sm_count(&sms) != NF_OK) return 0;
-    // enough for every backward path, so a later nf_set_path cannot make a
-    // previously sized workspace too small
     size_t most = 0;
-    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER}) {
+    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER, NF_PATH_SPLIT}) {
         nf_plan pl;
         if (nf_plan_compute(op, rows, hidden, sms, p, &pl) != NF_OK) continue;
-        const size_t b = static_cast<size_t>(pl.partials) * bwd_planes(op) *
-                         static_cast<size_t>(hidden) * sizeof(float);
+        const size_t b = plan_workspace_bytes(op, rows, hidden, sms, pl.path, pl.partials);
         if (b > most) most = b;
     }
     return most;
+}
+
+size_t bwd_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
+    return any_path_workspace_bytes(op, rows, hidden);
+}
+
+// The workspace a call needs under its plan, with the usual checks:
+// NF_ERR_WORKSPACE_TOO_SMALL when it is short (or missing), NF_ERR_MISALIGNED
+// when it is not 16-byte aligned.  *need = 0 for plans that use none.
+nf_status check_workspace(nf_op op, int64_t rows, int64_t hidden, const nf_plan& pl,
+                          const void* workspace, size_t workspace_bytes, size_t* need) {
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    *need = plan_workspace_bytes(op, rows, hidden, sms, pl.path, pl.partials);
+    if (*need == 0) return NF_OK;
+    if (!workspace || workspace_bytes < *need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return NF_ERR_MISALIGNED;
+    return NF_OK;
 }
 
 // The selftest kernel: one thread waits on a barrier nothing will complete.
@@ -197,6 +231,14 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 }  // namespace
 
+size_t plan_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms, int path, int partials) {
+    if (path == NF_PATH_SPLIT) return split_workspace_bytes(op, rows, hidden, sms);
+    if (op == NF_OP_LAYERNORM_BWD || op == NF_OP_RMSNORM_BWD)
+        return static_cast<size_t>(partials) * bwd_planes(static_cast<nf_op>(op)) *
+               static_cast<size_t>(hidden) * sizeof(float);
+    return 0;
+}
+
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {
     wait_selftest_kernel<<<1, 32, 0, st>>>(status, timeout_ns);
     return cudaGetLastError();
@@ -212,19 +254,23 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
                           nf_plan* out) {
     if (!out || rows < 0 || sm_count < 1) return NF_ERR_INVALID_ARG;
     if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return NF_ERR_INVALID_ARG;
-    if (path < NF_PATH_AUTO || path > NF_PATH_DYNAMIC) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_SPLIT) return NF_ERR_INVALID_ARG;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
     int tpr = 0, rpc = 1, dyn_threads = 0, long_c = 0, long_t = 0, long_slice = 0;
     const bool compiled = reg_shape(hidden, &tpr, &rpc);
     const bool dyn_ok = dyn_shape(op, hidden, &dyn_threads);
     const bool long_ok = long_shape(op, hidden, &long_c, &long_t, &long_slice);
-    if (!compiled && !dyn_ok && !long_ok) return NF_ERR_UNSUPPORTED_HIDDEN;
+    const bool splittable = split_ok(hidden);
+    if (!compiled && !dyn_ok && !long_ok && !splittable) return NF_ERR_UNSUPPORTED_HIDDEN;
 
     nf_path p = path;
     if (p == NF_PATH_AUTO)
+        // beyond the runtime-hidden limits the split family beat the
+        // cluster kernels at every measured row count (1.1-2.3x)
         p = compiled ? auto_path(op, rows, hidden, rpc, sm_count)
-                     : (dyn_ok ? NF_PATH_DYNAMIC : NF_PATH_CLUSTER);
+                     : dyn_ok ? NF_PATH_DYNAMIC : splittable ? NF_PATH_SPLIT : NF_PATH_CLUSTER;
+    if (p == NF_PATH_SPLIT && !splittable) return NF_ERR_UNSUPPORTED_PATH;
     if ((p == NF_PATH_REG || p == NF_PATH_BULK) && !compiled) return NF_ERR_UNSUPPORTED_PATH;
     if (p == NF_PATH_DYNAMIC && !dyn_ok) return NF_ERR_UNSUPPORTED_PATH;
     // the cluster family: the static kernels for compiled forward sizes,
@@ -236,7 +282,22 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
     std::memset(&pl, 0, sizeof pl);
     pl.path = p;
     constexpr int64_t kMaxGrid = 0x7FFFFFFF;
-    if (p == NF_PATH_REG && fwd) {
+    if (p == NF_PATH_SPLIT) {
+        int nc, rb;
+        split_shape(op, rows, hidden, sm_count, &nc, &rb);
+        const int64_t ry = rows < 65535 ? (rows > 0 ? rows : 1) : 65535;
+        pl.block = 256;
+        pl.cluster = 1;
+        pl.rows_per_cta = 1;
+        if (fwd) {
+            pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * ry);
+            pl.launches = 3;
+        } else {
+            pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * rb);
+            pl.launches = 4;
+            pl.partials = rb;
+        }
+    } else if (p == NF_PATH_REG && fwd) {
         const int64_t blocks = (rows + rpc - 1) / rpc;
         pl.grid = static_cast<int32_t>(blocks < kMaxGrid ? blocks : kMaxGrid);
         pl.block = tpr * rpc;
@@ -315,7 +376,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
 }
 
 nf_status nf_set_path(nf_path path) {
-    if (path < NF_PATH_AUTO || path > NF_PATH_DYNAMIC) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_SPLIT) return NF_ERR_INVALID_ARG;
     g_forced_path.store(path, std::memory_order_relaxed);
     return NF_OK;
 }
@@ -328,8 +389,19 @@ nf_status nf_plan_query(nf_op op, int64_t rows, int64_t hidden, nf_plan* out) {
     return plan_for_call(op, rows, hidden, out);
 }
 
+size_t nf_workspace_size(nf_op op, int64_t rows, int64_t hidden) {
+    if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return 0;
+    return any_path_workspace_bytes(op, rows, hidden);
+}
+
 nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int64_t rows,
                                int64_t hidden, float eps, nf_stream stream) {
+    return nf_fused_add_rmsnorm_ws(x, residual, weight, rows, hidden, eps, nullptr, 0, stream);
+}
+
+nf_status nf_fused_add_rmsnorm_ws(void* x, void* residual, const void* weight, int64_t rows,
+                                  int64_t hidden, float eps, void* workspace,
+                                  size_t workspace_bytes, nf_stream stream) {
     if (nf_status st = common_checks(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!x || !residual || !weight) return NF_ERR_INVALID_ARG;
@@ -339,8 +411,30 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
         overlap({residual, act}, {weight, par}))
         return NF_ERR_INVALID_ARG;
     nf_plan pl;
-    if (nf_status st = plan_for_call(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, &pl)) return st;
+    if (nf_status st = plan_for_fwd(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, workspace != nullptr, &pl))
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_SPLIT) {
+        size_t need;
+        if (nf_status st = check_workspace(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, pl, workspace,
+                                           workspace_bytes, &need))
+            return st;
+        const Span sws{workspace, static_cast<int64_t>(need)};
+        if (overlap(sws, {x, act}) || overlap(sws, {residual, act}) || overlap(sws, {weight, par}))
+            return NF_ERR_INVALID_ARG;
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(x);
+        a.out1 = static_cast<uint16_t*>(residual);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.in1 = static_cast<const uint16_t*>(residual);
+        a.p0 = static_cast<const uint16_t*>(weight);
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        int sms;
+        if (nf_status st = device_sm_count(&sms)) return st;
+        return from_cuda(launch_split(NF_OP_FUSED_ADD_RMSNORM, a, workspace, sms, s));
+    }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
     if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
@@ -366,6 +460,12 @@ nf_status nf_fused_add_rmsnorm(void* x, void* residual, const void* weight, int6
 
 nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t rows, int64_t hidden,
                          float eps, nf_stream stream) {
+    return nf_rmsnorm_fwd_ws(y, x, weight, rows, hidden, eps, nullptr, 0, stream);
+}
+
+nf_status nf_rmsnorm_fwd_ws(void* y, const void* x, const void* weight, int64_t rows,
+                            int64_t hidden, float eps, void* workspace, size_t workspace_bytes,
+                            nf_stream stream) {
     if (nf_status st = common_checks(NF_OP_RMSNORM_FWD, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!y || !x || !weight) return NF_ERR_INVALID_ARG;
@@ -374,8 +474,28 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
     if (bad_overlap_except_alias({y, act}, {x, act}) || overlap({y, act}, {weight, par}))
         return NF_ERR_INVALID_ARG;
     nf_plan pl;
-    if (nf_status st = plan_for_call(NF_OP_RMSNORM_FWD, rows, hidden, &pl)) return st;
+    if (nf_status st = plan_for_fwd(NF_OP_RMSNORM_FWD, rows, hidden, workspace != nullptr, &pl))
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_SPLIT) {
+        size_t need;
+        if (nf_status st = check_workspace(NF_OP_RMSNORM_FWD, rows, hidden, pl, workspace,
+                                           workspace_bytes, &need))
+            return st;
+        const Span sws{workspace, static_cast<int64_t>(need)};
+        if (overlap(sws, {y, act}) || overlap(sws, {x, act}) || overlap(sws, {weight, par}))
+            return NF_ERR_INVALID_ARG;
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(y);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.p0 = static_cast<const uint16_t*>(weight);
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        int sms;
+        if (nf_status st = device_sm_count(&sms)) return st;
+        return from_cuda(launch_split(NF_OP_RMSNORM_FWD, a, workspace, sms, s));
+    }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
     if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
@@ -400,6 +520,13 @@ nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t row
 nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                            const void* beta, int64_t rows, int64_t hidden, float eps,
                            nf_stream stream) {
+    return nf_layernorm_fwd_ws(y, mean, rstd, x, gamma, beta, rows, hidden, eps, nullptr, 0,
+                               stream);
+}
+
+nf_status nf_layernorm_fwd_ws(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                              const void* beta, int64_t rows, int64_t hidden, float eps,
+                              void* workspace, size_t workspace_bytes, nf_stream stream) {
     if (nf_status st = common_checks(NF_OP_LAYERNORM_FWD, rows, hidden, eps, true)) return st;
     if (rows == 0) return NF_OK;
     if (!y || !x || !gamma || !beta) return NF_ERR_INVALID_ARG;
@@ -415,8 +542,32 @@ nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, con
             overlap(o, {beta, par}))
             return NF_ERR_INVALID_ARG;
     nf_plan pl;
-    if (nf_status st = plan_for_call(NF_OP_LAYERNORM_FWD, rows, hidden, &pl)) return st;
+    if (nf_status st = plan_for_fwd(NF_OP_LAYERNORM_FWD, rows, hidden, workspace != nullptr, &pl))
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.path == NF_PATH_SPLIT) {
+        size_t need;
+        if (nf_status st = check_workspace(NF_OP_LAYERNORM_FWD, rows, hidden, pl, workspace,
+                                           workspace_bytes, &need))
+            return st;
+        const Span sws{workspace, static_cast<int64_t>(need)};
+        if (overlap(sws, {y, act}) || overlap(sws, {x, act}) || overlap(sws, {gamma, par}) ||
+            overlap(sws, {beta, par}) || overlap(sws, {mean, stat}) || overlap(sws, {rstd, stat}))
+            return NF_ERR_INVALID_ARG;
+        DynArgs a{};
+        a.out0 = static_cast<uint16_t*>(y);
+        a.in0 = static_cast<const uint16_t*>(x);
+        a.p0 = static_cast<const uint16_t*>(gamma);
+        a.p1 = static_cast<const uint16_t*>(beta);
+        a.mean = mean;
+        a.rstd = rstd;
+        a.rows = rows;
+        a.hidden = static_cast<int>(hidden);
+        a.eps = eps;
+        int sms;
+        if (nf_status st = device_sm_count(&sms)) return st;
+        return from_cuda(launch_split(NF_OP_LAYERNORM_FWD, a, workspace, sms, s));
+    }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
                                                pl.grid, s));
@@ -469,8 +620,10 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
-    const size_t need = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
-    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    size_t need;
+    if (nf_status st = check_workspace(NF_OP_LAYERNORM_BWD, rows, hidden, pl, workspace,
+                                       workspace_bytes, &need))
+        return st;
     const int64_t act = rows * hidden * 2, par = hidden * 2, stat = rows * 4, grad = hidden * 4;
     const Span sdx{dx, act}, sdg{dgamma, grad}, sdb{dbeta, grad}, sws{workspace, static_cast<int64_t>(need)};
     const Span ins[] = {{dy, act}, {x, act}, {mean, stat}, {rstd, stat}, {gamma, par}};
@@ -485,7 +638,7 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
             return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -496,8 +649,13 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         a.ws = ws;
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
-        const cudaError_t e = pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_LAYERNORM_BWD, a, pl.grid, s)
-                                                         : launch_dyn(NF_OP_LAYERNORM_BWD, a, pl.grid, s);
+        int sms = 0;
+        if (pl.path == NF_PATH_SPLIT)
+            if (nf_status st = device_sm_count(&sms)) return st;
+        const cudaError_t e =
+            pl.path == NF_PATH_SPLIT     ? launch_split(NF_OP_LAYERNORM_BWD, a, workspace, sms, s)
+            : pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_LAYERNORM_BWD, a, pl.grid, s)
+                                         : launch_dyn(NF_OP_LAYERNORM_BWD, a, pl.grid, s);
         if (e != cudaSuccess) return from_cuda(e);
     } else if (pl.path == NF_PATH_BULK) {
         int* status;
@@ -536,8 +694,10 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_RMSNORM_BWD, rows, hidden, &pl)) return st;
-    const size_t need = static_cast<size_t>(pl.partials) * static_cast<size_t>(hidden) * sizeof(float);
-    if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
+    size_t need;
+    if (nf_status st = check_workspace(NF_OP_RMSNORM_BWD, rows, hidden, pl, workspace,
+                                       workspace_bytes, &need))
+        return st;
     const int64_t act = rows * hidden * 2, par = hidden * 2, grad = hidden * 4;
     const Span sdx{dx, act}, sdw{dw, grad}, sws{workspace, static_cast<int64_t>(need)};
     const Span ins[] = {{dy, act}, {x, act}, {dres, dres ? act : 0}, {weight, par}};
@@ -549,7 +709,7 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         if (dx_clash || overlap(sdw, in) || overlap(sws, in)) return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -560,8 +720,13 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
-        const cudaError_t e = pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_RMSNORM_BWD, a, pl.grid, s)
-                                                         : launch_dyn(NF_OP_RMSNORM_BWD, a, pl.grid, s);
+        int sms = 0;
+        if (pl.path == NF_PATH_SPLIT)
+            if (nf_status st = device_sm_count(&sms)) return st;
+        const cudaError_t e =
+            pl.path == NF_PATH_SPLIT     ? launch_split(NF_OP_RMSNORM_BWD, a, workspace, sms, s)
+            : pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_RMSNORM_BWD, a, pl.grid, s)
+                                         : launch_dyn(NF_OP_RMSNORM_BWD, a, pl.grid, s);
         if (e != cudaSuccess) return from_cuda(e);
     } else if (pl.path == NF_PATH_BULK) {
         int* status;

@@ -251,6 +251,30 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     }
 }
 
+// The same sums when there are few slots (<= kNarrowSlots): one float4
+// column per thread, the slots added in order, so a CTA covers 1024
+// contiguous columns instead of 32 (the wide form would launch a CTA per 32
+// columns with 31 of its 32 slot lanes idle).
+constexpr int kNarrowSlots = 8;
+constexpr int kNarrowT = 256;
+
+__global__ void __launch_bounds__(kNarrowT)
+column_reduce_narrow(const float* __restrict__ ws, float* __restrict__ dgamma,
+                     float* __restrict__ dbeta, int nslots, int hidden, int planes) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kNarrowT + threadIdx.x;
+    if (c4 * 4 >= planes * static_cast<int64_t>(hidden)) return;
+    const int which = static_cast<int>((c4 * 4) / hidden);
+    const int64_t j = (c4 * 4) % hidden;
+    float4 s = __ldcs(reinterpret_cast<const float4*>(ws + static_cast<int64_t>(which) * hidden + j));
+    for (int p = 1; p < nslots; ++p) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(
+            ws + (static_cast<int64_t>(p) * planes + which) * hidden + j));
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    *reinterpret_cast<float4*>((which == 0 ? dgamma : dbeta) + j) = s;
+}
+
 }  // namespace
 
 cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
@@ -279,6 +303,12 @@ cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (nslots <= kNarrowSlots) {
+        cfg.gridDim = dim3(static_cast<unsigned>((cols4 + kNarrowT - 1) / kNarrowT), 1, 1);
+        cfg.blockDim = dim3(kNarrowT, 1, 1);
+        return cudaLaunchKernelEx(&cfg, column_reduce_narrow, ws, out0, out1, nslots,
+                                  static_cast<int>(hidden), planes);
+    }
     return cudaLaunchKernelEx(&cfg, column_reduce, ws, out0, out1, nslots,
                               static_cast<int>(hidden), planes);
 }

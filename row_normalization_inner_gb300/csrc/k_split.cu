@@ -1,0 +1,494 @@
+// Grid-parallel inner normalization across any number of CTAs: a row is
+// cut into chunks of 8192 elements, one CTA per (chunk, row), and the row
+// statistics travel through global memory instead of a cluster's shared
+// memory.  The "Llu/ln bwd" discussion names grid-parallel inner
+// normalization as the missing normalization variant; the cluster kernels
+// cover rows up to 8 CTAs, this family any length (the chunk count is not
+// bounded by a cluster).
+//
+// Forward (fused add + RMSNorm, RMSNorm, LayerNorm), three launches:
+//   1. split_stats: per (row, chunk) partial statistics -> part[row][chunk][2]
+//      (RMS: sum of squares; LayerNorm: the chunk's mean and M2, two passes
+//      over the chunk held in registers);
+//   2. split_merge: one CTA per row merges its chunks in a fixed order
+//      (thread t takes chunks t, t + 256, ..., then a fixed tree; Chan's
+//      formula for LayerNorm) -> stat[row] = (mean, rstd);
+//   3. split_apply: per (row, chunk) re-reads the chunk (from L2 when the
+//      batch fits there) and writes the normalized output.
+// The fused op reads x and residual in launches 1 and 3 and writes both in
+// 3, so it normalizes the unrounded fp32 sum like every other family.
+//
+// Backward (LayerNorm, RMSNorm, fused-add RMSNorm), four launches: the row
+// sums (LN: sum g, sum g * xhat; RMS: sum x^2, sum g * x) by (row, chunk),
+// a per-row merge, then split_bwd_apply over (chunk, row block) CTAs that
+// write dx and accumulate the column sums of their rows in registers (one
+// workspace slot per row block), and the fixed-order column reduction.
+//
+// Every launch after the first is a programmatic dependent of the one
+// before (griddepcontrol.wait before any read), and every sum runs in a
+// fixed order, so results are deterministic.
+#include "common.cuh"
+#include "launch.h"
+
+namespace nf {
+namespace {
+
+constexpr int kSpT = 256;                 // threads per CTA
+constexpr int kSpV = 4;                   // vectors per thread
+constexpr int kSpVecs = kSpT * kSpV;      // vectors per chunk
+constexpr int kSpChunk = kSpVecs * kVec;  // elements per chunk
+constexpr int kSpMaxGridY = 65535;
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Sum N values over the CTA (warp shuffles, then the 8 warps in order);
+// every thread gets the totals.  `red` holds 8 * N floats; callers
+// alternate two buffers between consecutive calls.
+template <int N>
+__device__ __forceinline__ void cta_sum(float (&v)[N], float* red) {
+    warp_sum<N>(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) red[warp * N + i] = v[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSpT / 32; ++w) s += red[w * N + i];
+        v[i] = s;
+    }
+}
+
+struct Chan {
+    float n, mean, m2;
+};
+
+__device__ __forceinline__ Chan chan_merge(Chan a, Chan b) {
+    if (a.n == 0.f) return b;
+    if (b.n == 0.f) return a;
+    const float n = a.n + b.n;
+    const float d = b.mean - a.mean;
+    const float wb = b.n / n;
+    return {n, a.mean + d * wb, a.m2 + b.m2 + d * d * a.n * wb};
+}
+
+// Elements of chunk c of a row of H elements.
+__device__ __forceinline__ int chunk_len(int c, int H) {
+    const int rest = H - c * kSpChunk;
+    return rest < kSpChunk ? rest : kSpChunk;
+}
+
+// Load this thread's vectors of chunk c of row r, widened; invalid vectors
+// are zero.  Vector k of thread t is chunk vector k * kSpT + t.
+__device__ __forceinline__ void load_chunk(const uint16_t* src, int64_t r, int c, int H,
+                                           float (&f)[kSpV][8]) {
+    const int NV = H / kVec;
+#pragma unroll
+    for (int k = 0; k < kSpV; ++k) {
+        const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (v < NV) u = ld_stream(src + r * H + static_cast<int64_t>(v) * kVec);
+        unpack8(u, f[k]);
+    }
+}
+
+// ---- forward ----------------------------------------------------------------
+// OP: 0 fused add + RMSNorm, 1 RMSNorm, 2 LayerNorm.
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict__ part, int nc) {
+    __shared__ float red[2][8 * 1];
+    pdl_wait();
+    const int c = blockIdx.x, H = a.hidden;
+    const int NV = H / kVec;
+    for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+        float f[kSpV][8];
+        load_chunk(a.in0, r, c, H, f);
+        if constexpr (OP == 0) {
+            float b[kSpV][8];
+            load_chunk(a.in1, r, c, H, b);
+#pragma unroll
+            for (int k = 0; k < kSpV; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[k][e] += b[k][e];
+        }
+        float2 out;
+        if constexpr (OP == 2) {
+            float s[1] = {0.f};
+#pragma unroll
+            for (int k = 0; k < kSpV; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[0] += f[k][e];
+            cta_sum<1>(s, red[0]);
+            const float mean = s[0] / static_cast<float>(chunk_len(c, H));
+            float q[1] = {0.f};
+#pragma unroll
+            for (int k = 0; k < kSpV; ++k) {
+                if (c * kSpVecs + k * kSpT + static_cast<int>(threadIdx.x) < NV) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float d = f[k][e] - mean;
+                        q[0] = fmaf(d, d, q[0]);
+                    }
+                }
+            }
+            cta_sum<1>(q, red[1]);
+            out = make_float2(mean, q[0]);
+        } else {
+            float q[1] = {0.f};
+#pragma unroll
+            for (int k = 0; k < kSpV; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[0] = fmaf(f[k][e], f[k][e], q[0]);
+            cta_sum<1>(q, red[0]);
+            out = make_float2(q[0], 0.f);
+        }
+        if (threadIdx.x == 0) reinterpret_cast<float2*>(part)[r * nc + c] = out;
+        __syncthreads();  // red is reused by the next row
+    }
+}
+
+// One CTA per row: merge the row's chunk partials -> stat[row] = (mean, rstd).
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_merge_fwd(DynArgs a, const float* __restrict__ part,
+                                                        float2* __restrict__ stat, int nc) {
+    __shared__ Chan sh[kSpT / 32];
+    pdl_wait();
+    const int H = a.hidden;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float2* p2 = reinterpret_cast<const float2*>(part);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        Chan acc{0.f, 0.f, 0.f};
+        for (int c = threadIdx.x; c < nc; c += kSpT) {
+            const float2 p = __ldcg(p2 + r * nc + c);
+            if constexpr (OP == 2) {
+                acc = chan_merge(acc, Chan{static_cast<float>(chunk_len(c, H)), p.x, p.y});
+            } else {
+                acc.n = 1.f;
+                acc.m2 += p.x;  // sum of squares
+            }
+        }
+        // fixed tree: lanes, then warps in order
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const Chan o{__shfl_down_sync(0xffffffffu, acc.n, off),
+                         __shfl_down_sync(0xffffffffu, acc.mean, off),
+                         __shfl_down_sync(0xffffffffu, acc.m2, off)};
+            if (lane < off) {
+                if constexpr (OP == 2) {
+                    acc = chan_merge(acc, o);
+                } else {
+                    acc.m2 += o.m2;
+                }
+            }
+        }
+        if (lane == 0) sh[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            Chan t = sh[0];
+#pragma unroll
+            for (int w = 1; w < kSpT / 32; ++w) {
+                if constexpr (OP == 2) {
+                    t = chan_merge(t, sh[w]);
+                } else {
+                    t.m2 += sh[w].m2;
+                }
+            }
+            const float invH = 1.0f / static_cast<float>(H);
+            const float rstd = rsqrtf(t.m2 * invH + a.eps);
+            const float mean = OP == 2 ? t.mean : 0.f;
+            stat[r] = make_float2(mean, rstd);
+            if (OP == 2) {
+                if (a.mean) a.mean[r] = mean;
+                if (a.rstd) a.rstd[r] = rstd;
+            }
+        }
+        __syncthreads();  // sh is reused by the next row
+    }
+}
+
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float2* __restrict__ stat) {
+    pdl_wait();
+    const int c = blockIdx.x, H = a.hidden;
+    const int NV = H / kVec;
+    for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+        const float2 st = __ldcg(stat + r);
+        float f[kSpV][8];
+        load_chunk(a.in0, r, c, H, f);
+        if constexpr (OP == 0) {
+            float b[kSpV][8];
+            load_chunk(a.in1, r, c, H, b);
+#pragma unroll
+            for (int k = 0; k < kSpV; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[k][e] += b[k][e];
+        }
+#pragma unroll
+        for (int k = 0; k < kSpV; ++k) {
+            const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+            if (v >= NV) continue;
+            const int64_t off = r * H + static_cast<int64_t>(v) * kVec;
+            float p[8], o[8];
+            unpack8(ld_param(a.p0 + static_cast<int64_t>(v) * kVec), p);
+            if constexpr (OP == 2) {
+                float b[8];
+                unpack8(ld_param(a.p1 + static_cast<int64_t>(v) * kVec), b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(f[k][e] - st.x, st.y * p[e], b[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = f[k][e] * st.y * p[e];
+            }
+            if constexpr (OP == 0) st_stream(a.out1 + off, pack8(f[k]));  // residual <- s
+            st_stream(a.out0 + off, pack8(o));
+        }
+    }
+}
+
+// ---- backward -----------------------------------------------------------------
+// OP: 3 LayerNorm (saved mean / rstd), 4 RMSNorm (rstd recomputed; a.add is
+// the fused-add residual-stream gradient, or null).  in0 = x, in1 = dy.
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_stats_bwd(DynArgs a, float* __restrict__ part, int nc) {
+    __shared__ float red[8 * 2];
+    pdl_wait();
+    const int c = blockIdx.x, H = a.hidden;
+    const int NV = H / kVec;
+    for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+        float x[kSpV][8], dy[kSpV][8];
+        load_chunk(a.in0, r, c, H, x);
+        load_chunk(a.in1, r, c, H, dy);
+        const float mu = OP == 3 ? __ldg(a.mean + r) : 0.f;
+        const float rs = OP == 3 ? __ldg(a.rstd + r) : 0.f;
+        float s[2] = {0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kSpV; ++k) {
+            const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+            if (v >= NV) continue;
+            float w[8];
+            unpack8(ld_param(a.p0 + static_cast<int64_t>(v) * kVec), w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float g = dy[k][e] * w[e];
+                if constexpr (OP == 3) {
+                    s[0] += g;
+                    s[1] = fmaf(g, (x[k][e] - mu) * rs, s[1]);
+                } else {
+                    s[0] = fmaf(x[k][e], x[k][e], s[0]);
+                    s[1] = fmaf(g, x[k][e], s[1]);
+                }
+            }
+        }
+        cta_sum<2>(s, red);
+        if (threadIdx.x == 0) reinterpret_cast<float2*>(part)[r * nc + c] = make_float2(s[0], s[1]);
+        __syncthreads();
+    }
+}
+
+// One CTA per row: stat[row] = LN (A, B) = (sum g / H, sum g xhat / H);
+// RMS (rstd, rstd^3 * sum g x / H).
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_merge_bwd(DynArgs a, const float* __restrict__ part,
+                                                        float2* __restrict__ stat, int nc) {
+    __shared__ float red[8 * 2];
+    pdl_wait();
+    const float2* p2 = reinterpret_cast<const float2*>(part);
+    const float invH = 1.0f / static_cast<float>(a.hidden);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        float s[2] = {0.f, 0.f};
+        for (int c = threadIdx.x; c < nc; c += kSpT) {
+            const float2 p = __ldcg(p2 + r * nc + c);
+            s[0] += p.x;
+            s[1] += p.y;
+        }
+        cta_sum<2>(s, red);
+        if (threadIdx.x == 0) {
+            if constexpr (OP == 3) {
+                stat[r] = make_float2(s[0] * invH, s[1] * invH);
+            } else {
+                const float rs = rsqrtf(s[0] * invH + a.eps);
+                stat[r] = make_float2(rs, rs * rs * rs * s[1] * invH);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Grid (chunks, row blocks): dx for the block's rows, and the block's column
+// sums of its chunk -> ws[block][plane][H].
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2* __restrict__ stat) {
+    constexpr int NP = OP == 3 ? 2 : 1;
+    pdl_wait();
+    const int c = blockIdx.x, H = a.hidden;
+    const int NV = H / kVec;
+    const int64_t nb = gridDim.y;
+    const int64_t r0 = a.rows * blockIdx.y / nb, r1 = a.rows * (blockIdx.y + 1) / nb;
+    float acc0[kSpV][8], acc1[NP == 2 ? kSpV : 1][8];
+#pragma unroll
+    for (int k = 0; k < kSpV; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            acc0[k][e] = 0.f;
+            if constexpr (NP == 2) acc1[k][e] = 0.f;
+        }
+    for (int64_t r = r0; r < r1; ++r) {
+        const float2 st = __ldcg(stat + r);
+        float x[kSpV][8], dy[kSpV][8];
+        load_chunk(a.in0, r, c, H, x);
+        load_chunk(a.in1, r, c, H, dy);
+        const float mu = OP == 3 ? __ldg(a.mean + r) : 0.f;
+        const float rs = OP == 3 ? __ldg(a.rstd + r) : st.x;
+#pragma unroll
+        for (int k = 0; k < kSpV; ++k) {
+            const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+            if (v >= NV) continue;
+            const int64_t off = r * H + static_cast<int64_t>(v) * kVec;
+            float w[8], o[8];
+            unpack8(ld_param(a.p0 + static_cast<int64_t>(v) * kVec), w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if constexpr (OP == 3) {
+                    const float xh = (x[k][e] - mu) * rs;
+                    o[e] = rs * (dy[k][e] * w[e] - st.x - xh * st.y);
+                    acc0[k][e] = fmaf(dy[k][e], xh, acc0[k][e]);
+                    acc1[k][e] += dy[k][e];
+                } else {
+                    o[e] = rs * dy[k][e] * w[e] - x[k][e] * st.y;
+                    acc0[k][e] = fmaf(dy[k][e] * x[k][e], rs, acc0[k][e]);
+                }
+            }
+            if (OP == 4 && a.add) {  // fused-add backward: + the residual-stream gradient
+                float d[8];
+                unpack8(ld_stream(a.add + off), d);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] += d[e];
+            }
+            st_stream(a.out0 + off, pack8(o));
+        }
+    }
+    float* wp = a.ws + static_cast<int64_t>(blockIdx.y) * NP * H;
+#pragma unroll
+    for (int k = 0; k < kSpV; ++k) {
+        const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+        if (v >= NV) continue;
+        float4* q0 = reinterpret_cast<float4*>(wp + static_cast<int64_t>(v) * kVec);
+        q0[0] = make_float4(acc0[k][0], acc0[k][1], acc0[k][2], acc0[k][3]);
+        q0[1] = make_float4(acc0[k][4], acc0[k][5], acc0[k][6], acc0[k][7]);
+        if constexpr (NP == 2) {
+            float4* q1 = reinterpret_cast<float4*>(wp + H + static_cast<int64_t>(v) * kVec);
+            q1[0] = make_float4(acc1[k][0], acc1[k][1], acc1[k][2], acc1[k][3]);
+            q1[1] = make_float4(acc1[k][4], acc1[k][5], acc1[k][6], acc1[k][7]);
+        }
+    }
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel k, dim3 grid, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kSpT);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+size_t align16(size_t b) { return (b + 15) / 16 * 16; }
+
+// Workspace layout: [column partials (backward)] [part rows x nc x 2] [stat rows x 2].
+struct SplitLayout {
+    size_t cols, part, stat, total;
+};
+
+SplitLayout split_layout(int op, int64_t rows, int64_t hidden, int sms) {
+    int nc = 0, rb = 0;
+    split_shape(op, rows, hidden, sms, &nc, &rb);
+    const bool bwd = op == 3 || op == 4;
+    SplitLayout l{};
+    l.cols = bwd ? align16(static_cast<size_t>(rb) * (op == 3 ? 2 : 1) * hidden * sizeof(float)) : 0;
+    l.part = align16(static_cast<size_t>(rows) * nc * 2 * sizeof(float));
+    l.stat = align16(static_cast<size_t>(rows) * 2 * sizeof(float));
+    l.total = l.cols + l.part + l.stat;
+    return l;
+}
+
+template <int OP>
+cudaError_t fwd_t(const DynArgs& a, char* ws, int sms, cudaStream_t st) {
+    int nc, rb;
+    split_shape(OP, a.rows, a.hidden, sms, &nc, &rb);
+    const SplitLayout l = split_layout(OP, a.rows, a.hidden, sms);
+    float* part = reinterpret_cast<float*>(ws + l.cols);
+    float2* stat = reinterpret_cast<float2*>(ws + l.cols + l.part);
+    const unsigned gy = static_cast<unsigned>(a.rows < kSpMaxGridY ? a.rows : kSpMaxGridY);
+    const unsigned gr = static_cast<unsigned>(a.rows < 0x7FFFFFFF ? a.rows : 0x7FFFFFFF);
+    if (cudaError_t e = launch_pdl(split_stats<OP>, dim3(nc, gy), st, a, part, nc)) return e;
+    if (cudaError_t e = launch_pdl(split_merge_fwd<OP>, dim3(gr), st, a,
+                                   static_cast<const float*>(part), stat, nc))
+        return e;
+    return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float2*>(stat));
+}
+
+template <int OP>
+cudaError_t bwd_t(DynArgs a, char* ws, int sms, cudaStream_t st) {
+    int nc, rb;
+    split_shape(OP, a.rows, a.hidden, sms, &nc, &rb);
+    const SplitLayout l = split_layout(OP, a.rows, a.hidden, sms);
+    a.ws = reinterpret_cast<float*>(ws);
+    float* part = reinterpret_cast<float*>(ws + l.cols);
+    float2* stat = reinterpret_cast<float2*>(ws + l.cols + l.part);
+    const unsigned gy = static_cast<unsigned>(a.rows < kSpMaxGridY ? a.rows : kSpMaxGridY);
+    const unsigned gr = static_cast<unsigned>(a.rows < 0x7FFFFFFF ? a.rows : 0x7FFFFFFF);
+    if (cudaError_t e = launch_pdl(split_stats_bwd<OP>, dim3(nc, gy), st, a, part, nc)) return e;
+    if (cudaError_t e = launch_pdl(split_merge_bwd<OP>, dim3(gr), st, a,
+                                   static_cast<const float*>(part), stat, nc))
+        return e;
+    return launch_pdl(split_apply_bwd<OP>, dim3(nc, rb), st, a, static_cast<const float2*>(stat));
+}
+
+}  // namespace
+
+bool split_shape(int op, int64_t rows, int64_t hidden, int sms, int* nchunks, int* rblocks) {
+    if (hidden < kVec || hidden % kVec != 0 || hidden > kSplitMaxHidden) return false;
+    const int64_t nc = (hidden + kSpChunk - 1) / kSpChunk;
+    int64_t rb = 0;
+    if (op == 3 || op == 4) {
+        // about two CTAs per SM over (chunk, row block); every row block
+        // adds a column-partial slot of planes x hidden fp32, so no more
+        // blocks than that
+        rb = (2LL * sms + nc - 1) / nc;
+        if (rb > rows) rb = rows;
+        if (rb > kSpMaxGridY) rb = kSpMaxGridY;
+        if (rb < 1) rb = 1;
+    }
+    *nchunks = static_cast<int>(nc);
+    *rblocks = static_cast<int>(rb);
+    return true;
+}
+
+size_t split_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms) {
+    if (rows <= 0 || hidden < kVec || hidden % kVec != 0 || hidden > kSplitMaxHidden) return 0;
+    return split_layout(op, rows, hidden, sms).total;
+}
+
+// a.out0 / out1 / in0 / in1 / p0 / p1 / add / mean / rstd / rows / hidden /
+// eps as for the other families; `workspace` holds split_workspace_bytes.
+cudaError_t launch_split(int op, const DynArgs& a, void* workspace, int sms, cudaStream_t st) {
+    char* ws = static_cast<char*>(workspace);
+    switch (op) {
+        case 0: return fwd_t<0>(a, ws, sms, st);
+        case 1: return fwd_t<1>(a, ws, sms, st);
+        case 2: return fwd_t<2>(a, ws, sms, st);
+        case 3: return bwd_t<3>(a, ws, sms, st);
+        case 4: return bwd_t<4>(a, ws, sms, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace nf

@@ -103,6 +103,17 @@ bool long_shape(int op, int64_t hidden, int* ctas, int* threads, int* slice);
 int64_t long_max_hidden(int op);
 cudaError_t launch_long(int op, const DynArgs& a, int grid, cudaStream_t st);
 
+// Split rows (grid-parallel inner normalization across any number of CTAs):
+// chunks of 8192 elements, partial statistics through the workspace.
+constexpr int64_t kSplitMaxHidden = 1LL << 26;
+bool split_shape(int op, int64_t rows, int64_t hidden, int sms, int* nchunks, int* rblocks);
+size_t split_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms);
+cudaError_t launch_split(int op, const DynArgs& a, void* workspace, int sms, cudaStream_t st);
+
+// Workspace bytes the plan `pl` of (op, rows, hidden) needs on a device of
+// `sms` SMs (0 for forward plans that need none).
+size_t plan_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms, int path, int partials);
+
 // Outer (per-column) normalization: row stripes per direction, workspace
 // bytes covering both directions, and the launch sequences.
 int outer_stripes(int64_t rows, int64_t hidden, int sms, bool bwd);

@@ -22,6 +22,7 @@
 #include <atomic>
 
 #include "../../include/nf.h"
+#include "launch.h"
 
 namespace nf {
 namespace {
@@ -63,7 +64,12 @@ nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const 
     // fixed area are refused up front, before anything is launched.
     nf_plan pl;
     if (nf_status st = nf_plan_query(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
-    const size_t need = static_cast<size_t>(pl.partials) * 2 * static_cast<size_t>(hidden) * sizeof(float);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return NF_ERR_CUDA;
+    const size_t need = nf::plan_workspace_bytes(NF_OP_LAYERNORM_BWD, rows, hidden, sms, pl.path,
+                                                 pl.partials);
     if (need > nf::kNoAllocScratchBytes) return NF_ERR_WORKSPACE_TOO_SMALL;
     void* scratch = nullptr;
     if (nf_status st = nf::scratch_address(&scratch)) return st;

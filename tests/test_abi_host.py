@@ -63,7 +63,7 @@ def test_status_strings_and_version():
 
 # ---------------------------------------------------------------- validation
 
-@pytest.mark.parametrize("hidden", [0, 1, 4, 12, 1002, 4095, 262152, 1 << 20, -4096])
+@pytest.mark.parametrize("hidden", [0, 1, 4, 12, 1002, 4095, (1 << 26) + 8, 1 << 27, -4096])
 def test_unsupported_hidden(hidden):
     assert nf.nf_fused_add_rmsnorm(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
     assert nf.nf_rmsnorm_fwd(A, B, C, 4, hidden, 1e-6, None) == nf.NF_ERR_UNSUPPORTED_HIDDEN
@@ -73,16 +73,18 @@ def test_unsupported_hidden(hidden):
     assert nf.nf_layernorm_bwd_workspace_size(4, hidden) == 0
 
 
-def test_backward_hidden_limit():
-    # backward rows go up to 131072 (cluster path beyond 16384); forward to 262144
+def test_family_hidden_limits():
+    # runtime hidden up to 32768 / 16384, cluster up to 262144 / 131072, split beyond
     for h in (131080, 262144):
-        assert nf.nf_layernorm_bwd(A, B, C, D, A, B, C, D, 4, h, A, 1 << 30, None) == \
-            nf.NF_ERR_UNSUPPORTED_HIDDEN
-        assert nf.nf_rmsnorm_bwd(A, B, C, D, A, 4, h, 1e-6, B, 1 << 30, None) == \
-            nf.NF_ERR_UNSUPPORTED_HIDDEN
+        assert nf.nf_plan_compute("layernorm_bwd", 4, h, 152)[1]["path"] == "split"
+        assert nf.nf_plan_compute("rmsnorm_bwd", 4, h, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262144, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262144, 152, "cluster")[1]["path"] == "cluster"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262152, 152, "cluster")[0] == \
+        nf.NF_ERR_UNSUPPORTED_PATH
     assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32768, 152)[1]["path"] == "dynamic"
-    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32776, 152)[1]["path"] == "cluster"
-    assert nf.nf_plan_compute("layernorm_bwd", 4, 16392, 152)[1]["path"] == "cluster"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32776, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("layernorm_bwd", 4, 16392, 152)[1]["path"] == "split"
 
 
 @pytest.mark.parametrize("hidden", [32776, 40000, 65536, 131072, 200008, 262144])
@@ -90,10 +92,12 @@ def test_long_row_plans(hidden):
     for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
         bwd = op.endswith("_bwd")
         if bwd and hidden > nf.LONG_MAX_HIDDEN_BWD:
-            assert nf.nf_plan_compute(op, 16, hidden, 152)[0] == nf.NF_ERR_UNSUPPORTED_HIDDEN
+            assert nf.nf_plan_compute(op, 16, hidden, 152)[1]["path"] == "split"
             continue
+        # automatic: the split family; forced: the cluster kernels
+        assert nf.nf_plan_compute(op, 7, hidden, 152)[1]["path"] == "split"
         for rows in (1, 7, 5000):
-            st, p = nf.nf_plan_compute(op, rows, hidden, 152)
+            st, p = nf.nf_plan_compute(op, rows, hidden, 152, "cluster")
             assert st == nf.NF_OK and p["path"] == "cluster", (op, hidden, p)
             c, t = p["cluster"], p["block"]
             assert c in (2, 4, 8) and t % 32 == 0 and t <= (512 if bwd else 1024)
@@ -124,8 +128,8 @@ def test_dynamic_plans(hidden):
     for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
         bwd = op.endswith("_bwd")
         if bwd and hidden > nf.DYN_MAX_HIDDEN_BWD:
-            # beyond the runtime-hidden backward limit the long-row cluster path takes over
-            assert nf.nf_plan_compute(op, 16, hidden, 152)[1]["path"] == "cluster"
+            # beyond the runtime-hidden backward limit the split family takes over
+            assert nf.nf_plan_compute(op, 16, hidden, 152)[1]["path"] == "split"
             continue
         for rows in (1, 77, 16384):
             st, p = nf.nf_plan_compute(op, rows, hidden, 152)
@@ -240,7 +244,7 @@ def test_rmsnorm_bwd_validation():
 
 def test_set_path_rejects_unknown():
     assert nf.nf_set_path(17) == nf.NF_ERR_INVALID_ARG
-    assert nf.nf_set_path(5) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(6) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(-1) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
 
@@ -376,3 +380,41 @@ def test_fused_add_rmsnorm_bwd_validation():
     # dres is optional but, when given, 16-byte aligned like the activations
     assert f(A, B + 0x1000000, C, D + 8, D + 0x1000000, A + 0x2000000, 4, 4096, 1e-6,
              B + 0x2000000, ws, None) == nf.NF_ERR_MISALIGNED
+
+
+OPS5 = ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd")
+
+
+@pytest.mark.parametrize("hidden", [8, 4096, 270336, 1 << 20, 1000008, 1 << 26])
+def test_split_plans(hidden):
+    # a row over any number of CTAs: 8192-element chunks, one CTA per (chunk, row)
+    nc = -(-hidden // 8192)
+    for op in OPS5:
+        bwd = op.endswith("_bwd")
+        for rows in (1, 3, 70000):
+            st, p = nf.nf_plan_compute(op, rows, hidden, 152, "split")
+            assert st == nf.NF_OK and p["path"] == "split" and p["block"] == 256
+            assert p["cluster"] == 1 and p["rows_per_cta"] == 1
+            if bwd:
+                rb = max(1, min(rows, -(-2 * 152 // nc), 65535))
+                assert p["launches"] == 4 and p["partials"] == rb and p["grid"] == nc * rb
+            else:
+                assert p["launches"] == 3 and p["grid"] == nc * min(rows, 65535)
+                assert p["partials"] == 0
+        # beyond the cluster limits the split family is the automatic choice
+        limit = nf.LONG_MAX_HIDDEN_BWD if bwd else nf.LONG_MAX_HIDDEN_FWD
+        if hidden > limit:
+            assert nf.nf_plan_compute(op, 2, hidden, 152)[1]["path"] == "split"
+            for path in ("reg", "bulk", "dynamic", "cluster"):
+                assert nf.nf_plan_compute(op, 2, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
+
+
+def test_split_path_settable_and_workspace_queries_without_gpu():
+    assert nf.nf_set_path(nf.NF_PATH_SPLIT) == nf.NF_OK
+    assert nf.nf_set_path(nf.NF_PATH_SPLIT + 1) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
+    # no device: the queries return 0 rather than failing
+    if not HAVE_GPU:
+        assert nf.nf_workspace_size(nf.NF_OP_RMSNORM_FWD, 4, 1 << 20) == 0
+    assert nf.nf_workspace_size(99, 4, 4096) == 0
+    assert nf.nf_workspace_size(nf.NF_OP_RMSNORM_FWD, 4, 4100) == 0

@@ -37,8 +37,7 @@ def test_fused_bwd(path, hidden, with_dres):
     rows = 3 if path == "cluster" else 300
     s, w, dy, dres = _inputs(rows, hidden, seed=hidden + rows)
     ds_ref, dw_ref = oracle.fused_add_rmsnorm_bwd(dy, dres if with_dres else None, s, w, 1e-6)
-    auto = path == "cluster" and hidden > nf.DYN_MAX_HIDDEN_BWD
-    with nf.forced_path("auto" if auto else path):
+    with nf.forced_path(path):
         assert nf.nf_plan_query("rmsnorm_bwd", rows, hidden)["path"] == path
         dx, dw = nf.fused_add_rmsnorm_bwd(dy.cuda(), s.cuda(), w.cuda(),
                                           dres.cuda() if with_dres else None, 1e-6)

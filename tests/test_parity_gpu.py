@@ -273,8 +273,11 @@ def test_layernorm_bwd_workspace_too_small():
     x, dy, g = _ln_bwd_case(rows, hidden)
     mean, rstd = _saved_stats(x)
     need = nf.nf_layernorm_bwd_workspace_size(rows, hidden)
-    assert need > 0
-    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    # the query covers every family; the call needs its own plan's partials
+    plan = nf.nf_plan_query("layernorm_bwd", rows, hidden)
+    need_run = plan["partials"] * 2 * hidden * 4
+    assert need >= need_run > 0
+    ws = torch.empty(need_run - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(nf.NFError) as e:
         nf.layernorm_bwd(dy.cuda(), x.cuda(), mean.cuda(), rstd.cuda(), g.cuda(), workspace=ws)
     assert e.value.status == nf.NF_ERR_WORKSPACE_TOO_SMALL
@@ -356,7 +359,9 @@ def test_rmsnorm_bwd_zero_rows_and_small_workspace():
     assert torch.count_nonzero(dw) == 0
     x, dy, w = workloads.rms_bwd_inputs(64, hidden)
     need = nf.nf_rmsnorm_bwd_workspace_size(64, hidden)
-    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    need_run = nf.nf_plan_query("rmsnorm_bwd", 64, hidden)["partials"] * hidden * 4
+    assert need >= need_run > 0
+    ws = torch.empty(need_run - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(nf.NFError) as e:
         nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-6, workspace=ws)
     assert e.value.status == nf.NF_ERR_WORKSPACE_TOO_SMALL

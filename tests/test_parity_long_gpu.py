@@ -1,6 +1,6 @@
-"""GPU parity of the grid-parallel (cluster, runtime hidden) kernels for long
+"""GPU parity of the grid-parallel cluster kernels (runtime hidden) for long
 rows against the fp64 oracle: forward hidden up to 262144, backward up to
-131072, plus shorter sizes forced onto the cluster family."""
+131072, plus shorter sizes, all forced onto the cluster family."""
 import numpy as np
 import pytest
 import torch
@@ -27,9 +27,9 @@ def built():
 
 
 def _path(hidden, bwd):
-    # long rows take the cluster family on their own; shorter ones are forced
-    limit = nf.DYN_MAX_HIDDEN_BWD if bwd else nf.DYN_MAX_HIDDEN_FWD
-    return "auto" if hidden > limit else "cluster"
+    # the automatic choice for long rows is the split family (measured
+    # faster); the cluster kernels are forced here
+    return "cluster"
 
 
 @pytest.mark.parametrize("hidden", FWD_LONG + FORCED[:2])
