@@ -569,13 +569,29 @@ def run_gpu(args):
                     ox.copy_(x, non_blocking=True)
                     orr.copy_(r, non_blocking=True)
 
-        def timed(nsteps):
+        # the host link's capacity for the same bytes: every host->device copy
+        # on one stream while every device->host copy runs on another (from a
+        # separate device buffer), no kernel and no dependency between them
+        link_src = torch.empty(max(t.numel() for t in (w_[2] for w_ in work)), dtype=torch.bfloat16,
+                               device=dev)
+
+        def link_step():
+            with torch.cuda.stream(streams[0]):
+                for (hx, hr, ox, orr, x, r, w) in work:
+                    x.copy_(hx, non_blocking=True)
+                    r.copy_(hr, non_blocking=True)
+            with torch.cuda.stream(streams[1]):
+                for (hx, hr, ox, orr, x, r, w) in work:
+                    ox.copy_(link_src[:ox.numel()].view_as(ox), non_blocking=True)
+                    orr.copy_(link_src[:orr.numel()].view_as(orr), non_blocking=True)
+
+        def timed(nsteps, step=e2e_step):
             a, b = _ev(), _ev()
             a.record(stream)
             for s in streams:
                 s.wait_event(a)
             for _ in range(nsteps):
-                e2e_step()
+                step()
             for s in streams:
                 ev = _ev()
                 ev.record(s)
@@ -594,10 +610,18 @@ def run_gpu(args):
         # check once that the round trip really returned the device results
         torch.cuda.synchronize()
         assert torch.equal(outs[-1][0][-1], sets[-1][0][-1].cpu())
-        e2e = {"value": round(whole_job_gbs(world, step_bytes, e2e_steps, e_ms), 2), "unit": UNIT,
+        c_ms = timed(e2e_steps, step=link_step)
+        c_ms = max_over_ranks(c_ms, dist, dev)
+        e2e_value = whole_job_gbs(world, step_bytes, e2e_steps, e_ms)
+        ceiling = whole_job_gbs(world, step_bytes, e2e_steps, c_ms)
+        e2e = {"value": round(e2e_value, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": round(e_ms / e2e_steps, 3),
-               "pipeline": f"{E2E_CHUNKS} row chunks per hidden size over {E2E_STREAMS} streams"}
+               "pipeline": f"{E2E_CHUNKS} row chunks per hidden size over {E2E_STREAMS} streams",
+               "link_gbs": round(ceiling, 2),
+               "frac_of_link": round(e2e_value / ceiling, 4) if ceiling > 0 else None,
+               "link": "the same host<->device bytes copied with no kernel, the two directions "
+                       "on two streams at once"}
         del hosts, outs, work
 
     ops = None

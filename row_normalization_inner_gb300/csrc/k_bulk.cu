@@ -35,6 +35,7 @@
 // leaves.  Either records NF_ERR_TIMEOUT in the device status word.
 #include "common.cuh"
 #include "pairs.cuh"
+#include "pdl.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -172,6 +173,9 @@ norm_bulk_kernel(BulkArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::BAR_OFF);
     uint64_t* empty = full + G::S;
+    // launched as a programmatic dependent: nothing is touched before the
+    // previous grid in the stream has finished
+    grid_dep_wait();
 
     const int64_t nct = gridDim.x;
     const int64_t r0 = a.rows * blockIdx.x / nct;
@@ -553,7 +557,8 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             attr_set[1] = true;
         }
-        norm_bulk_kernel<OP, H, true><<<grid, G::THREADS, G::SMEM, st>>>(a);
+        return launch_with_pdl(norm_bulk_kernel<OP, H, true>, dim3(grid), dim3(G::THREADS), G::SMEM,
+                               st, a);
     } else {
         if (!attr_set[0]) {
             cudaError_t e = cudaFuncSetAttribute(norm_bulk_kernel<OP, H, false>,
@@ -561,7 +566,8 @@ cudaError_t launch_bulk_t(const BulkArgs& a, int grid, cudaStream_t st) {
             if (e != cudaSuccess) return e;
             attr_set[0] = true;
         }
-        norm_bulk_kernel<OP, H, false><<<grid, G::THREADS, G::SMEM, st>>>(a);
+        return launch_with_pdl(norm_bulk_kernel<OP, H, false>, dim3(grid), dim3(G::THREADS), G::SMEM,
+                               st, a);
     }
     return cudaGetLastError();
 }

@@ -16,6 +16,7 @@
 // Stage 2 sums the nslots partials of every column in slot order, so dgamma
 // and dbeta are bit-identical from run to run.
 #include "common.cuh"
+#include "pdl.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -38,6 +39,7 @@ layernorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, cons
                   const uint16_t* __restrict__ gamma, int64_t rows) {
     using G = BGeo<H>;
     __shared__ float red[2][G::RPC * G::W * 2];
+    grid_dep_wait();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     const int64_t nslots = static_cast<int64_t>(gridDim.x) * G::RPC;
     const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::RPC + group;
@@ -132,6 +134,7 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
                 const uint16_t* dres, const uint16_t* __restrict__ w, int64_t rows, float eps) {
     using G = BGeo<H>;
     __shared__ float red[2][G::RPC * G::W * 2];
+    grid_dep_wait();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     const int64_t nslots = static_cast<int64_t>(gridDim.x) * G::RPC;
     const int64_t slot = static_cast<int64_t>(blockIdx.x) * G::RPC + group;
@@ -281,10 +284,10 @@ cudaError_t launch_ln_bwd_reg(int64_t hidden, void* dx, float* ws, const void* d
                               const float* mean, const float* rstd, const void* gamma,
                               int64_t rows, int grid, cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
-        layernorm_bwd_reg<H><<<grid, BGeo<H>::TPR * BGeo<H>::RPC, 0, st>>>(
-            static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
-            static_cast<const uint16_t*>(x), mean, rstd, static_cast<const uint16_t*>(gamma), rows);
-        return cudaGetLastError();
+        return launch_with_pdl(layernorm_bwd_reg<H>, dim3(grid), dim3(BGeo<H>::TPR * BGeo<H>::RPC), 0,
+                               st, static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
+                               static_cast<const uint16_t*>(x), mean, rstd,
+                               static_cast<const uint16_t*>(gamma), rows);
     })
 }
 
@@ -327,11 +330,10 @@ cudaError_t launch_rms_bwd_reg(int64_t hidden, void* dx, float* ws, const void* 
                                const void* dres, const void* w, int64_t rows, float eps, int grid,
                                cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
-        rmsnorm_bwd_reg<H><<<grid, BGeo<H>::TPR * BGeo<H>::RPC, 0, st>>>(
-            static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
-            static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dres),
-            static_cast<const uint16_t*>(w), rows, eps);
-        return cudaGetLastError();
+        return launch_with_pdl(rmsnorm_bwd_reg<H>, dim3(grid), dim3(BGeo<H>::TPR * BGeo<H>::RPC), 0,
+                               st, static_cast<uint16_t*>(dx), ws, static_cast<const uint16_t*>(dy),
+                               static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(dres),
+                               static_cast<const uint16_t*>(w), rows, eps);
     })
 }
 

@@ -17,6 +17,7 @@
 // in the static-size backward kernels, and the same fixed-order column
 // reduction finishes dgamma/dbeta (or dw).
 #include "common.cuh"
+#include "pdl.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -52,6 +53,8 @@ __device__ __forceinline__ void cta_sum(float (&v)[N], float* red) {
 template <int OP, int MAXV, int MAXT>
 __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
     __shared__ float red[2][kDynMaxWarps];
+    grid_dep_wait();
+    grid_dep_release();
     const int H = a.hidden;
     const int NV = H / kVec;
     const int T = blockDim.x, t = threadIdx.x;
@@ -136,6 +139,7 @@ template <int OP, int MAXV>
 __global__ void __launch_bounds__(kDynBwdMaxT) norm_dyn_bwd(DynArgs a) {
     constexpr int NP = OP == 3 ? 2 : 1;  // partial planes
     __shared__ float red[2][kDynMaxWarps * 2];
+    grid_dep_wait();
     const int H = a.hidden;
     const int NV = H / kVec;
     const int T = blockDim.x, t = threadIdx.x;
@@ -274,24 +278,21 @@ cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st) {
     int threads;
     if (!dyn_shape(op, a.hidden, &threads)) return cudaErrorInvalidValue;
     const bool big = threads > 256;
+    const dim3 g(grid), b(threads);
     switch (op) {
         case 0:
-            if (big) norm_dyn_fwd<0, kDynMaxV, 1024><<<grid, threads, 0, st>>>(a);
-            else norm_dyn_fwd<0, kDynMaxV, 256><<<grid, threads, 0, st>>>(a);
-            break;
+            return big ? launch_with_pdl(norm_dyn_fwd<0, kDynMaxV, 1024>, g, b, 0, st, a)
+                       : launch_with_pdl(norm_dyn_fwd<0, kDynMaxV, 256>, g, b, 0, st, a);
         case 1:
-            if (big) norm_dyn_fwd<1, kDynMaxV, 1024><<<grid, threads, 0, st>>>(a);
-            else norm_dyn_fwd<1, kDynMaxV, 256><<<grid, threads, 0, st>>>(a);
-            break;
+            return big ? launch_with_pdl(norm_dyn_fwd<1, kDynMaxV, 1024>, g, b, 0, st, a)
+                       : launch_with_pdl(norm_dyn_fwd<1, kDynMaxV, 256>, g, b, 0, st, a);
         case 2:
-            if (big) norm_dyn_fwd<2, kDynMaxV, 1024><<<grid, threads, 0, st>>>(a);
-            else norm_dyn_fwd<2, kDynMaxV, 256><<<grid, threads, 0, st>>>(a);
-            break;
-        case 3: norm_dyn_bwd<3, kDynMaxV><<<grid, threads, 0, st>>>(a); break;
-        case 4: norm_dyn_bwd<4, kDynMaxV><<<grid, threads, 0, st>>>(a); break;
+            return big ? launch_with_pdl(norm_dyn_fwd<2, kDynMaxV, 1024>, g, b, 0, st, a)
+                       : launch_with_pdl(norm_dyn_fwd<2, kDynMaxV, 256>, g, b, 0, st, a);
+        case 3: return launch_with_pdl(norm_dyn_bwd<3, kDynMaxV>, g, b, 0, st, a);
+        case 4: return launch_with_pdl(norm_dyn_bwd<4, kDynMaxV>, g, b, 0, st, a);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace nf

@@ -13,6 +13,8 @@
 // change): sum of squares for RMSNorm; for LayerNorm the sum, then the
 // centered sum of squares over the resident values (two passes, no reload).
 #include "common.cuh"
+#include "pairs.cuh"
+#include "pdl.cuh"
 #include "launch.h"
 
 namespace nf {
@@ -37,6 +39,8 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
                       const uint16_t* __restrict__ w, int64_t rows, float eps) {
     using G = Geo<H>;
     __shared__ float red[G::RPC * G::W];
+    grid_dep_wait();
+    grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
@@ -92,37 +96,42 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
                 int64_t rows, float eps) {
     using G = Geo<H>;
     __shared__ float red[G::RPC * G::W];
+    grid_dep_wait();
+    grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
         const bool active = row < rows;
-        // the row stays packed (bf16) in registers and is widened per pass
+        // the row stays packed (bf16) in registers and is widened per pass;
+        // the arithmetic runs on fp32 pairs
         uint4 xv[G::VPT];
-        float ss[1] = {0.f};
+        float2 s2 = make_float2(0.f, 0.f);
         if (active) {
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float f[8];
-                unpack8(xv[k], f);
+                float2 f[4];
+                unpack8x2(xv[k], f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss[0] += f[e] * f[e];
+                for (int q = 0; q < 4; ++q) s2 = __ffma2_rn(f[q], f[q], s2);
             }
         }
+        float ss[1] = {s2.x + s2.y};
         group_sum<G::TPR, 1>(ss, red, group, t);
         if (active) {
             const float rstd = rsqrtf(ss[0] * (1.0f / H) + eps);
+            const float2 rstd2 = make_float2(rstd, rstd);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float f[8], wf[8], o[8];
-                unpack8(xv[k], f);
-                unpack8(ld_param(w + v * kVec), wf);
+                float2 f[4], wf[4], o[4];
+                unpack8x2(xv[k], f);
+                unpack8x2(ld_param(w + v * kVec), wf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = f[e] * rstd * wf[e];
-                st_stream(y + row * H + v * kVec, pack8(o));
+                for (int q = 0; q < 4; ++q) o[q] = __fmul2_rn(__fmul2_rn(f[q], rstd2), wf[q]);
+                st_stream(y + row * H + v * kVec, pack8x2(o));
             }
         }
         if constexpr (G::W > 1) __syncthreads();
@@ -139,6 +148,8 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     using G = Geo<H>;
     __shared__ float red1[G::RPC * G::W];
     __shared__ float red2[G::RPC * G::W];
+    grid_dep_wait();
+    grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
@@ -147,65 +158,69 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
         // Small rows are instruction-bound: widen the row once and center it
         // in place.  Larger rows are occupancy-bound: keep it packed (half
         // the registers) and widen it on each pass.  Either way
-        // y = fma(x - mean, rstd * gamma, beta).
+        // y = fma(x - mean, rstd * gamma, beta), on fp32 pairs.
         constexpr bool kWide = H <= 1024;
-        float f[kWide ? G::VPT : 1][8];
+        float2 f[kWide ? G::VPT : 1][4];
         uint4 xv[G::VPT];
-        float acc[1] = {0.f};
+        float2 s1 = make_float2(0.f, 0.f);
         if (active) {
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float tmp[8];
-                unpack8(xv[k], tmp);
+                float2 tmp[4];
+                unpack8x2(xv[k], tmp);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if constexpr (kWide) f[k][e] = tmp[e];
-                    acc[0] += tmp[e];
+                for (int q = 0; q < 4; ++q) {
+                    if constexpr (kWide) f[k][q] = tmp[q];
+                    s1 = __fadd2_rn(s1, tmp[q]);
                 }
             }
         }
+        float acc[1] = {s1.x + s1.y};
         group_sum<G::TPR, 1>(acc, red1, group, t);
         const float mean = acc[0] * (1.0f / H);
-        float sq[1] = {0.f};
+        const float2 nmean2 = make_float2(-mean, -mean);
+        float2 s2 = make_float2(0.f, 0.f);
         if (active) {
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
-                float tmp[8];
-                if constexpr (!kWide) unpack8(xv[k], tmp);
+                float2 tmp[4];
+                if constexpr (!kWide) unpack8x2(xv[k], tmp);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int q = 0; q < 4; ++q) {
                     if constexpr (kWide) {
-                        f[k][e] -= mean;
-                        sq[0] = fmaf(f[k][e], f[k][e], sq[0]);
+                        f[k][q] = __fadd2_rn(f[k][q], nmean2);
+                        s2 = __ffma2_rn(f[k][q], f[k][q], s2);
                     } else {
-                        const float d = tmp[e] - mean;
-                        sq[0] = fmaf(d, d, sq[0]);
+                        const float2 d = __fadd2_rn(tmp[q], nmean2);
+                        s2 = __ffma2_rn(d, d, s2);
                     }
                 }
             }
         }
+        float sq[1] = {s2.x + s2.y};
         group_sum<G::TPR, 1>(sq, red2, group, t);
         if (active) {
             const float rstd = rsqrtf(sq[0] * (1.0f / H) + eps);
+            const float2 rstd2 = make_float2(rstd, rstd);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
-                float gf[8], bf[8], o[8], xm[8];
+                float2 gf[4], bf[4], o[4], xm[4];
                 if constexpr (kWide) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xm[e] = f[k][e];
+                    for (int q = 0; q < 4; ++q) xm[q] = f[k][q];
                 } else {
-                    unpack8(xv[k], xm);
+                    unpack8x2(xv[k], xm);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xm[e] -= mean;
+                    for (int q = 0; q < 4; ++q) xm[q] = __fadd2_rn(xm[q], nmean2);
                 }
-                unpack8(ld_param(gamma + v * kVec), gf);
-                unpack8(ld_param(beta + v * kVec), bf);
+                unpack8x2(ld_param(gamma + v * kVec), gf);
+                unpack8x2(ld_param(beta + v * kVec), bf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = fmaf(xm[e], rstd * gf[e], bf[e]);
-                st_stream(y + row * H + v * kVec, pack8(o));
+                for (int q = 0; q < 4; ++q) o[q] = __ffma2_rn(xm[q], __fmul2_rn(rstd2, gf[q]), bf[q]);
+                st_stream(y + row * H + v * kVec, pack8x2(o));
             }
             if (t == 0) {
                 if (mean_out) mean_out[row] = mean;
@@ -221,20 +236,19 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
                              float eps, int grid, cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
-        fused_add_rmsnorm_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
-            static_cast<uint16_t*>(x), static_cast<uint16_t*>(res),
-            static_cast<const uint16_t*>(w), rows, eps);
-        return cudaGetLastError();
+        return launch_with_pdl(fused_add_rmsnorm_reg<H>, dim3(grid),
+                               dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st, static_cast<uint16_t*>(x),
+                               static_cast<uint16_t*>(res), static_cast<const uint16_t*>(w), rows,
+                               eps);
     })
 }
 
 cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
                            float eps, int grid, cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
-        rmsnorm_fwd_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
-            static_cast<uint16_t*>(y), static_cast<const uint16_t*>(x),
-            static_cast<const uint16_t*>(w), rows, eps);
-        return cudaGetLastError();
+        return launch_with_pdl(rmsnorm_fwd_reg<H>, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0,
+                               st, static_cast<uint16_t*>(y), static_cast<const uint16_t*>(x),
+                               static_cast<const uint16_t*>(w), rows, eps);
     })
 }
 
@@ -242,10 +256,10 @@ cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd,
                               const void* gamma, const void* beta, int64_t rows, float eps,
                               int grid, cudaStream_t st) {
     NF_HIDDEN_SWITCH(hidden, {
-        layernorm_fwd_reg<H><<<grid, Geo<H>::TPR * Geo<H>::RPC, 0, st>>>(
-            static_cast<uint16_t*>(y), mean, rstd, static_cast<const uint16_t*>(x),
-            static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta), rows, eps);
-        return cudaGetLastError();
+        return launch_with_pdl(layernorm_fwd_reg<H>, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0,
+                               st, static_cast<uint16_t*>(y), mean, rstd,
+                               static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
+                               static_cast<const uint16_t*>(beta), rows, eps);
     })
 }
 
