@@ -212,29 +212,32 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
 }
 
 // out0[j] = sum_{slot} ws[slot][0][j] and, with two planes,
-// out1[j] = sum_{slot} ws[slot][1][j], in a fixed order: thread row ty sums
-// slots ty, ty+32, ty+64, ... and the 32 row sums are then added in ty
-// order.  A CTA covers 32 columns: 8 column lanes of one float4 each, so a
-// warp reads 4 slots x 128 contiguous bytes.  Many small CTAs keep every SM
-// busy even at hidden 1024 (64 CTAs for two planes).
-constexpr int kColX = 8, kColY = 32;
+// out1[j] = sum_{slot} ws[slot][1][j], in a fixed order: a CTA of 256
+// threads covers X = 256 / Y float4 columns with Y slot lanes each; lane ty
+// sums slots ty, ty + Y, ... and the Y lane sums are then combined by a
+// fixed halving tree.  Y grows with the slot count (each lane reads at most
+// two slots), so the reduction is one or two dependent loads deep and the
+// grid has many CTAs even at hidden 1024.
+constexpr int kColT = 256;
 
-__global__ void __launch_bounds__(kColX * kColY)
+template <int Y>
+__global__ void __launch_bounds__(kColT)
 column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
               float* __restrict__ dbeta, int nslots, int hidden, int planes) {
-    __shared__ float4 part[kColY][kColX];
+    constexpr int X = kColT / Y;
+    __shared__ float4 part[Y][X];
     // Launched as a programmatic dependent of stage 1: wait until stage 1
     // has finished and its partials are visible (a no-op otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int tx = threadIdx.x % kColX, ty = threadIdx.x / kColX;
-    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kColX + tx;  // float4 index in [planes][H]
+    const int tx = threadIdx.x % X, ty = threadIdx.x / X;
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * X + tx;  // float4 index in [planes][H]
     const bool ok = c4 * 4 < planes * static_cast<int64_t>(hidden);
     const int which = ok ? static_cast<int>((c4 * 4) / hidden) : 0;
     const int64_t j = ok ? (c4 * 4) % hidden : 0;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
-#pragma unroll 4
-        for (int p = ty; p < nslots; p += kColY) {
+#pragma unroll 2
+        for (int p = ty; p < nslots; p += Y) {
             const float4 v = __ldcs(reinterpret_cast<const float4*>(
                 ws + (static_cast<int64_t>(p) * planes + which) * hidden + j));
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
@@ -242,15 +245,18 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     }
     part[ty][tx] = s;
     __syncthreads();
-    if (ty == 0 && ok) {
-        float4 tot = part[0][tx];
 #pragma unroll
-        for (int y = 1; y < kColY; ++y) {
-            const float4 v = part[y][tx];
-            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+    for (int stride = Y / 2; stride > 0; stride >>= 1) {
+        if (ty < stride) {
+            const float4 v = part[ty + stride][tx];
+            float4& t = part[ty][tx];
+            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
         }
+        __syncthreads();
+    }
+    if (ty == 0 && ok) {
         float* out = (which == 0 ? dgamma : dbeta) + j;
-        *reinterpret_cast<float4*>(out) = tot;
+        *reinterpret_cast<float4*>(out) = part[0][tx];
     }
 }
 
@@ -298,8 +304,7 @@ cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out
                                         int64_t hidden, int planes, cudaStream_t st) {
     const int64_t cols4 = planes * hidden / 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((cols4 + kColX - 1) / kColX), 1, 1);
-    cfg.blockDim = dim3(kColX * kColY, 1, 1);
+    cfg.blockDim = dim3(kColT, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -312,8 +317,17 @@ cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out
         return cudaLaunchKernelEx(&cfg, column_reduce_narrow, ws, out0, out1, nslots,
                                   static_cast<int>(hidden), planes);
     }
-    return cudaLaunchKernelEx(&cfg, column_reduce, ws, out0, out1, nslots,
-                              static_cast<int>(hidden), planes);
+    // slot lanes per column: enough that each lane reads at most two slots
+    const auto launch = [&](auto kernel, int y) {
+        const int x = kColT / y;
+        cfg.gridDim = dim3(static_cast<unsigned>((cols4 + x - 1) / x), 1, 1);
+        return cudaLaunchKernelEx(&cfg, kernel, ws, out0, out1, nslots, static_cast<int>(hidden),
+                                  planes);
+    };
+    if (nslots <= 64) return launch(column_reduce<32>, 32);
+    if (nslots <= 128) return launch(column_reduce<64>, 64);
+    if (nslots <= 256) return launch(column_reduce<128>, 128);
+    return launch(column_reduce<256>, 256);
 }
 
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
