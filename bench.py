@@ -702,7 +702,7 @@ def run_profile_case(spec: str, reps: int):
     """Run `reps` launches of one operation at one size and exit: the small,
     self-contained command the ncu captures use.  spec = OP:ROWSxHIDDEN with
     OP in fused_add_rmsnorm, rmsnorm_fwd, layernorm_fwd, layernorm_bwd,
-    outer_norm_fwd, outer_norm_bwd."""
+    rmsnorm_bwd, fused_add_rmsnorm_bwd, outer_norm_fwd, outer_norm_bwd."""
     import row_normalization_inner_gb300 as nf
     from row_normalization_inner_gb300 import build as nf_build
     nf_build.build()
@@ -727,6 +727,18 @@ def run_profile_case(spec: str, reps: int):
                          dtype=torch.uint8, device=dev)
         dx = torch.empty_like(x)
         fn = lambda: nf.layernorm_bwd(dy, x, mean, rstd, g, workspace=ws, out=dx)  # noqa: E731
+    elif op == "rmsnorm_bwd":
+        x, dy, w = workloads.rms_bwd_inputs(rows, hidden, device=dev)
+        ws = torch.empty(max(nf.nf_rmsnorm_bwd_workspace_size(rows, hidden), 16),
+                         dtype=torch.uint8, device=dev)
+        dx = torch.empty_like(x)
+        fn = lambda: nf.rmsnorm_bwd(dy, x, w, EPS, workspace=ws, out=dx)  # noqa: E731
+    elif op == "fused_add_rmsnorm_bwd":
+        s_, w, dy, dres = workloads.fused_bwd_inputs(rows, hidden, device=dev)
+        ws = torch.empty(max(nf.nf_rmsnorm_bwd_workspace_size(rows, hidden), 16),
+                         dtype=torch.uint8, device=dev)
+        dx = torch.empty_like(s_)
+        fn = lambda: nf.fused_add_rmsnorm_bwd(dy, s_, w, dres, EPS, workspace=ws, out=dx)  # noqa: E731
     elif op in ("outer_norm_fwd", "outer_norm_bwd"):
         x, dy, g, b = workloads.outer_inputs(rows, hidden, device=dev)
         ws = torch.empty(max(nf.nf_outer_norm_workspace_size(rows, hidden), 16),
@@ -742,7 +754,8 @@ def run_profile_case(spec: str, reps: int):
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
-    plan = "outer" if op.startswith("outer") else nf.nf_plan_query(op, rows, hidden)
+    plan = "outer" if op.startswith("outer") else nf.nf_plan_query(
+        "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op, rows, hidden)
     print(f"profile case {spec}: {reps} call(s), plan {plan}")
     return 0
 
