@@ -650,8 +650,14 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         int sms = 0;
-        if (pl.path == NF_PATH_SPLIT)
+        if (pl.path == NF_PATH_SPLIT) {
             if (nf_status st = device_sm_count(&sms)) return st;
+            if (pl.partials == 1) {  // one row block: no column reduction
+                a.cols0 = dgamma;
+                a.cols1 = dbeta;
+                return from_cuda(launch_split(NF_OP_LAYERNORM_BWD, a, workspace, sms, s));
+            }
+        }
         const cudaError_t e =
             pl.path == NF_PATH_SPLIT     ? launch_split(NF_OP_LAYERNORM_BWD, a, workspace, sms, s)
             : pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_LAYERNORM_BWD, a, pl.grid, s)
@@ -721,8 +727,13 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
         int sms = 0;
-        if (pl.path == NF_PATH_SPLIT)
+        if (pl.path == NF_PATH_SPLIT) {
             if (nf_status st = device_sm_count(&sms)) return st;
+            if (pl.partials == 1) {  // one row block: no column reduction
+                a.cols0 = dw;
+                return from_cuda(launch_split(NF_OP_RMSNORM_BWD, a, workspace, sms, s));
+            }
+        }
         const cudaError_t e =
             pl.path == NF_PATH_SPLIT     ? launch_split(NF_OP_RMSNORM_BWD, a, workspace, sms, s)
             : pl.path == NF_PATH_CLUSTER ? launch_long(NF_OP_RMSNORM_BWD, a, pl.grid, s)

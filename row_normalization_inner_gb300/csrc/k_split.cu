@@ -370,16 +370,19 @@ __global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2*
             st_stream(a.out0 + off, pack8(o));
         }
     }
+    // one row block: the column sums are final and go straight to the outputs
     float* wp = a.ws + static_cast<int64_t>(blockIdx.y) * NP * H;
+    float* w0 = a.cols0 ? a.cols0 : wp;
+    float* w1 = a.cols0 ? a.cols1 : wp + H;
 #pragma unroll
     for (int k = 0; k < kSpV; ++k) {
         const int v = c * kSpVecs + k * kSpT + threadIdx.x;
         if (v >= NV) continue;
-        float4* q0 = reinterpret_cast<float4*>(wp + static_cast<int64_t>(v) * kVec);
+        float4* q0 = reinterpret_cast<float4*>(w0 + static_cast<int64_t>(v) * kVec);
         q0[0] = make_float4(acc0[k][0], acc0[k][1], acc0[k][2], acc0[k][3]);
         q0[1] = make_float4(acc0[k][4], acc0[k][5], acc0[k][6], acc0[k][7]);
         if constexpr (NP == 2) {
-            float4* q1 = reinterpret_cast<float4*>(wp + H + static_cast<int64_t>(v) * kVec);
+            float4* q1 = reinterpret_cast<float4*>(w1 + static_cast<int64_t>(v) * kVec);
             q1[0] = make_float4(acc1[k][0], acc1[k][1], acc1[k][2], acc1[k][3]);
             q1[1] = make_float4(acc1[k][4], acc1[k][5], acc1[k][6], acc1[k][7]);
         }

@@ -88,6 +88,8 @@ struct DynArgs {
     float* mean;             // ln fwd out / ln bwd in
     float* rstd;
     float* ws;               // bwd partials [grid][planes][hidden]
+    float* cols0;            // split bwd with one row block: dgamma / dw written directly
+    float* cols1;            //   and dbeta (the column reduction is then skipped), else null
     int64_t rows;
     int hidden;
     float eps;
