@@ -472,6 +472,9 @@ def ops_suite(nf, peak, stream, l2_bytes):
     for rows, h in ((16384, 1024), (16384, 4096), (65536, 1024), (4096, 8192)):
         entry("outer_norm_fwd", rows, h, EPS)
         entry("outer_norm_bwd", rows, h, EPS)
+    # rows longer than a cluster holds: the split family
+    for op in ("rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
+        entry(op, 4, 1 << 22, EPS)
     return out
 
 
