@@ -281,10 +281,19 @@ norm_bulk_kernel(BulkArgs a) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc_b[k][q] = make_float2(0.f, 0.f);
     }
-    // saved statistics of the group's next row, fetched one row ahead
-    float nmu = 0.f, nrs = 0.f;
-    if constexpr (OP == kLnBwd) {
-        if (gid < n) { nmu = __ldg(a.mean + r0 + gid); nrs = __ldg(a.rstd + r0 + gid); }
+    // saved statistics of the group's next rows, fetched ahead
+    // (a queue kStatAhead rows deep, shifted by one each row: no dynamic
+    // indexing, and the loads have several rows of work to land)
+    constexpr int kStatAhead = OP == kLnBwd ? 4 : 1;
+    float qmu[kStatAhead], qrs[kStatAhead];
+#pragma unroll
+    for (int d = 0; d < kStatAhead; ++d) {
+        qmu[d] = 0.f;
+        qrs[d] = 0.f;
+        if constexpr (OP == kLnBwd) {
+            const int ii = gid + d * G::NG;
+            if (ii < n) { qmu[d] = __ldg(a.mean + r0 + ii); qrs[d] = __ldg(a.rstd + r0 + ii); }
+        }
     }
 
     bool failed = false;
@@ -437,8 +446,16 @@ norm_bulk_kernel(BulkArgs a) {
         } else {  // kLnBwd
             // xhat = x * rstd - mean * rstd (one fma), g = dy * gamma;
             // dx = rstd * g - rstd * A - xhat * (rstd * B)
-            const float mu = nmu, rs = nrs;
-            if (i + G::NG < n) { nmu = __ldg(a.mean + row + G::NG); nrs = __ldg(a.rstd + row + G::NG); }
+            const float mu = qmu[0], rs = qrs[0];
+#pragma unroll
+            for (int d = 0; d + 1 < kStatAhead; ++d) {
+                qmu[d] = qmu[d + 1];
+                qrs[d] = qrs[d + 1];
+            }
+            if (i + kStatAhead * G::NG < n) {
+                qmu[kStatAhead - 1] = __ldg(a.mean + row + kStatAhead * G::NG);
+                qrs[kStatAhead - 1] = __ldg(a.rstd + row + kStatAhead * G::NG);
+            }
             const float nmr = -mu * rs;
             const float2 rs2 = make_float2(rs, rs), nmr2 = make_float2(nmr, nmr);
             float2 xf[kCacheW ? G::VPT : 1][4], df[kCacheW ? G::VPT : 1][4];
