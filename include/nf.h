@@ -14,6 +14,10 @@
  *     (outer) reduction: "Llu/ln bwd" (NVIDIA/Fuser PR #207), title and the
  *     discussion of "grid-parallel inner-and-outer normalization (special
  *     case for layernorm backward)".
+ *   - The other variants that discussion lists: grid-parallel inner
+ *     normalization (rows longer than one CTA: the cluster and split
+ *     families) and outer normalization (nf_outer_norm_*); and the
+ *     backward passes of RMSNorm and of the fused residual add.
  * The pages name the operations but print no formulas; each function below
  * states the textbook definition it implements.
  *
@@ -43,9 +47,13 @@
  * eps.      Finite and > 0.
  * Stream.   Work is enqueued on `stream` (NULL = the legacy default
  *           stream) and the call returns without synchronizing.
- * Ownership.The caller owns every buffer; the library allocates no device
- *           memory.  It caches, per device, the SM count and the address
- *           of its device status word.
+ * Ownership.The caller owns every buffer (workspaces included); the
+ *           library allocates no device memory.  It caches, per device, the
+ *           SM count and the address of its device status word.
+ * Launches. Kernels are launched as programmatic dependents of the work
+ *           ahead of them on the stream; each waits for that work to
+ *           complete before it touches memory, so stream order holds for
+ *           every caller, and the calls can be captured into CUDA graphs.
  * Errors.   Argument checks happen before any launch and return a status;
  *           a failed launch returns NF_ERR_CUDA.  Nothing is thrown across
  *           the ABI.  A kernel that gives up on a bounded wait records
