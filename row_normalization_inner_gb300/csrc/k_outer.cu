@@ -389,6 +389,8 @@ outer_finalize(const float2* __restrict__ part, const uint16_t* __restrict__ gam
     const int lane = threadIdx.x % 32;
     const int64_t j = col0 + static_cast<int64_t>(blockIdx.x) * kMW + threadIdx.x / 32;
     if (j >= col1) return;  // whole warps
+    // gamma / beta are loaded before the merge so their latency overlaps it
+    const uint16_t gj = gamma[j], bj = beta[j];
     Chan acc{0.f, 0.f, 0.f};
     for (int s0 = 0; s0 < nstripe; s0 += 32 * kMU) {
         float2 p[kMU];
@@ -411,8 +413,8 @@ outer_finalize(const float2* __restrict__ part, const uint16_t* __restrict__ gam
     if (lane != 0) return;
     const float var = acc.m2 / static_cast<float>(rows);
     const float rstd = rsqrtf(var + eps);
-    const float g = __uint_as_float(static_cast<uint32_t>(gamma[j]) << 16);
-    const float b = __uint_as_float(static_cast<uint32_t>(beta[j]) << 16);
+    const float g = __uint_as_float(static_cast<uint32_t>(gj) << 16);
+    const float b = __uint_as_float(static_cast<uint32_t>(bj) << 16);
     const float a = rstd * g;
     if (mean_out) mean_out[j] = acc.mean;
     if (rstd_out) rstd_out[j] = rstd;
@@ -550,13 +552,14 @@ cudaError_t bwd_t(void* dx, float* dgamma, float* dbeta, const void* dy, const v
 
 }  // namespace
 
-int outer_stripes(int64_t rows, int64_t hidden, int sms, bool bwd) {
-    // one wave of resident CTAs over the column tiles, and at least 4 rows
-    // per row lane
+int outer_stripes(int64_t rows, int64_t hidden, int sms) {
+    // about one CTA per SM over the column tiles (measured faster than a
+    // full wave of 2-3 resident CTAs per SM: fewer stripe partials to merge
+    // and longer streams per thread), and at least 4 rows per row lane
     const int64_t r = rows > 0 ? rows : 1;
     const int ox = lanes_for(hidden);
     const int64_t nt = (hidden + ox * kVec - 1) / (ox * kVec);
-    int64_t ns = static_cast<int64_t>(bwd ? kBwdCtasPerSm : kFwdCtasPerSm) * sms / nt;
+    int64_t ns = sms / nt;
     const int64_t rows_min = 4LL * (kOT / ox);
     const int64_t most = (r + rows_min - 1) / rows_min;
     if (ns > most) ns = most;
@@ -566,10 +569,9 @@ int outer_stripes(int64_t rows, int64_t hidden, int sms, bool bwd) {
 }
 
 size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
-    const size_t fwd = static_cast<size_t>(outer_stripes(rows, hidden, sms, false)) * hidden *
-                           sizeof(float2) + 2 * hidden * sizeof(float);
-    const size_t bwd = static_cast<size_t>(outer_stripes(rows, hidden, sms, true)) * 2 * hidden *
-                       sizeof(float);
+    const size_t ns = static_cast<size_t>(outer_stripes(rows, hidden, sms));
+    const size_t fwd = ns * hidden * sizeof(float2) + 2 * hidden * sizeof(float);
+    const size_t bwd = ns * 2 * hidden * sizeof(float);
     return fwd > bwd ? fwd : bwd;
 }
 
@@ -577,7 +579,7 @@ cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, c
                              const void* beta, int64_t rows, int64_t hidden, float eps,
                              void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
-    const int stripes = outer_stripes(rows, hidden, sms, false);
+    const int stripes = outer_stripes(rows, hidden, sms);
     return lanes_for(hidden) == 128
                ? fwd_t<128>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace, stripes, st)
                : fwd_t<32>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace, stripes, st);
@@ -587,7 +589,7 @@ cudaError_t launch_outer_bwd(void* dx, float* dgamma, float* dbeta, const void* 
                              const float* mean, const float* rstd, const void* gamma, int64_t rows,
                              int64_t hidden, void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
-    const int stripes = outer_stripes(rows, hidden, sms, true);
+    const int stripes = outer_stripes(rows, hidden, sms);
     return lanes_for(hidden) == 128
                ? bwd_t<128>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, workspace, stripes, st)
                : bwd_t<32>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, workspace, stripes, st);

@@ -116,9 +116,9 @@ cudaError_t launch_split(int op, const DynArgs& a, void* workspace, int sms, cud
 // `sms` SMs (0 for forward plans that need none).
 size_t plan_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms, int path, int partials);
 
-// Outer (per-column) normalization: row stripes per direction, workspace
-// bytes covering both directions, and the launch sequences.
-int outer_stripes(int64_t rows, int64_t hidden, int sms, bool bwd);
+// Outer (per-column) normalization: row stripes, workspace bytes covering
+// both directions, and the launch sequences.
+int outer_stripes(int64_t rows, int64_t hidden, int sms);
 size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms);
 cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                              const void* beta, int64_t rows, int64_t hidden, float eps,
