@@ -643,7 +643,7 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 storage, fp32 accumulate",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16",
             "data": "synthetic (seeded torch generator on the device; x ~ N(0,1), residual ~ 4 N(0,1), "
                     "weight ~ N(1,0.1))",
             "config": {"workload": f"fused add+RMSNorm forward in place, LLM prefill rows={ROWS}, "
