@@ -54,6 +54,9 @@
  *           ahead of them on the stream; each waits for that work to
  *           complete before it touches memory, so stream order holds for
  *           every caller, and the calls can be captured into CUDA graphs.
+ *           The first call of an entry point on a device sets kernel
+ *           attributes (cudaFuncSetAttribute) and caches device state, so
+ *           make that first call outside a stream capture.
  * Errors.   Argument checks happen before any launch and return a status;
  *           a failed launch returns NF_ERR_CUDA.  Nothing is thrown across
  *           the ABI.  A kernel that gives up on a bounded wait records
