@@ -55,9 +55,9 @@ int bwd_ctas_per_sm(int64_t hidden) {
 //  - forward ops: the register path is fastest at every row count, from 1
 //    row (about 2-3 us per launch, where a cluster split only adds its
 //    barrier latency) to 65536 rows (1.0x the measured copy bandwidth);
-//    the one exception is hidden 12288 RMSNorm / LayerNorm forward with
-//    many rows, where the bulk ring keeps more bytes in flight than 384
-//    threads per row can;
+//    the exceptions are hidden 12288 RMSNorm / LayerNorm forward from 1024
+//    rows and hidden 8192 LayerNorm forward from 16384 rows, where the bulk
+//    ring keeps more bytes in flight than the register-resident rows can;
 //  - backward ops: the bulk path, at every size (its row groups fold their
 //    column partials inside the CTA, so stage 2 stays small).
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
@@ -66,9 +66,10 @@ nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
     if (!fwd) return NF_PATH_BULK;
-    if (hidden >= 12288 && ((op == NF_OP_RMSNORM_FWD && rows >= 1024) ||
-                            (op == NF_OP_LAYERNORM_FWD && rows >= 4096)))
+    if (hidden >= 12288 && rows >= 1024 &&
+        (op == NF_OP_RMSNORM_FWD || op == NF_OP_LAYERNORM_FWD))
         return NF_PATH_BULK;
+    if (hidden == 8192 && rows >= 16384 && op == NF_OP_LAYERNORM_FWD) return NF_PATH_BULK;
     return NF_PATH_REG;
 }
 
