@@ -52,15 +52,17 @@ enum BulkOp { kFused = 0, kRms = 1, kLnFwd = 2, kLnBwd = 3, kRmsBwd = 4, kFusedB
 // Forward: GW warps per row, NGF groups; backward: GWB warps per row, NGB
 // groups (backward rows carry column accumulators, so most backward CTAs
 // stay at 384 threads, where consumers get 232 registers); the fused-add
-// backward (three staged rows) may differ: GWFB, NGFB.  At hidden 8192 the
-// LayerNorm / RMSNorm backward spreads a row over 16 warps (640 threads, 2
-// vectors per thread): the one row a CTA computes at a time finishes in
-// half the time (0.81 -> 0.92 of the copy peak for LayerNorm), while the
-// fused-add backward measured faster at 8 warps.
+// backward (three staged rows) may differ: GWFB, NGFB.  From hidden 2048 up
+// the LayerNorm / RMSNorm backward spreads a row over enough warps that
+// each thread holds 2 vectors (4 warps at 2048, 8 at 4096, 16 at 8192): a
+// row is reduced in fewer serial steps, and at 4096 / 8192 one wide group
+// per CTA measured faster than two narrow ones (LayerNorm 0.81 -> 0.89 and
+// 0.81 -> 0.92 of the copy peak).  The fused-add backward measured faster
+// with its narrower groups, and at 1024 wider groups were slower.
 template <int H> struct BulkRow;
 template <> struct BulkRow<1024>  { static constexpr int GW = 1,  NGF = 16, GWB = 1,  NGB = 8, GWFB = 1,  NGFB = 8; };
-template <> struct BulkRow<2048>  { static constexpr int GW = 2,  NGF = 8,  GWB = 2,  NGB = 4, GWFB = 2,  NGFB = 4; };
-template <> struct BulkRow<4096>  { static constexpr int GW = 4,  NGF = 4,  GWB = 4,  NGB = 2, GWFB = 4,  NGFB = 2; };
+template <> struct BulkRow<2048>  { static constexpr int GW = 2,  NGF = 8,  GWB = 4,  NGB = 2, GWFB = 2,  NGFB = 4; };
+template <> struct BulkRow<4096>  { static constexpr int GW = 4,  NGF = 4,  GWB = 8,  NGB = 1, GWFB = 4,  NGFB = 2; };
 template <> struct BulkRow<5120>  { static constexpr int GW = 4,  NGF = 4,  GWB = 4,  NGB = 2, GWFB = 4,  NGFB = 2; };  // 5 vectors/thread
 template <> struct BulkRow<8192>  { static constexpr int GW = 8,  NGF = 2,  GWB = 16, NGB = 1, GWFB = 8,  NGFB = 1; };
 template <> struct BulkRow<12288> { static constexpr int GW = 12, NGF = 1,  GWB = 12, NGB = 1, GWFB = 12, NGFB = 1; };
