@@ -22,7 +22,7 @@ constexpr int kVec = 8;  // bf16 elements per 128-bit vector
 // row (a multiple of 32), RPC rows per CTA, VPT = hidden / 8 / TPR vectors
 // per thread.
 template <int H> struct RegShape;
-template <> struct RegShape<1024>  { static constexpr int TPR = 32,  RPC = 4; };
+template <> struct RegShape<1024>  { static constexpr int TPR = 32,  RPC = 2; };
 template <> struct RegShape<2048>  { static constexpr int TPR = 64,  RPC = 2; };
 template <> struct RegShape<4096>  { static constexpr int TPR = 128, RPC = 2; };
 template <> struct RegShape<5120>  { static constexpr int TPR = 160, RPC = 1; };
