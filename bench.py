@@ -613,7 +613,7 @@ def run_gpu(args):
             b.synchronize()
             return a.elapsed_time(b)
 
-        # three rounds, each timing the pipeline and then the bare link on the
+        # five rounds, each timing the pipeline and then the bare link on the
         # same bytes; the median round of each is reported (the host link is
         # shared with the rest of the machine, so single rounds vary)
         e2e_steps = max(3, min(args.steps // 40, 25))
@@ -622,7 +622,7 @@ def run_gpu(args):
         if dist is not None:
             dist.barrier()
         e_round, c_round = [], []
-        for r in range(3):
+        for r in range(5):
             e_round.append(max_over_ranks(timed(e2e_steps), dist, dev))
             if r == 0:
                 # check once that the round trip really returned the device

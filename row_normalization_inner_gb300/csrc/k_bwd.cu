@@ -212,52 +212,60 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
 }
 
 // out0[j] = sum_{slot} ws[slot][0][j] and, with two planes,
-// out1[j] = sum_{slot} ws[slot][1][j], in a fixed order: a CTA of 256
-// threads covers X = 256 / Y float4 columns with Y slot lanes each; lane ty
-// sums slots ty, ty + Y, ... and the Y lane sums are then combined by a
-// fixed halving tree.  Y grows with the slot count (each lane reads at most
-// two slots), so the reduction is one or two dependent loads deep and the
-// grid has many CTAs even at hidden 1024.
-constexpr int kColT = 256;
+// out1[j] = sum_{slot} ws[slot][1][j], in a fixed order.  Each float4
+// column gets Y slot lanes of one warp (Y = 16 or 32, so a warp covers
+// 32 / Y columns): lane ly sums slots ly, ly + Y, ly + 2Y, ... in that
+// order, issuing four loads before it adds them, and the Y lane sums are
+// combined by a shuffle butterfly.  Every butterfly step adds the same two
+// values on both partner lanes, so all Y lanes end with the same bits and
+// the result does not depend on the launch.  No shared memory and no CTA
+// barrier: the reduction is a few loads deep plus log2(Y) shuffles.
+constexpr int kColT = 64;  // two warps: many small CTAs spread the columns evenly over the SMs
 
 template <int Y>
-__global__ void __launch_bounds__(kColT)
+__global__ void __launch_bounds__(kColT, 16)
 column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
               float* __restrict__ dbeta, int nslots, int hidden, int planes) {
-    constexpr int X = kColT / Y;
-    __shared__ float4 part[Y][X];
+    static_assert(Y == 16 || Y == 32, "slot lanes per column");
+    constexpr int CPW = 32 / Y;  // float4 columns per warp
     // Launched as a programmatic dependent of stage 1: wait until stage 1
     // has finished and its partials are visible (a no-op otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int tx = threadIdx.x % X, ty = threadIdx.x / X;
-    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * X + tx;  // float4 index in [planes][H]
-    const bool ok = c4 * 4 < planes * static_cast<int64_t>(hidden);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ly = lane % Y, lx = lane / Y;
+    const int64_t c4 = (static_cast<int64_t>(blockIdx.x) * (kColT / 32) + warp) * CPW + lx;
+    const int64_t total4 = static_cast<int64_t>(planes) * hidden / 4;
+    const bool ok = c4 < total4;
     const int which = ok ? static_cast<int>((c4 * 4) / hidden) : 0;
     const int64_t j = ok ? (c4 * 4) % hidden : 0;
+    // slot p of this column is float4 number p * total4 + c4
+    const float4* src = reinterpret_cast<const float4*>(ws) + (ok ? c4 : 0);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
-#pragma unroll 2
-        for (int p = ty; p < nslots; p += Y) {
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(
-                ws + (static_cast<int64_t>(p) * planes + which) * hidden + j));
+        int p = ly;
+        for (; p + 3 * Y < nslots; p += 4 * Y) {
+            const float4 v0 = __ldcs(src + static_cast<int64_t>(p) * total4);
+            const float4 v1 = __ldcs(src + static_cast<int64_t>(p + Y) * total4);
+            const float4 v2 = __ldcs(src + static_cast<int64_t>(p + 2 * Y) * total4);
+            const float4 v3 = __ldcs(src + static_cast<int64_t>(p + 3 * Y) * total4);
+            s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
+            s.x += v1.x; s.y += v1.y; s.z += v1.z; s.w += v1.w;
+            s.x += v2.x; s.y += v2.y; s.z += v2.z; s.w += v2.w;
+            s.x += v3.x; s.y += v3.y; s.z += v3.z; s.w += v3.w;
+        }
+        for (; p < nslots; p += Y) {
+            const float4 v = __ldcs(src + static_cast<int64_t>(p) * total4);
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
     }
-    part[ty][tx] = s;
-    __syncthreads();
 #pragma unroll
-    for (int stride = Y / 2; stride > 0; stride >>= 1) {
-        if (ty < stride) {
-            const float4 v = part[ty + stride][tx];
-            float4& t = part[ty][tx];
-            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-        }
-        __syncthreads();
+    for (int off = Y / 2; off > 0; off >>= 1) {
+        s.x += __shfl_xor_sync(0xFFFFFFFFu, s.x, off);
+        s.y += __shfl_xor_sync(0xFFFFFFFFu, s.y, off);
+        s.z += __shfl_xor_sync(0xFFFFFFFFu, s.z, off);
+        s.w += __shfl_xor_sync(0xFFFFFFFFu, s.w, off);
     }
-    if (ty == 0 && ok) {
-        float* out = (which == 0 ? dgamma : dbeta) + j;
-        *reinterpret_cast<float4*>(out) = part[0][tx];
-    }
+    if (ok && ly == 0) *reinterpret_cast<float4*>((which == 0 ? dgamma : dbeta) + j) = s;
 }
 
 // The same sums when there are few slots (<= kNarrowSlots): one float4
@@ -317,17 +325,16 @@ cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out
         return cudaLaunchKernelEx(&cfg, column_reduce_narrow, ws, out0, out1, nslots,
                                   static_cast<int>(hidden), planes);
     }
-    // slot lanes per column: enough that each lane reads at most two slots
+    // slot lanes per column: 16 up to 64 slots (at most 4 loads a lane),
+    // else 32
     const auto launch = [&](auto kernel, int y) {
-        const int x = kColT / y;
-        cfg.gridDim = dim3(static_cast<unsigned>((cols4 + x - 1) / x), 1, 1);
+        const int64_t per_cta = (kColT / 32) * (32 / y);  // float4 columns per CTA
+        cfg.gridDim = dim3(static_cast<unsigned>((cols4 + per_cta - 1) / per_cta), 1, 1);
         return cudaLaunchKernelEx(&cfg, kernel, ws, out0, out1, nslots, static_cast<int>(hidden),
                                   planes);
     };
-    if (nslots <= 64) return launch(column_reduce<32>, 32);
-    if (nslots <= 128) return launch(column_reduce<64>, 64);
-    if (nslots <= 256) return launch(column_reduce<128>, 128);
-    return launch(column_reduce<256>, 256);
+    if (nslots <= 64) return launch(column_reduce<16>, 16);
+    return launch(column_reduce<32>, 32);
 }
 
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
