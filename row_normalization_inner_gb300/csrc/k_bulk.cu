@@ -14,12 +14,11 @@
 // stage's barrier phases and the group's row sequence move in lockstep and
 // a parity wait can never match a phase from an earlier use).  A group
 // waits on its row's "full" barrier, reads the row from shared memory with
-// 128-bit loads into registers (4 or 5 vectors of 8 bf16 per thread), releases the
-// stage on its
-// "empty" mbarrier at once (so the next copy starts while it computes),
-// reduces the row within the group (warp shuffles, then a named barrier
-// private to the group), normalizes in registers and stores with 128-bit
-// streaming stores.  Up to S rows per SM are in flight in the ring and NG
+// 128-bit loads into registers (2 to 5 vectors of 8 bf16 per thread),
+// releases the stage on its "empty" mbarrier at once (so the next copy
+// starts while it computes), reduces the row within the group (warp
+// shuffles, then a named barrier private to the group), normalizes in
+// registers and stores with 128-bit streaming stores.  Up to S rows per SM are in flight in the ring and NG
 // rows are being computed at once, independent of the register budget.
 //
 // Register sharing: with SHARE the producer warp group drops to 40
@@ -29,8 +28,9 @@
 // launches the variant without setmaxnreg (same results).
 //
 // Every mbarrier wait is bounded (2 s on the global timer).  A consumer
-// warp that gives up contributes a failure count to its group's reduction,
-// so the whole group sees the same total and leaves together; the producer,
+// warp that gives up contributes a failure count to its group's reduction
+// (a one-warp group needs no count: its lanes vote on the wait), so the
+// whole group sees the same outcome and leaves together; the producer,
 // on giving up, waits (bounded) for the copies it already issued and
 // leaves.  Either records NF_ERR_TIMEOUT in the device status word.
 #include "common.cuh"
