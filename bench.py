@@ -233,7 +233,7 @@ def run_reference(args):
     steps, warmup = args.steps, max(args.warmup, 0)
     import oracle
     oracle.build()
-    # size the per-step sample so that all steps take about a minute
+    # size the per-step sample so that all steps take about --ref-seconds
     probe = [workloads.fused_inputs(64, h, residual_scale=4.0) for h in HIDDENS]
     t0 = time.perf_counter()
     for (x, r, w) in probe:
@@ -241,7 +241,7 @@ def run_reference(args):
         oracle.to_bf16(s)
         oracle.to_bf16(y)
     per_row = (time.perf_counter() - t0) / 64
-    rows_s = int(max(1, min(1024, 60.0 / (max(steps, 1) * per_row))))
+    rows_s = int(max(1, min(1024, args.ref_seconds / (max(steps, 1) * per_row))))
     inputs = [workloads.fused_inputs(rows_s, h, residual_scale=4.0) for h in HIDDENS]
 
     def step():
@@ -793,6 +793,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: about this many seconds of timed oracle steps in all")
     ap.add_argument("--profile-case", default=None, help="OP:ROWSxHIDDEN, run --reps launches and exit")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
