@@ -270,8 +270,8 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
 
 // The same sums when there are few slots (<= kNarrowSlots): one float4
 // column per thread, the slots added in order, so a CTA covers 1024
-// contiguous columns instead of 32 (the wide form would launch a CTA per 32
-// columns with 31 of its 32 slot lanes idle).
+// contiguous columns (the wide form would leave at least half of each
+// column's 16 slot lanes idle).
 constexpr int kNarrowSlots = 8;
 constexpr int kNarrowT = 256;
 
