@@ -419,3 +419,36 @@ def test_split_path_settable_and_workspace_queries_without_gpu():
         assert nf.nf_workspace_size(nf.NF_OP_RMSNORM_FWD, 4, 1 << 20) == 0
     assert nf.nf_workspace_size(99, 4, 4096) == 0
     assert nf.nf_workspace_size(nf.NF_OP_RMSNORM_FWD, 4, 4100) == 0
+
+
+def _header_enums():
+    """NAME = value pairs of every enum in include/nf.h, and the integer
+    #defines, read from the header text."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    vals = {}
+    for body in re.findall(r"typedef\s+enum\s*\{(.*?)\}", src, flags=re.S):
+        for name, v in re.findall(r"\b(NF_[A-Z0-9_]+)\s*=\s*(\d+)", body):
+            vals[name] = int(v)
+    for name, expr in re.findall(r"#define\s+(NF_[A-Z0-9_]+)\s+\((.*?)\)\s*$", src, flags=re.M):
+        m = re.fullmatch(r"\s*(\d+)(?:u|LL)?\s*(?:<<\s*(\d+))?\s*", expr)
+        if m:
+            vals[name] = int(m.group(1)) << int(m.group(2) or 0)
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    h = _header_enums()
+    for name in ("NF_OK", "NF_ERR_INVALID_ARG", "NF_ERR_UNSUPPORTED_HIDDEN", "NF_ERR_MISALIGNED",
+                 "NF_ERR_WORKSPACE_TOO_SMALL", "NF_ERR_CUDA", "NF_ERR_TIMEOUT",
+                 "NF_ERR_UNSUPPORTED_PATH", "NF_PATH_AUTO", "NF_PATH_REG", "NF_PATH_CLUSTER",
+                 "NF_PATH_BULK", "NF_PATH_DYNAMIC", "NF_PATH_SPLIT", "NF_OP_FUSED_ADD_RMSNORM",
+                 "NF_OP_RMSNORM_FWD", "NF_OP_LAYERNORM_FWD", "NF_OP_LAYERNORM_BWD",
+                 "NF_OP_RMSNORM_BWD"):
+        assert getattr(nf, name) == h[name], name
+    assert nf.SPLIT_MAX_HIDDEN == h["NF_SPLIT_MAX_HIDDEN"]
+    assert nf.NOALLOC_SCRATCH_BYTES == h["NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES"]
+    assert set(nf.PATHS.values()) == {v for k, v in h.items() if k.startswith("NF_PATH_")}
+    assert nf.OPS == {k[len("NF_OP_"):].lower(): v for k, v in h.items() if k.startswith("NF_OP_")}
+    for status in range(h["NF_ERR_UNSUPPORTED_PATH"] + 1):
+        name = [k for k, v in h.items() if k.startswith(("NF_OK", "NF_ERR_")) and v == status][0]
+        assert nf.status_string(status) == name
