@@ -199,31 +199,55 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the oracle arm
 
-def oracle_sample(budget_s: float, rows_per_hidden: int = 1024):
+def host_cores():
+    """Cores this process may run on (its affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_sample(budget_s: float, rows_per_hidden: int = 1024, threads: int = 1):
     """Time the fp64 oracle on a bounded sample of the workload: the first
     `rows_per_hidden` rows of each hidden size, repeated until `budget_s`
-    seconds have passed.  Returns (GB/s under the same byte accounting,
-    description, cores)."""
+    seconds have passed.  With threads > 1 the rows are cut into `threads`
+    contiguous slices and each host thread runs the unchanged oracle
+    functions on its own slices (ctypes releases the interpreter lock while
+    the C code runs).  Returns (GB/s under the same byte accounting,
+    description, threads, seconds, passes)."""
+    import concurrent.futures as cf
     import oracle
     oracle.build()
     inputs = [workloads.fused_inputs(rows_per_hidden, h, residual_scale=4.0) for h in HIDDENS]
-    nbytes = 0
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        for (x, r, w), h in zip(inputs, HIDDENS):
+    cuts = [rows_per_hidden * k // threads for k in range(threads + 1)]
+    slices = [[(x[cuts[k]:cuts[k + 1]], r[cuts[k]:cuts[k + 1]], w) for (x, r, w) in inputs]
+              for k in range(threads)]
+
+    def work(part):
+        for (x, r, w) in part:
+            if x.shape[0] == 0:
+                continue
             s, y, _ = oracle.fused_add_rmsnorm(x, r, w, EPS)
             oracle.to_bf16(s)
             oracle.to_bf16(y)
-            nbytes += fused_bytes(rows_per_hidden, h)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
+
+    pass_bytes = sum(fused_bytes(rows_per_hidden, h) for h in HIDDENS)
+    nbytes = 0
+    reps = 0
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        while True:
+            list(ex.map(work, slices))
+            nbytes += pass_bytes
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
     gbs = nbytes / el / 1e9
-    desc = (f"fp64 C oracle, single thread, {reps} pass(es) over the first {rows_per_hidden} rows "
+    kind = "single thread" if threads == 1 else f"{threads} host threads (row slices)"
+    desc = (f"fp64 C oracle, {kind}, {reps} pass(es) over the first {rows_per_hidden} rows "
             f"of each hidden in {list(HIDDENS)} ({el:.1f} s)")
-    return gbs, desc, 1, el, reps
+    return gbs, desc, threads, el, reps
 
 
 def run_reference(args):
@@ -241,7 +265,7 @@ def run_reference(args):
         oracle.to_bf16(s)
         oracle.to_bf16(y)
     per_row = (time.perf_counter() - t0) / 64
-    rows_s = int(max(1, min(1024, args.ref_seconds / (max(steps, 1) * per_row))))
+    rows_s = int(max(1, min(1024, args.ref_seconds / (max(steps + warmup, 1) * per_row))))
     inputs = [workloads.fused_inputs(rows_s, h, residual_scale=4.0) for h in HIDDENS]
 
     def step():
@@ -249,7 +273,7 @@ def run_reference(args):
             s, y, _ = oracle.fused_add_rmsnorm(x, r, w, EPS)
             oracle.to_bf16(s)
             oracle.to_bf16(y)
-    for _ in range(min(warmup, 3)):
+    for _ in range(warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -259,7 +283,7 @@ def run_reference(args):
     v = nbytes / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
-        "n_gpus": 1, "steps": steps, "warmup": min(warmup, 3),
+        "n_gpus": 1, "steps": steps, "warmup": warmup,
         "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, torch CPU generator)",
         "config": {"workload": f"fused add+RMSNorm LLM prefill, bounded sample: first {rows_s} rows "
@@ -326,6 +350,11 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         foot, nbytes = 4 * hidden * rows, outer_fwd_bytes(rows, hidden)
     elif op == "outer_norm_bwd":
         foot, nbytes = 6 * hidden * rows, outer_bwd_bytes(rows, hidden)
+    elif op == "floor_copy":
+        # a plain copy of the fused op's activation bytes at (rows, hidden)
+        foot, nbytes = 8 * hidden * rows, 8 * hidden * rows
+    elif op == "floor_empty":
+        foot, nbytes = 1 << 30, 0
     else:
         foot, nbytes = (6 * hidden + 8) * rows, ln_bwd_bytes(rows, hidden)
     sets = max(1, min(16384, -(-2 * l2_bytes // foot)))
@@ -338,7 +367,18 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
         fwd_ws = torch.empty(max(nf.nf_workspace_size(nf.OPS[op], rows, hidden), 16),
                              dtype=torch.uint8, device=dev)
         fwp, fwn = fwd_ws.data_ptr(), fwd_ws.numel()
-    if op == "fused_add_rmsnorm":
+    if op == "floor_empty":
+        keep = ()
+        fn = lambda i, sh: lib.nf_selftest_floor(0, None, None, 0, sh)  # noqa: E731
+    elif op == "floor_copy":
+        cb = 4 * hidden * rows  # bytes read (= bytes written) per launch
+        src = torch.empty(sets * cb, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        ps, pd = src.data_ptr(), dst.data_ptr()
+        keep = (src, dst)
+        fn = lambda i, sh: lib.nf_selftest_floor(1, pd + (i % sets) * cb, ps + (i % sets) * cb,  # noqa: E731
+                                                  cb, sh)
+    elif op == "fused_add_rmsnorm":
         x, r, w = workloads.fused_inputs(tot, hidden, residual_scale=4.0, device=dev)
         px, pr, pw = x.data_ptr(), r.data_ptr(), w.data_ptr()
         keep = (x, r, w)
@@ -442,20 +482,44 @@ def time_op(nf, op, rows, hidden, eps, l2_bytes, stream, min_launches=20):
 def ops_suite(nf, peak, stream, l2_bytes):
     """Per-operation device time at every workload size: launches captured
     back to back in a CUDA graph over L2-cold input sets (section 9 of the
-    design notes)."""
+    design notes).  Keys are "op ROWSxHIDDEN", with " [path]" when a kernel
+    family is forced instead of the library's own choice."""
     out = {}
 
-    def entry(op, rows, h, eps):
-        ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
+    def entry(op, rows, h, eps, path=None):
+        if path is None:
+            ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
+        else:
+            with nf.forced_path(path):
+                ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        plan_op = "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op
-        path = "outer" if op.startswith("outer") else nf.nf_plan_query(plan_op, rows, h)["path"]
-        out[f"{op} {rows}x{h}"] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                   "us": round(ms * 1e3, 3), "path": path}
+        if op.startswith("floor"):
+            used = "probe"
+        elif op.startswith("outer"):
+            used = "outer"
+        elif path is not None:
+            used = path
+        else:
+            plan_op = "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op
+            used = nf.nf_plan_query(plan_op, rows, h)["path"]
+        key = f"{op} {rows}x{h}" + (f" [{path}]" if path else "")
+        out[key] = {"gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "us": round(ms * 1e3, 3),
+                    "path": used}
 
+    # the launch floor beside the small-batch rows: an empty dependent launch
+    # and a plain copy of the fused op's activation bytes, same harness
+    entry("floor_empty", 1, 8, 0.0)
+    for h in (4096, 8192):
+        for rows in (1, 8, 128):
+            entry("floor_copy", rows, h, 0.0)
     for h in (4096, 8192):
         for rows in (1, 2, 4, 8, 16, 32, 128):
             entry("fused_add_rmsnorm", rows, h, 1e-6)
+        # both families on the small-batch sweep (the automatic choice
+        # follows these numbers)
+        for rows in (1, 2, 4, 8, 32, 128):
+            entry("fused_add_rmsnorm", rows, h, 1e-6, path="reg")
+            entry("fused_add_rmsnorm", rows, h, 1e-6, path="cluster")
     for rows in (4096, 16384, 65536):
         for h in (2048, 4096, 5120, 8192):
             entry("fused_add_rmsnorm", rows, h, EPS)
@@ -463,16 +527,17 @@ def ops_suite(nf, peak, stream, l2_bytes):
         entry("rmsnorm_fwd", ROWS, h, EPS)
     for h in (1024, 4096, 12288):
         entry("layernorm_fwd", ROWS, h, EPS)
-    for h in (1024, 4096, 8192):
+    for h in (1024, 2048, 4096, 8192):
         entry("layernorm_bwd", ROWS, h, EPS)
-    for h in (4096, 8192):
+    for h in (1024, 2048, 4096, 8192):
         entry("rmsnorm_bwd", ROWS, h, EPS)
+    for h in (1024, 2048, 4096, 5120, 8192, 12288):
         entry("fused_add_rmsnorm_bwd", ROWS, h, EPS)
     for rows, h in ((16384, 1024), (16384, 4096), (65536, 1024), (4096, 8192)):
         entry("outer_norm_fwd", rows, h, EPS)
         entry("outer_norm_bwd", rows, h, EPS)
     # rows longer than a cluster holds: the split family
-    for op in ("rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
+    for op in ("rmsnorm_fwd", "layernorm_fwd", "fused_add_rmsnorm", "layernorm_bwd", "rmsnorm_bwd"):
         entry(op, 4, 1 << 22, EPS)
     return out
 
@@ -655,8 +720,12 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        v, desc, cores, el, reps = oracle_sample(args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        ncores = host_cores()
+        v1, desc1, _, _, _ = oracle_sample(args.cpu_seconds)
+        vn, descn, used, _, _ = oracle_sample(args.cpu_seconds, threads=ncores)
+        cpu = {"value": round(vn, 4), "unit": UNIT, "cores": used, "kind": "oracle", "sample": descn,
+               "single_thread": {"value": round(v1, 4), "cores": 1, "sample": desc1},
+               "affinity_cores": ncores}
 
     if rank == 0:
         line = {

@@ -281,17 +281,22 @@ nf_status nf_fused_add_rmsnorm_bwd(void* dx, float* dw, const void* dy, const vo
  * minus the workspace: the column partials go to a fixed
  * NF_LAYERNORM_BWD_NOALLOC_SCRATCH_BYTES area of static device memory
  * inside the library (held by every GPU that loads the library until the
- * process exits).  A size whose partials need more than that area under
- * the plan the call runs (nf_plan_query(NF_OP_LAYERNORM_BWD, ...).partials
- * * 2 * hidden * 4 bytes; about 10 MB at the compiled sizes on a 152-SM
- * GPU) returns NF_ERR_WORKSPACE_TOO_SMALL before anything is launched; argument
- * errors return what nf_layernorm_bwd would.  The first call on
- * each device looks up the area's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream
- * capture.  Every call shares the one area, which keeps the last call's
- * contents (nothing needs clearing: every partial is written before it is
- * read); calls that overlap on the GPU -- on different streams or from
- * different host threads -- race on it, so serialize them. */
+ * process exits).  Argument errors return what nf_layernorm_bwd returns, in
+ * the same order, before the area is looked at.  A size whose partials need
+ * more than the area under the plan the call runs returns
+ * NF_ERR_WORKSPACE_TOO_SMALL before anything is launched.  At the compiled
+ * sizes the largest need is hidden 12288 (one slot of 2 * 12288 fp32 per
+ * SM: 14.25 MiB on a 152-SM GPU, so a part with more than 170 SMs refuses
+ * it); the runtime-hidden sizes near 16384 and the split family's very long
+ * rows can need more and are refused.  The first call on each device looks
+ * up the area's device address (cudaGetSymbolAddress, with that device
+ * current) and caches it; make that first call before any stream capture.
+ * cudaDeviceReset ends the context that owns the area, so a process that
+ * resets a device must not call this entry point on that device again.
+ * Every call shares the one area, which keeps the last call's contents
+ * (nothing needs clearing: every partial is written before it is read);
+ * calls that overlap on the GPU -- on different streams or from different
+ * host threads -- race on it, so serialize them. */
 nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const void* dy,
                                    const void* x, const float* mean, const float* rstd,
                                    const void* gamma, int64_t rows, int64_t hidden,
@@ -362,6 +367,19 @@ nf_status nf_get_device_status(nf_stream stream);
  * NF_ERR_TIMEOUT in the device status word and returns normally; the
  * context stays usable. */
 nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream);
+
+/* Measurement hook: the launch floor set beside small-batch timings.
+ * kind 0 launches one 32-thread CTA that only waits for the previous
+ * kernel in the stream and exits (launched as a programmatic dependent,
+ * like every operation's kernels); dst, src and bytes are ignored.  kind 1
+ * copies `bytes` bytes (a positive multiple of 16) from src to dst
+ * (16-byte aligned device pointers, not overlapping) with 256-thread CTAs
+ * holding 4 16-byte vectors per thread, launched the same way: the
+ * simplest kernel that moves a small-batch call's bytes.  Returns
+ * NF_ERR_INVALID_ARG (unknown kind, bad size, null or overlapping
+ * buffers) or NF_ERR_MISALIGNED before launching anything. */
+nf_status nf_selftest_floor(int32_t kind, void* dst, const void* src, int64_t bytes,
+                            nf_stream stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nf_status_string(nf_status status);

@@ -58,7 +58,7 @@ EXPORTS = (
     "nf_fused_add_rmsnorm_bwd", "nf_workspace_size", "nf_fused_add_rmsnorm_ws", "nf_rmsnorm_fwd_ws",
     "nf_layernorm_fwd_ws",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
-    "nf_selftest_wait_timeout", "nf_status_string", "nf_version",
+    "nf_selftest_wait_timeout", "nf_selftest_floor", "nf_status_string", "nf_version",
 )
 
 
@@ -112,6 +112,7 @@ def _bind(lib):
         "nf_plan_compute": (_S, [_S, _I64, _I64, ctypes.c_int32, _S, ctypes.POINTER(Plan)]),
         "nf_get_device_status": (_S, [_P]),
         "nf_selftest_wait_timeout": (_S, [_I64, _P]),
+        "nf_selftest_floor": (_S, [ctypes.c_int32, _P, _P, _I64, _P]),
         "nf_status_string": (ctypes.c_char_p, [_S]),
         "nf_version": (ctypes.c_char_p, []),
     }
@@ -262,6 +263,10 @@ def nf_get_device_status(stream) -> int:
 
 def nf_selftest_wait_timeout(timeout_ns, stream) -> int:
     return lib().nf_selftest_wait_timeout(timeout_ns, stream)
+
+
+def nf_selftest_floor(kind, dst, src, nbytes, stream) -> int:
+    return lib().nf_selftest_floor(kind, dst, src, nbytes, stream)
 
 
 # ---------------------------------------------------------------- tensor helpers

@@ -16,7 +16,9 @@
 
 #include "../../include/nf.h"
 #include "common.cuh"
+#include "internal.h"
 #include "launch.h"
+#include "pdl.cuh"
 
 namespace nf {
 
@@ -227,6 +229,34 @@ __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         if (!mbar_wait(&bar, 0, timeout_ns)) record_status(status, kStatusTimeout);
+    }
+}
+
+// Launch-floor probes (nf_selftest_floor): an empty dependent launch, and a
+// plain copy of 16-byte vectors, 4 per thread, launched the same way as the
+// operations' kernels.
+__global__ void floor_empty_kernel() {
+    grid_dep_wait();
+    grid_dep_release();
+}
+
+constexpr int kFloorThreads = 256;
+
+__global__ void __launch_bounds__(kFloorThreads)
+floor_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_t n16) {
+    grid_dep_wait();
+    grid_dep_release();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * 4 * kFloorThreads + threadIdx.x;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = base + k * kFloorThreads;
+        if (i < n16) v[k] = ld_stream(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = base + k * kFloorThreads;
+        if (i < n16) st_stream(dst + i, v[k]);
     }
 }
 
@@ -603,6 +633,19 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
                            const float* mean, const float* rstd, const void* gamma, int64_t rows,
                            int64_t hidden, void* workspace, size_t workspace_bytes,
                            nf_stream stream) {
+    return nf::layernorm_bwd_impl(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                                  workspace, workspace_bytes, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace nf {
+
+// (declared in internal.h)
+nf_status layernorm_bwd_impl(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                             const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                             int64_t hidden, void* workspace, size_t workspace_bytes,
+                             nf_status (*scratch)(void**), nf_stream stream) {
     if (nf_status st = common_checks(NF_OP_LAYERNORM_BWD, rows, hidden, 0.f, false)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (rows == 0) {
@@ -613,18 +656,25 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         if (dbeta && cudaMemsetAsync(dbeta, 0, hidden * sizeof(float), s) != cudaSuccess) return NF_ERR_CUDA;
         return NF_OK;
     }
-    if (!dx || !dgamma || !dbeta || !dy || !x || !mean || !rstd || !gamma || !workspace)
+    if (!dx || !dgamma || !dbeta || !dy || !x || !mean || !rstd || !gamma || (!scratch && !workspace))
         return NF_ERR_INVALID_ARG;
     if (!aligned(dx, 16) || !aligned(dy, 16) || !aligned(x, 16) || !aligned(gamma, 16) ||
-        !aligned(workspace, 16) || !aligned(dgamma, 16) || !aligned(dbeta, 16) ||
+        (!scratch && !aligned(workspace, 16)) || !aligned(dgamma, 16) || !aligned(dbeta, 16) ||
         !aligned(mean, 4) || !aligned(rstd, 4))
         return NF_ERR_MISALIGNED;
     nf_plan pl;
     if (nf_status st = plan_for_call(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
     size_t need;
-    if (nf_status st = check_workspace(NF_OP_LAYERNORM_BWD, rows, hidden, pl, workspace,
-                                       workspace_bytes, &need))
+    if (scratch) {
+        int sms;
+        if (nf_status st = device_sm_count(&sms)) return st;
+        need = plan_workspace_bytes(NF_OP_LAYERNORM_BWD, rows, hidden, sms, pl.path, pl.partials);
+        if (need > workspace_bytes) return NF_ERR_WORKSPACE_TOO_SMALL;
+        workspace = nullptr;  // the library's own area cannot overlap the caller's buffers
+    } else if (nf_status st = check_workspace(NF_OP_LAYERNORM_BWD, rows, hidden, pl, workspace,
+                                              workspace_bytes, &need)) {
         return st;
+    }
     const int64_t act = rows * hidden * 2, par = hidden * 2, stat = rows * 4, grad = hidden * 4;
     const Span sdx{dx, act}, sdg{dgamma, grad}, sdb{dbeta, grad}, sws{workspace, static_cast<int64_t>(need)};
     const Span ins[] = {{dy, act}, {x, act}, {mean, stat}, {rstd, stat}, {gamma, par}};
@@ -637,6 +687,9 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
         const bool dx_clash = i < 2 ? bad_overlap_except_alias(sdx, in) : overlap(sdx, in);
         if (dx_clash || overlap(sdg, in) || overlap(sdb, in) || overlap(sws, in))
             return NF_ERR_INVALID_ARG;
+    }
+    if (scratch) {
+        if (nf_status st = scratch(&workspace)) return st;
     }
     float* ws = static_cast<float*>(workspace);
     if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT) {
@@ -676,6 +729,10 @@ nf_status nf_layernorm_bwd(void* dx, float* dgamma, float* dbeta, const void* dy
     }
     return from_cuda(launch_column_reduce(ws, dgamma, dbeta, pl.partials, hidden, s));
 }
+
+}  // namespace nf
+
+extern "C" {
 
 size_t nf_rmsnorm_bwd_workspace_size(int64_t rows, int64_t hidden) {
     return bwd_workspace_bytes(NF_OP_RMSNORM_BWD, rows, hidden);
@@ -874,6 +931,22 @@ nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream) {
     if (timeout_ns > 1000000000) timeout_ns = 1000000000;
     return from_cuda(launch_wait_selftest(addr, static_cast<uint64_t>(timeout_ns),
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nf_status nf_selftest_floor(int32_t kind, void* dst, const void* src, int64_t bytes,
+                            nf_stream stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kind == 0) return from_cuda(launch_with_pdl(floor_empty_kernel, dim3(1), dim3(32), 0, s));
+    if (kind != 1) return NF_ERR_INVALID_ARG;
+    if (!dst || !src || bytes <= 0 || bytes % 16 != 0) return NF_ERR_INVALID_ARG;
+    if (!aligned(dst, 16) || !aligned(src, 16)) return NF_ERR_MISALIGNED;
+    if (overlap({dst, bytes}, {src, bytes})) return NF_ERR_INVALID_ARG;
+    const int64_t n16 = bytes / 16;
+    const int64_t grid = (n16 + 4 * kFloorThreads - 1) / (4 * kFloorThreads);
+    if (grid > 0x7FFFFFFF) return NF_ERR_INVALID_ARG;
+    return from_cuda(launch_with_pdl(floor_copy_kernel, dim3(static_cast<unsigned>(grid)),
+                                     dim3(kFloorThreads), 0, s, static_cast<uint4*>(dst),
+                                     static_cast<const uint4*>(src), n16));
 }
 
 const char* nf_status_string(nf_status status) {

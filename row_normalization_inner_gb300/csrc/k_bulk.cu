@@ -635,6 +635,8 @@ bool shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* groups)
 }  // namespace
 
 bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups) {
+    if ((op == kLnBwd || op == kRmsBwd) && rows_bwd_shape(op, hidden, threads, stages, smem_bytes, groups))
+        return true;
     switch (op) {
         case kFused: return shape_of<kFused>(hidden, threads, stages, smem_bytes, groups);
         case kRms: return shape_of<kRms>(hidden, threads, stages, smem_bytes, groups);
@@ -690,6 +692,9 @@ cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd
 cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st) {
+    int t, sg, sm, ng;
+    if (rows_bwd_shape(kLnBwd, hidden, &t, &sg, &sm, &ng))
+        return launch_ln_bwd_rows(hidden, dx, ws, dy, x, mean, rstd, gamma, rows, grid, status, st);
     BulkArgs a{};
     a.out0 = static_cast<uint16_t*>(dx);
     a.in0 = static_cast<const uint16_t*>(x);
@@ -706,6 +711,9 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* 
 cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                 const void* dres, const void* w, int64_t rows, float eps, int grid,
                                 int* status, cudaStream_t st) {
+    int t, sg, sm, ng;
+    if (rows_bwd_shape(kRmsBwd, hidden, &t, &sg, &sm, &ng))
+        return launch_rms_bwd_rows(hidden, dx, ws, dy, x, dres, w, rows, eps, grid, status, st);
     BulkArgs a{};
     a.out0 = static_cast<uint16_t*>(dx);
     a.in0 = static_cast<const uint16_t*>(x);

@@ -75,6 +75,18 @@ cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void*
                                 const void* dres, const void* w, int64_t rows, float eps, int grid,
                                 int* status, cudaStream_t st);
 
+// Row-block backward kernels for hidden 1024 and 2048 (the bulk path's
+// backward there): blocks of consecutive rows per bulk copy, a whole row per
+// thread group, one column-partial slot per CTA.  op: 3 LayerNorm
+// backward, 4 RMSNorm backward.
+bool rows_bwd_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups);
+cudaError_t launch_ln_bwd_rows(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                               const float* mean, const float* rstd, const void* gamma,
+                               int64_t rows, int grid, int* status, cudaStream_t st);
+cudaError_t launch_rms_bwd_rows(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
+                                const void* dres, const void* w, int64_t rows, float eps, int grid,
+                                int* status, cudaStream_t st);
+
 // Runtime-hidden path (any hidden that is a multiple of 8 up to
 // dyn_max_hidden(op)).  op: 0 fused, 1 rms fwd, 2 ln fwd, 3 ln bwd, 4 rms bwd.
 struct DynArgs {

@@ -7,22 +7,24 @@
 // framework's caching allocator must not be entered, in a plugin that only
 // receives pre-allocated tensors, in a real-time path where cudaMalloc's
 // implicit synchronization is not acceptable).  For them this file keeps a
-// fixed scratch area in the library's own static device memory and
-// forwards to the ordinary entry point with it.
+// fixed scratch area in the library's own static device memory and runs
+// the ordinary LayerNorm backward on it.
 //
 // The area is a file-scope __device__ array: every GPU that loads the
 // library holds kNoAllocScratchBytes of it until the process exits.  In
 // host code its name only stands in for the device object, so the device
 // address is looked up once per device with cudaGetSymbolAddress (with that
 // device current) and cached; that first call on a device should come
-// before any stream capture.  Calls that overlap on the GPU (different
-// streams, or different host threads) share the one area and race.
+// before any stream capture.  A cudaDeviceReset ends the context that owns
+// the area, so the cached address is stale afterwards: a process that
+// resets a device must not call this entry point on it again.  Calls that
+// overlap on the GPU (different streams, or different host threads) share
+// the one area and race.
 #include <cuda_runtime.h>
 
 #include <atomic>
 
-#include "../../include/nf.h"
-#include "launch.h"
+#include "internal.h"
 
 namespace nf {
 namespace {
@@ -57,26 +59,10 @@ nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const 
                                    const void* x, const float* mean, const float* rstd,
                                    const void* gamma, int64_t rows, int64_t hidden,
                                    nf_stream stream) {
-    if (rows == 0)  // no scratch is touched; same result as the ordinary entry point
-        return nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
-                                nullptr, 0, stream);
-    // Sizes whose partials (for the plan this call will run) exceed the
-    // fixed area are refused up front, before anything is launched.
-    nf_plan pl;
-    if (nf_status st = nf_plan_query(NF_OP_LAYERNORM_BWD, rows, hidden, &pl)) return st;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return NF_ERR_CUDA;
-    const size_t need = nf::plan_workspace_bytes(NF_OP_LAYERNORM_BWD, rows, hidden, sms, pl.path,
-                                                 pl.partials);
-    if (need > nf::kNoAllocScratchBytes) return NF_ERR_WORKSPACE_TOO_SMALL;
-    void* scratch = nullptr;
-    if (nf_status st = nf::scratch_address(&scratch)) return st;
-    // Stage 1 writes every partial slot before stage 2 reads it, so the
-    // area needs no clearing between calls.
-    return nf_layernorm_bwd(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, scratch,
-                            nf::kNoAllocScratchBytes, stream);
+    // Stage 1 writes every partial slot it uses before stage 2 reads it, so
+    // the area needs no clearing between calls.
+    return nf::layernorm_bwd_impl(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden,
+                                  nullptr, nf::kNoAllocScratchBytes, nf::scratch_address, stream);
 }
 
 }  // extern "C"

@@ -452,3 +452,29 @@ def test_binding_constants_match_the_header():
     for status in range(h["NF_ERR_UNSUPPORTED_PATH"] + 1):
         name = [k for k, v in h.items() if k.startswith(("NF_OK", "NF_ERR_")) and v == status][0]
         assert nf.status_string(status) == name
+
+
+def test_floor_probe_rejects_bad_arguments_before_launch():
+    # every check runs before any CUDA call, so no GPU is needed here
+    assert nf.nf_selftest_floor(2, A, B, 1024, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_selftest_floor(1, 0, B, 1024, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_selftest_floor(1, A, B, 1000, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_selftest_floor(1, A, B, 0, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_selftest_floor(1, A + 8, B, 1024, None) == nf.NF_ERR_MISALIGNED
+    assert nf.nf_selftest_floor(1, A, A + 512, 1024, None) == nf.NF_ERR_INVALID_ARG
+
+
+def test_noalloc_argument_errors_match_the_workspace_entry_point():
+    # null and misaligned arguments are reported as nf_layernorm_bwd reports
+    # them, before the scratch area's size or address is looked at (a size
+    # far beyond the area, so a size check first would say otherwise)
+    args = [A, B, B + 0x100000, C, D, D + 0x1000000, D + 0x2000000, D + 0x3000000]
+    for i in range(8):
+        bad = list(args)
+        bad[i] = 0
+        assert nf.nf_layernorm_bwd_noalloc(*bad, 4096, 16384, None) == nf.NF_ERR_INVALID_ARG
+        assert nf.nf_layernorm_bwd(*bad, 4096, 16384, A + 0x10000000, 1 << 30, None) == \
+            nf.NF_ERR_INVALID_ARG
+    bad = list(args)
+    bad[0] = A + 8   # dx not 16-byte aligned
+    assert nf.nf_layernorm_bwd_noalloc(*bad, 4096, 16384, None) == nf.NF_ERR_MISALIGNED

@@ -422,3 +422,17 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     y = nf.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6)
     torch.cuda.synchronize()
     check_bf16(y, oracle.rmsnorm_fwd(x, w, 1e-6)[0], "after timeout")
+
+
+def test_floor_probes_run_and_copy_exactly():
+    # the launch-floor probes the benchmark times: an empty dependent launch
+    # and a plain copy of a small-batch call's bytes (one CTA and a ragged
+    # multi-CTA size)
+    s = torch.cuda.current_stream().cuda_stream
+    assert nf.nf_selftest_floor(0, 0, 0, 0, s) == nf.NF_OK
+    for nbytes in (16, 16384, 16 * 5000 + 16):
+        src = torch.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=torch.int32, device="cuda")
+        dst = torch.zeros_like(src)
+        assert nf.nf_selftest_floor(1, dst.data_ptr(), src.data_ptr(), nbytes, s) == nf.NF_OK
+        torch.cuda.synchronize()
+        assert torch.equal(dst, src)
