@@ -379,9 +379,12 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
             pl.partials = static_cast<int32_t>(g);
         }
     } else if (p == NF_PATH_BULK) {
-        int threads, stages, smem, groups;
+        int threads, stages, smem, groups, per_sm = 1;
         if (!bulk_shape(op, hidden, &threads, &stages, &smem, &groups)) return NF_ERR_UNSUPPORTED_PATH;
-        int64_t g = rows < sm_count ? rows : sm_count;
+        int t2, s2, m2, g2;
+        if (!fwd) rows_bwd_shape(op, hidden, &t2, &s2, &m2, &g2, &per_sm);  // row-block kernels
+        const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+        int64_t g = rows < slots ? rows : slots;
         if (g < 1) g = 1;
         pl.grid = static_cast<int32_t>(g);
         pl.block = threads;

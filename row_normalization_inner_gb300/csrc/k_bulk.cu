@@ -635,7 +635,9 @@ bool shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* groups)
 }  // namespace
 
 bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups) {
-    if ((op == kLnBwd || op == kRmsBwd) && rows_bwd_shape(op, hidden, threads, stages, smem_bytes, groups))
+    int gm;
+    if ((op == kLnBwd || op == kRmsBwd) &&
+        rows_bwd_shape(op, hidden, threads, stages, smem_bytes, groups, &gm))
         return true;
     switch (op) {
         case kFused: return shape_of<kFused>(hidden, threads, stages, smem_bytes, groups);
@@ -692,8 +694,8 @@ cudaError_t launch_ln_fwd_bulk(int64_t hidden, void* y, float* mean, float* rstd
 cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st) {
-    int t, sg, sm, ng;
-    if (rows_bwd_shape(kLnBwd, hidden, &t, &sg, &sm, &ng))
+    int t, sg, sm, ng, gm;
+    if (rows_bwd_shape(kLnBwd, hidden, &t, &sg, &sm, &ng, &gm))
         return launch_ln_bwd_rows(hidden, dx, ws, dy, x, mean, rstd, gamma, rows, grid, status, st);
     BulkArgs a{};
     a.out0 = static_cast<uint16_t*>(dx);
@@ -711,8 +713,8 @@ cudaError_t launch_ln_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* 
 cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                 const void* dres, const void* w, int64_t rows, float eps, int grid,
                                 int* status, cudaStream_t st) {
-    int t, sg, sm, ng;
-    if (rows_bwd_shape(kRmsBwd, hidden, &t, &sg, &sm, &ng))
+    int t, sg, sm, ng, gm;
+    if (rows_bwd_shape(kRmsBwd, hidden, &t, &sg, &sm, &ng, &gm))
         return launch_rms_bwd_rows(hidden, dx, ws, dy, x, dres, w, rows, eps, grid, status, st);
     BulkArgs a{};
     a.out0 = static_cast<uint16_t*>(dx);

@@ -229,8 +229,10 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     static_assert(Y == 16 || Y == 32, "slot lanes per column");
     constexpr int CPW = 32 / Y;  // float4 columns per warp
     // Launched as a programmatic dependent of stage 1: wait until stage 1
-    // has finished and its partials are visible (a no-op otherwise).
+    // has finished and its partials are visible (a no-op otherwise), then
+    // let the next kernel in the stream be scheduled while this one runs.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ly = lane % Y, lx = lane / Y;
     const int64_t c4 = (static_cast<int64_t>(blockIdx.x) * (kColT / 32) + warp) * CPW + lx;
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(kNarrowT)
 column_reduce_narrow(const float* __restrict__ ws, float* __restrict__ dgamma,
                      float* __restrict__ dbeta, int nslots, int hidden, int planes) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t c4 = static_cast<int64_t>(blockIdx.x) * kNarrowT + threadIdx.x;
     if (c4 * 4 >= planes * static_cast<int64_t>(hidden)) return;
     const int which = static_cast<int>((c4 * 4) / hidden);

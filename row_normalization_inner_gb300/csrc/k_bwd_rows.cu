@@ -51,12 +51,22 @@ namespace nf {
 
 enum RowsOp { kRowsLn = 0, kRowsRms = 1, kRowsFused = 2 };
 
-// Per hidden size: VPT vectors per thread, R rows per block, NG groups.
+// Per hidden size: VPT vectors per thread, R rows per block, NG groups;
+// IL = 0 gives each CTA a contiguous stripe of rows, IL = q >= 1 deals the
+// blocks out to the CTAs in chunks of q consecutive blocks, round robin;
+// CPS CTAs are resident per SM and the grid is GM x SMs CTAs (GM > CPS
+// runs several waves, and the hardware hands the later CTAs to whichever
+// SMs finish first).  Either mapping is a fixed function of (rows, grid),
+// so which rows feed which partial slot never depends on timing.
 template <int OP, int H> struct RowsShape;
-template <int OP> struct RowsShape<OP, 1024> { static constexpr int VPT = 1, R = 4, NG = 3; };
-template <int OP> struct RowsShape<OP, 2048> { static constexpr int VPT = 1, R = 2, NG = 2; };
+template <int OP> struct RowsShape<OP, 1024> {
+    static constexpr int VPT = 1, R = 4, NG = 3, IL = 0, CPS = 1, GM = 1;
+};
+template <int OP> struct RowsShape<OP, 2048> {
+    static constexpr int VPT = 2, R = 2, NG = 3, IL = 0, CPS = 1, GM = 1;
+};
 
-constexpr int kRowsSmemBudget = 200 * 1024;
+constexpr int kRowsSmemBudget = 200 * 1024;  // per SM
 constexpr int kRowsMaxStages = 8;
 
 template <int OP, int H>
@@ -64,6 +74,10 @@ struct RGeo {
     static constexpr int VPT = RowsShape<OP, H>::VPT;
     static constexpr int R = RowsShape<OP, H>::R;
     static constexpr int NG = RowsShape<OP, H>::NG;
+    static constexpr int IL = RowsShape<OP, H>::IL;
+    static constexpr int CPS = RowsShape<OP, H>::CPS;
+    static constexpr int GM = RowsShape<OP, H>::GM;
+    static_assert(CPS >= 1 && GM >= CPS, "at least one wave");
     static constexpr int NV = H / kVec;
     static constexpr int GT = NV / VPT;       // threads per group: one row's width
     static constexpr int GW = GT / 32;
@@ -75,7 +89,7 @@ struct RGeo {
     static constexpr int ROW_BYTES = H * 2;
     static constexpr int TBYTES = R * ROW_BYTES;          // one tensor's block
     static constexpr int STAGE_BYTES = NIN * TBYTES;
-    static constexpr int SG0 = kRowsSmemBudget / STAGE_BYTES / NG;
+    static constexpr int SG0 = kRowsSmemBudget / CPS / STAGE_BYTES / NG;
     static constexpr int SG = SG0 > kRowsMaxStages ? kRowsMaxStages : SG0;
     static_assert(SG >= 2, "at least two stages per group");
     static constexpr int NSUM = 2 * R;                    // row sums per block
@@ -155,11 +169,55 @@ __device__ __forceinline__ void warp_halving_sum(float (&v)[N], int lane) {
     for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
 }
 
+// The blocks of R rows a CTA owns, in the order its groups take them
+// (group g takes the CTA's blocks g, g + NG, ...).
+template <int R, int IL>
+struct BlockMap {
+    int64_t rows, r0;  // contiguous: the CTA's stripe [r0, r0 + n)
+    int n;
+    int64_t c, grid, nblocks;  // interleaved: CTA c of `grid`, nblocks in all
+    int count;         // blocks of this CTA
+
+    __device__ __forceinline__ BlockMap(int64_t rows_, int64_t c_, int64_t grid_)
+        : rows(rows_), c(c_), grid(grid_) {
+        if constexpr (IL == 0) {
+            r0 = rows * c / grid;
+            n = static_cast<int>(rows * (c + 1) / grid - r0);
+            count = (n + R - 1) / R;
+            nblocks = 0;
+        } else {
+            r0 = 0;
+            n = 0;
+            nblocks = (rows + R - 1) / R;
+            const int64_t nchunks = (nblocks + IL - 1) / IL;
+            int64_t k = 0;
+            if (c < nchunks) {
+                const int64_t mc = (nchunks - 1 - c) / grid + 1;  // chunks of this CTA
+                k = mc * IL;
+                const int64_t rem = nblocks % IL;
+                if (rem != 0 && (nchunks - 1 - c) % grid == 0) k -= IL - rem;  // owns the short last chunk
+            }
+            count = static_cast<int>(k);
+        }
+    }
+    // first row and row count of this CTA's k-th block (k < count)
+    __device__ __forceinline__ void block(int k, int64_t* row0, int* nr) const {
+        if constexpr (IL == 0) {
+            *row0 = r0 + static_cast<int64_t>(k) * R;
+            *nr = min(R, n - k * R);
+        } else {
+            const int64_t b = (c + static_cast<int64_t>(k / IL) * grid) * IL + k % IL;
+            *row0 = b * R;
+            *nr = static_cast<int>(min(static_cast<int64_t>(R), rows - b * R));
+        }
+    }
+};
+
 template <int N> struct Log2 { static constexpr int v = 1 + Log2<N / 2>::v; };
 template <> struct Log2<1> { static constexpr int v = 0; };
 
 template <int OP, int H>
-__global__ void __launch_bounds__(RGeo<OP, H>::THREADS, 1)
+__global__ void __launch_bounds__(RGeo<OP, H>::THREADS, RGeo<OP, H>::CPS)
 norm_rows_bwd_kernel(RowsArgs a) {
     using G = RGeo<OP, H>;
     constexpr int R = G::R, VPT = G::VPT, NSUM = G::NSUM;
@@ -169,10 +227,8 @@ norm_rows_bwd_kernel(RowsArgs a) {
     const int g = threadIdx.x / G::GT;
     const int gt = threadIdx.x % G::GT;
     const int warp = gt >> 5, lane = gt & 31;
-    const int64_t r0 = a.rows * blockIdx.x / gridDim.x;
-    const int64_t r1 = a.rows * (blockIdx.x + 1) / gridDim.x;
-    const int n = static_cast<int>(r1 - r0);
-    const int nb = (n + R - 1) / R;                                  // blocks of the stripe
+    const BlockMap<R, G::IL> map(a.rows, blockIdx.x, gridDim.x);
+    const int nb = map.count;                                       // blocks of this CTA
     const int mine = nb > g ? (nb - g + G::NG - 1) / G::NG : 0;     // blocks of this group
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::BAR_OFF) + g * G::SG;
@@ -185,11 +241,11 @@ norm_rows_bwd_kernel(RowsArgs a) {
     }
     __syncthreads();
 
-    // block j of this group: rows [r0 + b R, +nr) with b = g + j NG, stage j % SG
+    // block j of this group is the CTA's block g + j NG; it uses stage j % SG
     const auto issue = [&](int j) {
-        const int b = g + j * G::NG;
-        const int nr = min(R, n - b * R);
-        const int64_t row = r0 + static_cast<int64_t>(b) * R;
+        int64_t row;
+        int nr;
+        map.block(g + j * G::NG, &row, &nr);
         const int s = j % G::SG;
         const uint32_t bytes = static_cast<uint32_t>(nr) * G::ROW_BYTES;
         mbar_arrive_expect_tx(&full[s], G::NIN * bytes);
@@ -228,9 +284,9 @@ norm_rows_bwd_kernel(RowsArgs a) {
         for (int r = 0; r < R; ++r) { m[r] = 0.f; rr[r] = 0.f; }
         if constexpr (OP == kRowsLn) {
             if (j < mine) {
-                const int b = g + j * G::NG;
-                const int nr = min(R, n - b * R);
-                const int64_t row = r0 + static_cast<int64_t>(b) * R;
+                int64_t row;
+                int nr;
+                map.block(g + j * G::NG, &row, &nr);
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     if (r < nr) { m[r] = __ldg(a.mean + row + r); rr[r] = __ldg(a.rstd + row + r); }
@@ -242,9 +298,9 @@ norm_rows_bwd_kernel(RowsArgs a) {
     bool failed = false;
     int j = 0;
     for (; j < mine; ++j) {
-        const int b = g + j * G::NG;
-        const int nr = min(R, n - b * R);
-        const int64_t row0 = r0 + static_cast<int64_t>(b) * R;
+        int64_t row0;
+        int nr;
+        map.block(g + j * G::NG, &row0, &nr);
         const int s = j % G::SG;
         const uint32_t par = (j / G::SG) & 1;
         fetch_stats(j + 1, mu_n, rs_n);
@@ -445,11 +501,12 @@ cudaError_t launch_rows_op(int64_t hidden, const RowsArgs& a, int grid, cudaStre
 }
 
 template <int OP>
-bool rows_shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* groups) {
+bool rows_shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* groups, int* grid_per_sm) {
     switch (hidden) {
 #define NF_ROWS_CASE(HV)                                                                 \
         case HV: *threads = RGeo<OP, HV>::THREADS; *stages = RGeo<OP, HV>::NG * RGeo<OP, HV>::SG; \
-                 *smem = RGeo<OP, HV>::SMEM; *groups = RGeo<OP, HV>::NG; return true;
+                 *smem = RGeo<OP, HV>::SMEM; *groups = RGeo<OP, HV>::NG;                  \
+                 *grid_per_sm = RGeo<OP, HV>::GM; return true;
         NF_ROWS_CASE(1024) NF_ROWS_CASE(2048)
 #undef NF_ROWS_CASE
         default: return false;
@@ -458,10 +515,11 @@ bool rows_shape_of(int64_t hidden, int* threads, int* stages, int* smem, int* gr
 
 }  // namespace
 
-bool rows_bwd_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups) {
+bool rows_bwd_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups,
+                    int* grid_per_sm) {
     // op numbering of the bulk family: 3 LayerNorm backward, 4 RMSNorm backward
-    if (op == 3) return rows_shape_of<kRowsLn>(hidden, threads, stages, smem_bytes, groups);
-    if (op == 4) return rows_shape_of<kRowsRms>(hidden, threads, stages, smem_bytes, groups);
+    if (op == 3) return rows_shape_of<kRowsLn>(hidden, threads, stages, smem_bytes, groups, grid_per_sm);
+    if (op == 4) return rows_shape_of<kRowsRms>(hidden, threads, stages, smem_bytes, groups, grid_per_sm);
     return false;
 }
 

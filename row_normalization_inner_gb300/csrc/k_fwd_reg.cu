@@ -31,9 +31,32 @@ struct Geo {
     static_assert(TPR % 32 == 0, "a row uses whole warps");
 };
 
+// A parameter vector (weight, gamma or beta) of this thread's columns.
+// With PRE the thread loads all VPT vectors once, before its first row, so
+// a call with few rows makes one memory round trip (the row and the
+// parameters together) instead of loading the parameters after the row
+// reduction; without it each is read when it is used, costing no registers
+// across the reduction (the choice for large row counts, where occupancy
+// matters and the parameters sit in L1).
+template <int VPT, bool PRE>
+struct ParamVecs {
+    uint4 v[PRE ? VPT : 1];
+    __device__ __forceinline__ ParamVecs(const uint16_t* p, int tpr, int t) {
+        if constexpr (PRE) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) v[k] = ld_param(p + (k * tpr + t) * kVec);
+        }
+    }
+    // vector k of this thread, which is vector `vi` of the row
+    __device__ __forceinline__ uint4 get(int k, const uint16_t* p, int vi) const {
+        if constexpr (PRE) return v[k];
+        else return ld_param(p + vi * kVec);
+    }
+};
+
 // residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
 // [kernel-span fused_add_rmsnorm_reg]
-template <int H>
+template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
                       const uint16_t* __restrict__ w, int64_t rows, float eps) {
@@ -42,6 +65,7 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
     grid_dep_wait();
     grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    ParamVecs<G::VPT, PRE> wp(w, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
@@ -78,7 +102,7 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
             for (int k = 0; k < G::VPT; ++k) {
                 const int v = k * G::TPR + t;
                 float wf[8], o[8];
-                unpack8(ld_param(w + v * kVec), wf);
+                unpack8(wp.get(k, w, v), wf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = s[k][e] * rstd * wf[e];
                 st_stream(xr + v * kVec, pack8(o));
@@ -90,7 +114,7 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
 // [end kernel-span fused_add_rmsnorm_reg]
 
 // y <- bf16(x * rsqrt(mean(x^2) + eps) * w)
-template <int H>
+template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
                 int64_t rows, float eps) {
@@ -99,6 +123,7 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
     grid_dep_wait();
     grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    ParamVecs<G::VPT, PRE> wp(w, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
@@ -128,7 +153,7 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
                 const int v = k * G::TPR + t;
                 float2 f[4], wf[4], o[4];
                 unpack8x2(xv[k], f);
-                unpack8x2(ld_param(w + v * kVec), wf);
+                unpack8x2(wp.get(k, w, v), wf);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) o[q] = __fmul2_rn(__fmul2_rn(f[q], rstd2), wf[q]);
                 st_stream(y + row * H + v * kVec, pack8x2(o));
@@ -140,7 +165,7 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
 
 // mean = sum(x)/H ; var = sum((x-mean)^2)/H ; rstd = rsqrt(var + eps)
 // y <- bf16((x - mean) * rstd * gamma + beta)
-template <int H>
+template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                   const uint16_t* x, const uint16_t* __restrict__ gamma,
@@ -151,6 +176,7 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     grid_dep_wait();
     grid_dep_release();
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    ParamVecs<G::VPT, PRE> gp(gamma, G::TPR, t), bp(beta, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
         const int64_t row = blk * G::RPC + group;
@@ -216,8 +242,8 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 #pragma unroll
                     for (int q = 0; q < 4; ++q) xm[q] = __fadd2_rn(xm[q], nmean2);
                 }
-                unpack8x2(ld_param(gamma + v * kVec), gf);
-                unpack8x2(ld_param(beta + v * kVec), bf);
+                unpack8x2(gp.get(k, gamma, v), gf);
+                unpack8x2(bp.get(k, beta, v), bf);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) o[q] = __ffma2_rn(xm[q], __fmul2_rn(rstd2, gf[q]), bf[q]);
                 st_stream(y + row * H + v * kVec, pack8x2(o));
@@ -231,33 +257,141 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     }
 }
 
+// LayerNorm forward with one reduction per row: each warp shifts its values
+// by one of them (c = the first element its lane 0 holds) and sums d = x - c
+// and d^2; the warp's (mean, M2) = (c + sum d / n, sum d^2 - (sum d)^2 / n)
+// over its n elements, and the warps of a row are combined with Chan,
+// Golub and LeVeque's pairwise update in warp order.  Because c is one of
+// the warp's own values, (c - mean)^2 <= n * var, so the cancellation in
+// sum d^2 - (sum d)^2 / n costs at most about n fp32 roundings relative to
+// M2 (n <= 1024 here): far below the bf16 output rounding.
+template <int H, bool PRE>
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
+                    const uint16_t* x, const uint16_t* __restrict__ gamma,
+                    const uint16_t* __restrict__ beta, int64_t rows, float eps) {
+    using G = Geo<H>;
+    constexpr float kNW = 32.0f * G::VPT * kVec;  // elements per warp
+    __shared__ float red[G::W > 1 ? G::RPC * G::W * 2 : 1];
+    grid_dep_wait();
+    grid_dep_release();
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    ParamVecs<G::VPT, PRE> gp(gamma, G::TPR, t), bp(beta, G::TPR, t);
+    const int warp = t >> 5, lane = t & 31;
+    const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int64_t row = blk * G::RPC + group;
+        const bool active = row < rows;
+        uint4 xv[G::VPT];
+        float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+        float c = 0.f;
+        if (active) {
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) xv[k] = ld_stream(x + row * H + (k * G::TPR + t) * kVec);
+            c = __shfl_sync(0xFFFFFFFFu, bf_lo(xv[0].x), 0);
+            const float2 nc2 = make_float2(-c, -c);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                float2 f[4];
+                unpack8x2(xv[k], f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 d = __fadd2_rn(f[q], nc2);
+                    s1 = __fadd2_rn(s1, d);
+                    s2 = __ffma2_rn(d, d, s2);
+                }
+            }
+        }
+        float v[2] = {s1.x + s1.y, s2.x + s2.y};
+        warp_sum<2>(v);
+        const float dm = v[0] * (1.0f / kNW);
+        float mean = c + dm;
+        float m2 = fmaxf(v[1] - v[0] * dm, 0.f);
+        if constexpr (G::W > 1) {
+            float* rb = red + group * G::W * 2;
+            if (lane == 0) {
+                rb[warp * 2] = mean;
+                rb[warp * 2 + 1] = m2;
+            }
+            __syncthreads();
+            mean = rb[0];
+            m2 = rb[1];
+            float n = kNW;
+#pragma unroll
+            for (int w = 1; w < G::W; ++w) {
+                const float d = rb[w * 2] - mean;
+                const float nt = n + kNW;
+                const float fb = kNW / nt;
+                mean = fmaf(d, fb, mean);
+                m2 += rb[w * 2 + 1] + d * d * n * fb;
+                n = nt;
+            }
+        }
+        if (active) {
+            const float rstd = rsqrtf(m2 * (1.0f / H) + eps);
+            const float2 rstd2 = make_float2(rstd, rstd), nmean2 = make_float2(-mean, -mean);
+#pragma unroll
+            for (int k = 0; k < G::VPT; ++k) {
+                const int vi = k * G::TPR + t;
+                float2 xm[4], gf[4], bf[4], o[4];
+                unpack8x2(xv[k], xm);
+                unpack8x2(gp.get(k, gamma, vi), gf);
+                unpack8x2(bp.get(k, beta, vi), bf);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o[q] = __ffma2_rn(__fadd2_rn(xm[q], nmean2), __fmul2_rn(rstd2, gf[q]), bf[q]);
+                st_stream(y + row * H + vi * kVec, pack8x2(o));
+            }
+            if (t == 0) {
+                if (mean_out) mean_out[row] = mean;
+                if (rstd_out) rstd_out[row] = rstd;
+            }
+        }
+        if constexpr (G::W > 1) __syncthreads();  // `red` is reused by the next row block
+    }
+}
+
+// Which LayerNorm forward statistics the register path uses (two passes
+// over the resident row, or one shifted pass).
+constexpr bool kLnFwdShifted = false;
+
+// Calls of at most this many rows load their parameters before the first
+// row (ParamVecs with PRE).
+constexpr int64_t kPrefetchParamRows = 1024;
+
 }  // namespace
 
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
                              float eps, int grid, cudaStream_t st) {
+    const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
-        return launch_with_pdl(fused_add_rmsnorm_reg<H>, dim3(grid),
-                               dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st, static_cast<uint16_t*>(x),
-                               static_cast<uint16_t*>(res), static_cast<const uint16_t*>(w), rows,
-                               eps);
+        return launch_with_pdl(pre ? fused_add_rmsnorm_reg<H, true> : fused_add_rmsnorm_reg<H, false>,
+                               dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st,
+                               static_cast<uint16_t*>(x), static_cast<uint16_t*>(res),
+                               static_cast<const uint16_t*>(w), rows, eps);
     })
 }
 
 cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
                            float eps, int grid, cudaStream_t st) {
+    const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
-        return launch_with_pdl(rmsnorm_fwd_reg<H>, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0,
-                               st, static_cast<uint16_t*>(y), static_cast<const uint16_t*>(x),
-                               static_cast<const uint16_t*>(w), rows, eps);
+        return launch_with_pdl(pre ? rmsnorm_fwd_reg<H, true> : rmsnorm_fwd_reg<H, false>, dim3(grid),
+                               dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st, static_cast<uint16_t*>(y),
+                               static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w),
+                               rows, eps);
     })
 }
 
 cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                               const void* gamma, const void* beta, int64_t rows, float eps,
                               int grid, cudaStream_t st) {
+    const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
-        return launch_with_pdl(layernorm_fwd_reg<H>, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0,
-                               st, static_cast<uint16_t*>(y), mean, rstd,
+        const auto k = kLnFwdShifted ? (pre ? layernorm_fwd_shift<H, true> : layernorm_fwd_shift<H, false>)
+                                     : (pre ? layernorm_fwd_reg<H, true> : layernorm_fwd_reg<H, false>);
+        return launch_with_pdl(k, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st,
+                               static_cast<uint16_t*>(y), mean, rstd,
                                static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
                                static_cast<const uint16_t*>(beta), rows, eps);
     })

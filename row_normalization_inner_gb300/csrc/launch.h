@@ -77,9 +77,10 @@ cudaError_t launch_rms_bwd_bulk(int64_t hidden, void* dx, float* ws, const void*
 
 // Row-block backward kernels for hidden 1024 and 2048 (the bulk path's
 // backward there): blocks of consecutive rows per bulk copy, a whole row per
-// thread group, one column-partial slot per CTA.  op: 3 LayerNorm
-// backward, 4 RMSNorm backward.
-bool rows_bwd_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups);
+// thread group, one column-partial slot per CTA, grid_per_sm x SMs CTAs.
+// op: 3 LayerNorm backward, 4 RMSNorm backward.
+bool rows_bwd_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups,
+                    int* grid_per_sm);
 cudaError_t launch_ln_bwd_rows(int64_t hidden, void* dx, float* ws, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* gamma,
                                int64_t rows, int grid, int* status, cudaStream_t st);
