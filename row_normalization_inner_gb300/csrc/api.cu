@@ -322,10 +322,14 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.rows_per_cta = 1;
         if (fwd) {
             pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * ry);
-            pl.launches = 3;
+            pl.launches = 2;  // statistics, then apply (which merges its row's partials)
         } else {
             pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * rb);
-            pl.launches = 4;
+            // statistics, a merge launch unless the row blocks are short
+            // enough to merge in the apply pass, apply, and the column
+            // reduction unless one row block writes dgamma / dbeta itself
+            const int64_t rows_per_block = (rows + rb - 1) / (rb > 0 ? rb : 1);
+            pl.launches = 2 + (rows_per_block > kSplitMergeRows ? 1 : 0) + (rb > 1 ? 1 : 0);
             pl.partials = rb;
         }
     } else if (p == NF_PATH_REG && fwd) {
@@ -489,7 +493,9 @@ nf_status nf_fused_add_rmsnorm_ws(void* x, void* residual, const void* weight, i
         if (nf_status st = device_status_addr(&status)) return st;
         return from_cuda(launch_fused_bulk(hidden, x, residual, weight, rows, eps, pl.grid, status, s));
     }
-    return from_cuda(launch_fused_reg(hidden, x, residual, weight, rows, eps, pl.grid, s));
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    return from_cuda(launch_fused_reg(hidden, x, residual, weight, rows, eps, pl.grid, sms, s));
 }
 
 nf_status nf_rmsnorm_fwd(void* y, const void* x, const void* weight, int64_t rows, int64_t hidden,
@@ -548,7 +554,9 @@ nf_status nf_rmsnorm_fwd_ws(void* y, const void* x, const void* weight, int64_t 
         if (nf_status st = device_status_addr(&status)) return st;
         return from_cuda(launch_rms_bulk(hidden, y, x, weight, rows, eps, pl.grid, status, s));
     }
-    return from_cuda(launch_rms_reg(hidden, y, x, weight, rows, eps, pl.grid, s));
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    return from_cuda(launch_rms_reg(hidden, y, x, weight, rows, eps, pl.grid, sms, s));
 }
 
 nf_status nf_layernorm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
@@ -625,7 +633,9 @@ nf_status nf_layernorm_fwd_ws(void* y, float* mean, float* rstd, const void* x, 
         return from_cuda(launch_ln_fwd_bulk(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
                                             pl.grid, status, s));
     }
-    return from_cuda(launch_ln_fwd_reg(hidden, y, mean, rstd, x, gamma, beta, rows, eps, pl.grid, s));
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    return from_cuda(launch_ln_fwd_reg(hidden, y, mean, rstd, x, gamma, beta, rows, eps, pl.grid, sms, s));
 }
 
 size_t nf_layernorm_bwd_workspace_size(int64_t rows, int64_t hidden) {

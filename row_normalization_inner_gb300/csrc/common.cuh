@@ -37,6 +37,27 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinte
 __device__ __forceinline__ uint4 ld_param(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ void st_stream(void* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
 
+// Warm L2 with the line that holds p.  A hint only: no thread reads a
+// different value because of it, and L2 is where global memory is kept
+// coherent, so a kernel launched as a programmatic dependent may issue it
+// for its first rows before griddepcontrol.wait; DRAM then serves those
+// rows while the kernel before it drains.  Only addresses inside the
+// caller's buffers are passed.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// A read-only load that asks L2 to keep the line (evict-last priority): for
+// data a later kernel of the same operation reads again.
+__device__ __forceinline__ uint4 ld_keep(const void* p) {
+    uint4 v;
+    asm volatile("{\n\t.reg .b64 pol;\n\t"
+                 "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+                 "ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], pol;\n\t}"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 // ---- bf16 <-> fp32 ----------------------------------------------------------
 // Widening is exact: a bf16 is the high half of a binary32 pattern.
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }

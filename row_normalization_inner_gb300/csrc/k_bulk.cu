@@ -189,14 +189,27 @@ norm_bulk_kernel(BulkArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::BAR_OFF);
     uint64_t* empty = full + G::S;
-    // launched as a programmatic dependent: nothing is touched before the
-    // previous grid in the stream has finished
-    grid_dep_wait();
-
     const int64_t nct = gridDim.x;
     const int64_t r0 = a.rows * blockIdx.x / nct;
     const int64_t r1 = a.rows * (blockIdx.x + 1) / nct;
     const int n = static_cast<int>(r1 - r0);
+    // Launched as a programmatic dependent: nothing is read before the
+    // previous grid in the stream has finished.  Only L2 is warmed first
+    // with the stripe's first ring-full of rows (a hint; the bulk copies
+    // then find them there).
+    {
+        static_assert(G::ROW_BYTES % 128 == 0, "rows are whole 128-byte lines");
+        const int lines = (n < G::S ? n : G::S) * (G::ROW_BYTES / 128);
+        const uint8_t* t0 = reinterpret_cast<const uint8_t*>(a.in0 + r0 * H);
+        const uint8_t* t1 = OpIO<OP>::NIN >= 2 ? reinterpret_cast<const uint8_t*>(a.in1 + r0 * H) : nullptr;
+        const uint8_t* t2 = OpIO<OP>::NIN == 3 ? reinterpret_cast<const uint8_t*>(a.add + r0 * H) : nullptr;
+        for (int i = threadIdx.x; i < lines; i += G::THREADS) {
+            prefetch_l2(t0 + i * 128);
+            if (t1) prefetch_l2(t1 + i * 128);
+            if (t2) prefetch_l2(t2 + i * 128);
+        }
+    }
+    grid_dep_wait();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G::S; ++s) {

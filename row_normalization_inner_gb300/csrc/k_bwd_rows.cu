@@ -87,6 +87,7 @@ struct RGeo {
     static_assert(THREADS <= 1024 && NG <= 15, "CTA size; named barriers 1..NG");
     static constexpr int NIN = OP == kRowsFused ? 3 : 2;   // staged tensors
     static constexpr int ROW_BYTES = H * 2;
+    static_assert(ROW_BYTES % 128 == 0, "rows are whole 128-byte lines");
     static constexpr int TBYTES = R * ROW_BYTES;          // one tensor's block
     static constexpr int STAGE_BYTES = NIN * TBYTES;
     static constexpr int SG0 = kRowsSmemBudget / CPS / STAGE_BYTES / NG;
@@ -222,7 +223,6 @@ norm_rows_bwd_kernel(RowsArgs a) {
     using G = RGeo<OP, H>;
     constexpr int R = G::R, VPT = G::VPT, NSUM = G::NSUM;
     extern __shared__ __align__(128) uint8_t smem[];
-    grid_dep_wait();
 
     const int g = threadIdx.x / G::GT;
     const int gt = threadIdx.x % G::GT;
@@ -230,6 +230,21 @@ norm_rows_bwd_kernel(RowsArgs a) {
     const BlockMap<R, G::IL> map(a.rows, blockIdx.x, gridDim.x);
     const int nb = map.count;                                       // blocks of this CTA
     const int mine = nb > g ? (nb - g + G::NG - 1) / G::NG : 0;     // blocks of this group
+    // Warm L2 with the group's first SG blocks before waiting for the kernel
+    // ahead in the stream (a hint; the bulk copies below then find them there).
+    for (int j = 0; j < G::SG && j < mine; ++j) {
+        int64_t row;
+        int nr;
+        map.block(g + j * G::NG, &row, &nr);
+        const int lines = nr * (G::ROW_BYTES / 128);
+        for (int i = gt; i < lines; i += G::GT) {
+            prefetch_l2(reinterpret_cast<const uint8_t*>(a.x + row * H) + i * 128);
+            prefetch_l2(reinterpret_cast<const uint8_t*>(a.dy + row * H) + i * 128);
+            if constexpr (OP == kRowsFused)
+                prefetch_l2(reinterpret_cast<const uint8_t*>(a.dres + row * H) + i * 128);
+        }
+    }
+    grid_dep_wait();
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::BAR_OFF) + g * G::SG;
     uint8_t* slice = smem + g * G::SG * G::STAGE_BYTES;
@@ -276,24 +291,26 @@ norm_rows_bwd_kernel(RowsArgs a) {
             if constexpr (OP == kRowsLn) acc1[v][q] = make_float2(0.f, 0.f);
         }
 
-    // LayerNorm: the saved statistics of the group's current block, the
-    // next block's fetched one block ahead
-    float mu[R], rsv[R], mu_n[R], rs_n[R];
-    const auto fetch_stats = [&](int j, float (&m)[R], float (&rr)[R]) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) { m[r] = 0.f; rr[r] = 0.f; }
+    // LayerNorm: the saved statistics of the group's blocks.  Lane l < R of
+    // each warp holds the mean of row l of the block, lane R + l its rstd;
+    // the next block's are fetched one block ahead and broadcast with
+    // shuffles when used.
+    static_assert(2 * R <= 32, "one lane per saved statistic");
+    const auto fetch_stat = [&](int j) {
+        float v = 0.f;
         if constexpr (OP == kRowsLn) {
-            if (j < mine) {
+            if (j < mine && lane < 2 * R) {
                 int64_t row;
                 int nr;
                 map.block(g + j * G::NG, &row, &nr);
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    if (r < nr) { m[r] = __ldg(a.mean + row + r); rr[r] = __ldg(a.rstd + row + r); }
+                const int r = lane % R;
+                if (r < nr) v = __ldg((lane < R ? a.mean : a.rstd) + row + r);
             }
         }
+        return v;
     };
-    fetch_stats(0, mu, rsv);
+    float stat = fetch_stat(0);
+    float mu[R], rsv[R];
 
     bool failed = false;
     int j = 0;
@@ -303,7 +320,12 @@ norm_rows_bwd_kernel(RowsArgs a) {
         map.block(g + j * G::NG, &row0, &nr);
         const int s = j % G::SG;
         const uint32_t par = (j / G::SG) & 1;
-        fetch_stats(j + 1, mu_n, rs_n);
+        const float stat_next = fetch_stat(j + 1);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            mu[r] = __shfl_sync(0xFFFFFFFFu, stat, r);
+            rsv[r] = __shfl_sync(0xFFFFFFFFu, stat, R + r);
+        }
         const bool ok = mbar_wait(&full[s], par, kWaitLimitNs);
         const uint32_t st = smem_addr(slice + s * G::STAGE_BYTES);
 
@@ -429,8 +451,7 @@ norm_rows_bwd_kernel(RowsArgs a) {
                 if (r < nr) st_stream(a.dx + (row0 + r) * H + (v * G::GT + gt) * kVec, pack8x2(o));
             }
         }
-#pragma unroll
-        for (int r = 0; r < R; ++r) { mu[r] = mu_n[r]; rsv[r] = rs_n[r]; }
+        stat = stat_next;
     }
     grid_dep_release();
 

@@ -54,17 +54,40 @@ struct ParamVecs {
     }
 };
 
+// Before waiting for the kernel ahead of it in the stream, warm L2 with
+// this thread's vectors of its CTA's first row (of `a`, and of `b` when
+// given): a hint, no data is read.
+template <typename G>
+__device__ __forceinline__ void prefetch_first_row(const uint16_t* a, const uint16_t* b,
+                                                   int64_t rows, int group, int t,
+                                                   int64_t first_wave) {
+    // Only the first wave of CTAs (first_wave = resident CTAs per SM x SMs)
+    // can be resident before the kernel ahead finishes; later CTAs start
+    // after it and would only duplicate their own loads.
+    if (static_cast<int64_t>(blockIdx.x) >= first_wave) return;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * G::RPC + group;
+    if (row >= rows) return;
+    constexpr int H = G::NV * kVec;
+#pragma unroll
+    for (int k = 0; k < G::VPT; ++k) {
+        const int64_t off = row * H + (k * G::TPR + t) * kVec;
+        prefetch_l2(a + off);
+        if (b) prefetch_l2(b + off);
+    }
+}
+
 // residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
 // [kernel-span fused_add_rmsnorm_reg]
 template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
-                      const uint16_t* __restrict__ w, int64_t rows, float eps) {
+                      const uint16_t* __restrict__ w, int64_t rows, float eps, int64_t first_wave) {
     using G = Geo<H>;
     __shared__ float red[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    prefetch_first_row<G>(x, res, rows, group, t, first_wave);
     grid_dep_wait();
     grid_dep_release();
-    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     ParamVecs<G::VPT, PRE> wp(w, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
@@ -117,12 +140,13 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
 template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
-                int64_t rows, float eps) {
+                int64_t rows, float eps, int64_t first_wave) {
     using G = Geo<H>;
     __shared__ float red[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    prefetch_first_row<G>(x, nullptr, rows, group, t, first_wave);
     grid_dep_wait();
     grid_dep_release();
-    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     ParamVecs<G::VPT, PRE> wp(w, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
@@ -169,13 +193,14 @@ template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                   const uint16_t* x, const uint16_t* __restrict__ gamma,
-                  const uint16_t* __restrict__ beta, int64_t rows, float eps) {
+                  const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
     using G = Geo<H>;
     __shared__ float red1[G::RPC * G::W];
     __shared__ float red2[G::RPC * G::W];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    prefetch_first_row<G>(x, nullptr, rows, group, t, first_wave);
     grid_dep_wait();
     grid_dep_release();
-    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     ParamVecs<G::VPT, PRE> gp(gamma, G::TPR, t), bp(beta, G::TPR, t);
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
     for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
@@ -269,13 +294,14 @@ template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                     const uint16_t* x, const uint16_t* __restrict__ gamma,
-                    const uint16_t* __restrict__ beta, int64_t rows, float eps) {
+                    const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
     using G = Geo<H>;
     constexpr float kNW = 32.0f * G::VPT * kVec;  // elements per warp
     __shared__ float red[G::W > 1 ? G::RPC * G::W * 2 : 1];
+    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
+    prefetch_first_row<G>(x, nullptr, rows, group, t, first_wave);
     grid_dep_wait();
     grid_dep_release();
-    const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     ParamVecs<G::VPT, PRE> gp(gamma, G::TPR, t), bp(beta, G::TPR, t);
     const int warp = t >> 5, lane = t & 31;
     const int64_t nblk = (rows + G::RPC - 1) / G::RPC;
@@ -353,47 +379,67 @@ layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict
 
 // Which LayerNorm forward statistics the register path uses (two passes
 // over the resident row, or one shifted pass).
-constexpr bool kLnFwdShifted = false;
+constexpr bool kLnFwdShifted = true;
 
 // Calls of at most this many rows load their parameters before the first
 // row (ParamVecs with PRE).
-constexpr int64_t kPrefetchParamRows = 1024;
+constexpr int64_t kPrefetchParamRows = 256;
 
 }  // namespace
 
+// CTAs of a kernel's first wave on this device (resident per SM x SMs).
+// `slot` caches the occupancy of one kernel instantiation (a benign race at
+// worst repeats the query).
+template <typename K>
+int64_t first_wave_ctas(K kernel, int threads, int sms, int* slot) {
+    int o = *slot;
+    if (o <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, threads, 0) != cudaSuccess || o <= 0)
+            o = 1;
+        *slot = o;
+    }
+    return static_cast<int64_t>(o) * sms;
+}
+
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
-                             float eps, int grid, cudaStream_t st) {
+                             float eps, int grid, int sms, cudaStream_t st) {
     const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
-        return launch_with_pdl(pre ? fused_add_rmsnorm_reg<H, true> : fused_add_rmsnorm_reg<H, false>,
-                               dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st,
-                               static_cast<uint16_t*>(x), static_cast<uint16_t*>(res),
-                               static_cast<const uint16_t*>(w), rows, eps);
+        static int occ[2] = {0, 0};
+        const auto k = pre ? fused_add_rmsnorm_reg<H, true> : fused_add_rmsnorm_reg<H, false>;
+        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(x),
+                               static_cast<uint16_t*>(res), static_cast<const uint16_t*>(w), rows,
+                               eps, first_wave_ctas(k, threads, sms, &occ[pre]));
     })
 }
 
 cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
-                           float eps, int grid, cudaStream_t st) {
+                           float eps, int grid, int sms, cudaStream_t st) {
     const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
-        return launch_with_pdl(pre ? rmsnorm_fwd_reg<H, true> : rmsnorm_fwd_reg<H, false>, dim3(grid),
-                               dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st, static_cast<uint16_t*>(y),
+        static int occ[2] = {0, 0};
+        const auto k = pre ? rmsnorm_fwd_reg<H, true> : rmsnorm_fwd_reg<H, false>;
+        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(y),
                                static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w),
-                               rows, eps);
+                               rows, eps, first_wave_ctas(k, threads, sms, &occ[pre]));
     })
 }
 
 cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                               const void* gamma, const void* beta, int64_t rows, float eps,
-                              int grid, cudaStream_t st) {
+                              int grid, int sms, cudaStream_t st) {
     const bool pre = rows <= kPrefetchParamRows;
     NF_HIDDEN_SWITCH(hidden, {
+        static int occ[2] = {0, 0};
         const auto k = kLnFwdShifted ? (pre ? layernorm_fwd_shift<H, true> : layernorm_fwd_shift<H, false>)
                                      : (pre ? layernorm_fwd_reg<H, true> : layernorm_fwd_reg<H, false>);
-        return launch_with_pdl(k, dim3(grid), dim3(Geo<H>::TPR * Geo<H>::RPC), 0, st,
-                               static_cast<uint16_t*>(y), mean, rstd,
-                               static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
-                               static_cast<const uint16_t*>(beta), rows, eps);
+        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(y), mean,
+                               rstd, static_cast<const uint16_t*>(x),
+                               static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta),
+                               rows, eps, first_wave_ctas(k, threads, sms, &occ[pre]));
     })
 }
 

@@ -82,7 +82,11 @@ __device__ __forceinline__ int chunk_len(int c, int H) {
 }
 
 // Load this thread's vectors of chunk c of row r, widened; invalid vectors
-// are zero.  Vector k of thread t is chunk vector k * kSpT + t.
+// are zero.  Vector k of thread t is chunk vector k * kSpT + t.  KEEP asks
+// L2 to keep the lines (the statistics pass: the apply pass reads the same
+// chunk again, from L2 when the batch fits there); otherwise the load
+// streams (last use).
+template <bool KEEP = false>
 __device__ __forceinline__ void load_chunk(const uint16_t* src, int64_t r, int c, int H,
                                            float (&f)[kSpV][8]) {
     const int NV = H / kVec;
@@ -90,8 +94,22 @@ __device__ __forceinline__ void load_chunk(const uint16_t* src, int64_t r, int c
     for (int k = 0; k < kSpV; ++k) {
         const int v = c * kSpVecs + k * kSpT + threadIdx.x;
         uint4 u = make_uint4(0, 0, 0, 0);
-        if (v < NV) u = ld_stream(src + r * H + static_cast<int64_t>(v) * kVec);
+        if (v < NV) {
+            const uint16_t* p = src + r * H + static_cast<int64_t>(v) * kVec;
+            u = KEEP ? ld_keep(p) : ld_stream(p);
+        }
         unpack8(u, f[k]);
+    }
+}
+
+// Warm L2 with this thread's vectors of chunk c of row r (a hint, issued
+// before waiting for the kernel ahead in the stream).
+__device__ __forceinline__ void prefetch_chunk(const uint16_t* src, int64_t r, int c, int H) {
+    const int NV = H / kVec;
+#pragma unroll
+    for (int k = 0; k < kSpV; ++k) {
+        const int v = c * kSpVecs + k * kSpT + threadIdx.x;
+        if (v < NV) prefetch_l2(src + r * H + static_cast<int64_t>(v) * kVec);
     }
 }
 
@@ -100,15 +118,19 @@ __device__ __forceinline__ void load_chunk(const uint16_t* src, int64_t r, int c
 template <int OP>
 __global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict__ part, int nc) {
     __shared__ float red[2][8 * 1];
-    pdl_wait();
     const int c = blockIdx.x, H = a.hidden;
+    if (blockIdx.y < a.rows) {
+        prefetch_chunk(a.in0, blockIdx.y, c, H);
+        if (OP == 0) prefetch_chunk(a.in1, blockIdx.y, c, H);
+    }
+    pdl_wait();
     const int NV = H / kVec;
     for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
         float f[kSpV][8];
-        load_chunk(a.in0, r, c, H, f);
+        load_chunk<true>(a.in0, r, c, H, f);
         if constexpr (OP == 0) {
             float b[kSpV][8];
-            load_chunk(a.in1, r, c, H, b);
+            load_chunk<true>(a.in1, r, c, H, b);
 #pragma unroll
             for (int k = 0; k < kSpV; ++k)
 #pragma unroll
@@ -148,74 +170,74 @@ __global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict
         if (threadIdx.x == 0) reinterpret_cast<float2*>(part)[r * nc + c] = out;
         __syncthreads();  // red is reused by the next row
     }
+    // this CTA's partials are written: let the apply pass be scheduled (it
+    // still waits for this grid to finish before reading them)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// One CTA per row: merge the row's chunk partials -> stat[row] = (mean, rstd).
+// (mean, rstd) of row r from its nc chunk partials, merged by the whole CTA
+// in a fixed order (thread t takes chunks t, t + 256, ..., then lanes and
+// warps in a fixed tree), so every CTA that merges row r gets the same
+// bits.  Every thread returns the result; `sh` is the CTA's scratch.
 template <int OP>
-__global__ void __launch_bounds__(kSpT) split_merge_fwd(DynArgs a, const float* __restrict__ part,
-                                                        float2* __restrict__ stat, int nc) {
-    __shared__ Chan sh[kSpT / 32];
-    pdl_wait();
+__device__ __forceinline__ float2 merge_row_fwd(const DynArgs& a, const float* __restrict__ part,
+                                                int64_t r, int nc, Chan* sh) {
     const int H = a.hidden;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float2* p2 = reinterpret_cast<const float2*>(part);
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        Chan acc{0.f, 0.f, 0.f};
-        for (int c = threadIdx.x; c < nc; c += kSpT) {
-            const float2 p = __ldcg(p2 + r * nc + c);
-            if constexpr (OP == 2) {
-                acc = chan_merge(acc, Chan{static_cast<float>(chunk_len(c, H)), p.x, p.y});
-            } else {
-                acc.n = 1.f;
-                acc.m2 += p.x;  // sum of squares
-            }
+    Chan acc{0.f, 0.f, 0.f};
+    for (int c = threadIdx.x; c < nc; c += kSpT) {
+        const float2 p = __ldcg(p2 + r * nc + c);
+        if constexpr (OP == 2) {
+            acc = chan_merge(acc, Chan{static_cast<float>(chunk_len(c, H)), p.x, p.y});
+        } else {
+            acc.n = 1.f;
+            acc.m2 += p.x;  // sum of squares
         }
-        // fixed tree: lanes, then warps in order
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const Chan o{__shfl_down_sync(0xffffffffu, acc.n, off),
-                         __shfl_down_sync(0xffffffffu, acc.mean, off),
-                         __shfl_down_sync(0xffffffffu, acc.m2, off)};
-            if (lane < off) {
-                if constexpr (OP == 2) {
-                    acc = chan_merge(acc, o);
-                } else {
-                    acc.m2 += o.m2;
-                }
-            }
-        }
-        if (lane == 0) sh[warp] = acc;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            Chan t = sh[0];
-#pragma unroll
-            for (int w = 1; w < kSpT / 32; ++w) {
-                if constexpr (OP == 2) {
-                    t = chan_merge(t, sh[w]);
-                } else {
-                    t.m2 += sh[w].m2;
-                }
-            }
-            const float invH = 1.0f / static_cast<float>(H);
-            const float rstd = rsqrtf(t.m2 * invH + a.eps);
-            const float mean = OP == 2 ? t.mean : 0.f;
-            stat[r] = make_float2(mean, rstd);
-            if (OP == 2) {
-                if (a.mean) a.mean[r] = mean;
-                if (a.rstd) a.rstd[r] = rstd;
-            }
-        }
-        __syncthreads();  // sh is reused by the next row
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const Chan o{__shfl_down_sync(0xffffffffu, acc.n, off),
+                     __shfl_down_sync(0xffffffffu, acc.mean, off),
+                     __shfl_down_sync(0xffffffffu, acc.m2, off)};
+        if (lane < off) {
+            if constexpr (OP == 2) {
+                acc = chan_merge(acc, o);
+            } else {
+                acc.m2 += o.m2;
+            }
+        }
+    }
+    if (lane == 0) sh[warp] = acc;
+    __syncthreads();
+    Chan t = sh[0];
+#pragma unroll
+    for (int w = 1; w < kSpT / 32; ++w) {
+        if constexpr (OP == 2) {
+            t = chan_merge(t, sh[w]);
+        } else {
+            t.m2 += sh[w].m2;
+        }
+    }
+    __syncthreads();  // sh is reused by the next row
+    const float rstd = rsqrtf(t.m2 * (1.0f / static_cast<float>(H)) + a.eps);
+    return make_float2(OP == 2 ? t.mean : 0.f, rstd);
 }
 
+// The apply pass merges its row's chunk partials itself (every CTA of the
+// row does the same fixed-order merge), so the forward is two launches.
 template <int OP>
-__global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float2* __restrict__ stat) {
-    pdl_wait();
+__global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float* __restrict__ part,
+                                                        int nc) {
+    __shared__ Chan sh[kSpT / 32];
     const int c = blockIdx.x, H = a.hidden;
+    if (blockIdx.y < a.rows) {
+        prefetch_chunk(a.in0, blockIdx.y, c, H);
+        if (OP == 0) prefetch_chunk(a.in1, blockIdx.y, c, H);
+    }
+    pdl_wait();
     const int NV = H / kVec;
     for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
-        const float2 st = __ldcg(stat + r);
         float f[kSpV][8];
         load_chunk(a.in0, r, c, H, f);
         if constexpr (OP == 0) {
@@ -225,6 +247,11 @@ __global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float2*
             for (int k = 0; k < kSpV; ++k)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[k][e] += b[k][e];
+        }
+        const float2 st = merge_row_fwd<OP>(a, part, r, nc, sh);
+        if (OP == 2 && c == 0 && threadIdx.x == 0) {
+            if (a.mean) a.mean[r] = st.x;
+            if (a.rstd) a.rstd[r] = st.y;
         }
 #pragma unroll
         for (int k = 0; k < kSpV; ++k) {
@@ -254,13 +281,17 @@ __global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float2*
 template <int OP>
 __global__ void __launch_bounds__(kSpT) split_stats_bwd(DynArgs a, float* __restrict__ part, int nc) {
     __shared__ float red[8 * 2];
-    pdl_wait();
     const int c = blockIdx.x, H = a.hidden;
+    if (blockIdx.y < a.rows) {
+        prefetch_chunk(a.in0, blockIdx.y, c, H);
+        prefetch_chunk(a.in1, blockIdx.y, c, H);
+    }
+    pdl_wait();
     const int NV = H / kVec;
     for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
         float x[kSpV][8], dy[kSpV][8];
-        load_chunk(a.in0, r, c, H, x);
-        load_chunk(a.in1, r, c, H, dy);
+        load_chunk<true>(a.in0, r, c, H, x);
+        load_chunk<true>(a.in1, r, c, H, dy);
         const float mu = OP == 3 ? __ldg(a.mean + r) : 0.f;
         const float rs = OP == 3 ? __ldg(a.rstd + r) : 0.f;
         float s[2] = {0.f, 0.f};
@@ -286,6 +317,7 @@ __global__ void __launch_bounds__(kSpT) split_stats_bwd(DynArgs a, float* __rest
         if (threadIdx.x == 0) reinterpret_cast<float2*>(part)[r * nc + c] = make_float2(s[0], s[1]);
         __syncthreads();
     }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One CTA per row: stat[row] = LN (A, B) = (sum g / H, sum g xhat / H);
@@ -317,16 +349,86 @@ __global__ void __launch_bounds__(kSpT) split_merge_bwd(DynArgs a, const float* 
     }
 }
 
-// Grid (chunks, row blocks): dx for the block's rows, and the block's column
-// sums of its chunk -> ws[block][plane][H].
+constexpr int kSpMergeRows = kSplitMergeRows;
+
+// The per-row statistics of rows [r0, r0 + nrow) (nrow <= kSpMergeRows) from
+// their chunk partials, into sh_stat[0 .. nrow): thread t adds chunks t,
+// t + 256, ... of every row (all loads issued together), then lanes and
+// warps are added in a fixed order, so every CTA of the row block gets the
+// same bits.  LN: (A, B) = (sum g / H, sum g xhat / H); RMS: (rstd,
+// rstd^3 * sum g x / H).
 template <int OP>
-__global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2* __restrict__ stat) {
+__device__ __forceinline__ void merge_rows_bwd(const DynArgs& a, const float* __restrict__ part,
+                                               int64_t r0, int nrow, int nc, float2* sh_stat,
+                                               float* red) {
+    const float2* p2 = reinterpret_cast<const float2*>(part);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float2 acc[kSpMergeRows];
+#pragma unroll
+    for (int i = 0; i < kSpMergeRows; ++i) acc[i] = make_float2(0.f, 0.f);
+    for (int c = threadIdx.x; c < nc; c += kSpT) {
+#pragma unroll
+        for (int i = 0; i < kSpMergeRows; ++i) {
+            if (i < nrow) {
+                const float2 p = __ldcg(p2 + (r0 + i) * nc + c);
+                acc[i].x += p.x;
+                acc[i].y += p.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kSpMergeRows; ++i) {
+        if (i < nrow) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                acc[i].x += __shfl_xor_sync(0xFFFFFFFFu, acc[i].x, off);
+                acc[i].y += __shfl_xor_sync(0xFFFFFFFFu, acc[i].y, off);
+            }
+            if (lane == 0) {
+                red[(warp * kSpMergeRows + i) * 2] = acc[i].x;
+                red[(warp * kSpMergeRows + i) * 2 + 1] = acc[i].y;
+            }
+        }
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < nrow) {
+        const int i = threadIdx.x;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSpT / 32; ++w) {
+            s0 += red[(w * kSpMergeRows + i) * 2];
+            s1 += red[(w * kSpMergeRows + i) * 2 + 1];
+        }
+        const float invH = 1.0f / static_cast<float>(a.hidden);
+        if constexpr (OP == 3) {
+            sh_stat[i] = make_float2(s0 * invH, s1 * invH);
+        } else {
+            const float rs = rsqrtf(s0 * invH + a.eps);
+            sh_stat[i] = make_float2(rs, rs * rs * rs * s1 * invH);
+        }
+    }
+    __syncthreads();
+}
+
+// Grid (chunks, row blocks): dx for the block's rows, and the block's column
+// sums of its chunk -> ws[block][plane][H].  With `stat` null the block
+// (at most kSpMergeRows rows) merges its rows' partials itself.
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2* __restrict__ stat,
+                                                        const float* __restrict__ part, int nc) {
     constexpr int NP = OP == 3 ? 2 : 1;
-    pdl_wait();
+    __shared__ float2 sh_stat[kSpMergeRows];
+    __shared__ float red[(kSpT / 32) * kSpMergeRows * 2];
     const int c = blockIdx.x, H = a.hidden;
     const int NV = H / kVec;
     const int64_t nb = gridDim.y;
     const int64_t r0 = a.rows * blockIdx.y / nb, r1 = a.rows * (blockIdx.y + 1) / nb;
+    if (r0 < r1) {
+        prefetch_chunk(a.in0, r0, c, H);
+        prefetch_chunk(a.in1, r0, c, H);
+    }
+    pdl_wait();
+    if (!stat) merge_rows_bwd<OP>(a, part, r0, static_cast<int>(r1 - r0), nc, sh_stat, red);
     float acc0[kSpV][8], acc1[NP == 2 ? kSpV : 1][8];
 #pragma unroll
     for (int k = 0; k < kSpV; ++k)
@@ -336,7 +438,7 @@ __global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2*
             if constexpr (NP == 2) acc1[k][e] = 0.f;
         }
     for (int64_t r = r0; r < r1; ++r) {
-        const float2 st = __ldcg(stat + r);
+        const float2 st = stat ? __ldcg(stat + r) : sh_stat[r - r0];
         float x[kSpV][8], dy[kSpV][8];
         load_chunk(a.in0, r, c, H, x);
         load_chunk(a.in1, r, c, H, dy);
@@ -431,11 +533,10 @@ cudaError_t fwd_t(const DynArgs& a, char* ws, int sms, cudaStream_t st) {
     float2* stat = reinterpret_cast<float2*>(ws + l.cols + l.part);
     const unsigned gy = static_cast<unsigned>(a.rows < kSpMaxGridY ? a.rows : kSpMaxGridY);
     const unsigned gr = static_cast<unsigned>(a.rows < 0x7FFFFFFF ? a.rows : 0x7FFFFFFF);
+    (void)stat;
+    (void)gr;
     if (cudaError_t e = launch_pdl(split_stats<OP>, dim3(nc, gy), st, a, part, nc)) return e;
-    if (cudaError_t e = launch_pdl(split_merge_fwd<OP>, dim3(gr), st, a,
-                                   static_cast<const float*>(part), stat, nc))
-        return e;
-    return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float2*>(stat));
+    return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float*>(part), nc);
 }
 
 template <int OP>
@@ -449,10 +550,16 @@ cudaError_t bwd_t(DynArgs a, char* ws, int sms, cudaStream_t st) {
     const unsigned gy = static_cast<unsigned>(a.rows < kSpMaxGridY ? a.rows : kSpMaxGridY);
     const unsigned gr = static_cast<unsigned>(a.rows < 0x7FFFFFFF ? a.rows : 0x7FFFFFFF);
     if (cudaError_t e = launch_pdl(split_stats_bwd<OP>, dim3(nc, gy), st, a, part, nc)) return e;
-    if (cudaError_t e = launch_pdl(split_merge_bwd<OP>, dim3(gr), st, a,
-                                   static_cast<const float*>(part), stat, nc))
-        return e;
-    return launch_pdl(split_apply_bwd<OP>, dim3(nc, rb), st, a, static_cast<const float2*>(stat));
+    // row blocks short enough merge their rows' statistics themselves
+    const bool merge_in_apply = (a.rows + rb - 1) / rb <= kSpMergeRows;
+    if (!merge_in_apply) {
+        if (cudaError_t e = launch_pdl(split_merge_bwd<OP>, dim3(gr), st, a,
+                                       static_cast<const float*>(part), stat, nc))
+            return e;
+    }
+    return launch_pdl(split_apply_bwd<OP>, dim3(nc, rb), st, a,
+                      merge_in_apply ? static_cast<const float2*>(nullptr) : static_cast<const float2*>(stat),
+                      static_cast<const float*>(part), nc);
 }
 
 }  // namespace

@@ -21,13 +21,15 @@ bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);
 bool bulk_shape(int op, int64_t hidden, int* threads, int* stages, int* smem_bytes, int* groups);
 
 // Register path (rows resident in registers).
+// `sms` bounds the first wave of CTAs, which warm L2 with their first row
+// before waiting for the kernel ahead in the stream.
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
-                             float eps, int grid, cudaStream_t st);
+                             float eps, int grid, int sms, cudaStream_t st);
 cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
-                           float eps, int grid, cudaStream_t st);
+                           float eps, int grid, int sms, cudaStream_t st);
 cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                               const void* gamma, const void* beta, int64_t rows, float eps,
-                              int grid, cudaStream_t st);
+                              int grid, int sms, cudaStream_t st);
 
 // Cluster path (one row split across a cluster of CTAs).
 cudaError_t launch_fused_cluster(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
@@ -121,6 +123,9 @@ cudaError_t launch_long(int op, const DynArgs& a, int grid, cudaStream_t st);
 // Split rows (grid-parallel inner normalization across any number of CTAs):
 // chunks of 8192 elements, partial statistics through the workspace.
 constexpr int64_t kSplitMaxHidden = 1LL << 26;
+// Backward row blocks of at most this many rows merge their rows' statistics
+// inside the apply pass instead of in a separate launch.
+constexpr int kSplitMergeRows = 16;
 bool split_shape(int op, int64_t rows, int64_t hidden, int sms, int* nchunks, int* rblocks);
 size_t split_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms);
 cudaError_t launch_split(int op, const DynArgs& a, void* workspace, int sms, cudaStream_t st);

@@ -17,6 +17,9 @@ FORCED = ((5, 8), (300, 1000), (33, 8200), (7, 20000))   # (rows, hidden); 8200 
 AUTO_FWD = ((2, 262152), (1, 1 << 20))
 AUTO_BWD = ((3, 131080), (2, 1 << 20), (2, 1 << 22))   # the last: one row block (no column reduction)
 ONE_BLOCK = ((1, 8200),)                                 # forced, one row: one row block
+# forced, more than 16 rows per row block: the row statistics go through the
+# separate merge launch instead of being merged inside the apply pass
+MANY_ROWS = ((5000, 8200),)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -69,7 +72,7 @@ def test_split_layernorm_fwd(rows, hidden):
     check_f32(rstd, r_ref, f"split ln rstd {rows}x{hidden}", rtol=1e-4)
 
 
-@pytest.mark.parametrize("rows,hidden", FORCED + ONE_BLOCK + AUTO_BWD)
+@pytest.mark.parametrize("rows,hidden", FORCED + ONE_BLOCK + MANY_ROWS + AUTO_BWD)
 def test_split_layernorm_bwd(rows, hidden):
     x, dy, g = workloads.layernorm_bwd_inputs(rows, hidden, seed=rows + hidden)
     _, m, r = oracle.layernorm_fwd(x, np.ones(hidden), np.zeros(hidden), 1e-5)
@@ -86,7 +89,7 @@ def test_split_layernorm_bwd(rows, hidden):
     assert torch.equal(dx, dx2) and torch.equal(dg, dg2) and torch.equal(db, db2)
 
 
-@pytest.mark.parametrize("rows,hidden", FORCED + ONE_BLOCK + AUTO_BWD)
+@pytest.mark.parametrize("rows,hidden", FORCED + ONE_BLOCK + MANY_ROWS + AUTO_BWD)
 @pytest.mark.parametrize("fused", (False, True))
 def test_split_rmsnorm_bwd(rows, hidden, fused):
     if fused:
