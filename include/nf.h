@@ -8,12 +8,12 @@
  *     scheduler for static fusion" (NVIDIA/Fuser PR #5281), changes
  *     walkthrough, test_rmsnorm_add_fwd.py entry.
  *   - RMSNorm forward and LayerNorm forward: "TMA inner persistent
- *     scheduler" (NVIDIA/Fuser PR #5587), description ("RMS norm and layer
- *     norm implementations with workspace support").
+ *     scheduler" (NVIDIA/Fuser PR #5587), description (RMS norm and layer
+ *     norm, with a workspace).
  *   - LayerNorm backward as a combined per-row (inner) and across-rows
  *     (outer) reduction: "Llu/ln bwd" (NVIDIA/Fuser PR #207), title and the
- *     discussion of "grid-parallel inner-and-outer normalization (special
- *     case for layernorm backward)".
+ *     discussion, which names the layer norm backward as the special case of
+ *     a grid-parallel normalization reducing both within and across rows.
  *   - The other variants that discussion lists: grid-parallel inner
  *     normalization (rows longer than one CTA: the cluster and split
  *     families) and outer normalization (nf_outer_norm_*); and the
@@ -236,7 +236,7 @@ size_t nf_rmsnorm_bwd_workspace_size(int64_t rows, int64_t hidden);
 
 /* RMSNorm backward (the RMS counterpart of the combined inner + outer
  * reduction of "Llu/ln bwd"; "TMA inner persistent scheduler": RMS norm
- * "with workspace support").  For y = x * rstd * w with
+ * with a workspace).  For y = x * rstd * w with
  * rstd = rsqrt(mean_k(x_k^2) + eps), g = dy * w and xhat = x * rstd:
  *   inner (per row):    dx[r][j] = bf16( rstd * ( g_j - xhat_j * mean_k(g_k * xhat_k) ) )
  *   outer (per column): dw[j]    = sum_r dy[r][j] * xhat[r][j]          (fp32, overwritten)

@@ -22,7 +22,7 @@ Operations and where the pages name them:
                         backward, a combined inner + outer reduction.
   rmsnorm_bwd        -- the RMS norm counterpart of the same combined
                         reduction ("TMA inner persistent scheduler",
-                        description: RMS norm with workspace support).
+                        description: RMS norm, with a workspace).
   outer_norm_fwd,
   outer_norm_bwd     -- outer normalization (statistics per column, over the
                         rows), listed among the normalization variants in

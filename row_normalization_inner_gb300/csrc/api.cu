@@ -322,7 +322,9 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.rows_per_cta = 1;
         if (fwd) {
             pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * ry);
-            pl.launches = 2;  // statistics, then apply (which merges its row's partials)
+            // statistics, then apply (RMSNorm and the fused op merge their row's
+            // partials there; LayerNorm has a merge launch between)
+            pl.launches = op == NF_OP_LAYERNORM_FWD ? 3 : 2;
         } else {
             pl.grid = static_cast<int32_t>(static_cast<int64_t>(nc) * rb);
             // statistics, a merge launch unless the row blocks are short

@@ -1,8 +1,9 @@
-// LayerNorm backward: the combined inner + outer reduction ("Llu/ln bwd",
-// NVIDIA/Fuser PR #207: "grid-parallel inner-and-outer normalization
-// (special case for layernorm backward)"), with the cross-CTA partials kept
-// in a workspace ("TMA inner persistent scheduler": "with workspace
-// support").
+// LayerNorm backward: the combined inner + outer reduction of "Llu/ln bwd"
+// (NVIDIA/Fuser PR #207, whose discussion treats the layer norm backward as
+// the special case of a grid-parallel normalization that reduces both
+// within rows and across them), with the cross-CTA partials kept in a
+// workspace (the workspace support of "TMA inner persistent scheduler",
+// description).
 //
 // Stage 1 (register path): `grid` persistent CTAs of RPC row groups.  Row
 // group `slot` owns the contiguous row stripe

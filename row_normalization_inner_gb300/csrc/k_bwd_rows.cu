@@ -2,10 +2,10 @@
 // LayerNorm backward, the RMSNorm backward and the fused residual-add
 // RMSNorm backward, with the combined inner (per-row dx) and outer
 // (across-rows dgamma / dbeta or dw) reductions of "Llu/ln bwd" (NVIDIA/Fuser
-// PR #207, discussion: grid-parallel inner-and-outer normalization for the
-// layer norm backward) and the column partials kept in a workspace ("TMA
-// inner persistent scheduler", NVIDIA/Fuser PR #5587, description: RMS norm
-// and layer norm with workspace support).
+// PR #207, discussion of the layer norm backward as a normalization that
+// reduces within rows and across them) and the column partials kept in a
+// workspace ("TMA inner persistent scheduler", NVIDIA/Fuser PR #5587,
+// description: the RMS norm and layer norm workspace support).
 //
 // Layout.  One persistent CTA per SM owns a contiguous stripe of rows and
 // cuts it into blocks of R consecutive rows.  The CTA's threads form NG

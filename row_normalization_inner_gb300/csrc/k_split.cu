@@ -175,6 +175,68 @@ __global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// LayerNorm forward: one CTA per row merges the row's chunk partials ->
+// stat[row] = (mean, rstd) (Chan's pairwise update in a fixed order).  A
+// separate launch measured faster for LayerNorm than every apply CTA
+// repeating the Chan merge; RMSNorm merges inside the apply pass.
+template <int OP>
+__global__ void __launch_bounds__(kSpT) split_merge_fwd(DynArgs a, const float* __restrict__ part,
+                                                        float2* __restrict__ stat, int nc) {
+    __shared__ Chan sh[kSpT / 32];
+    pdl_wait();
+    const int H = a.hidden;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float2* p2 = reinterpret_cast<const float2*>(part);
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        Chan acc{0.f, 0.f, 0.f};
+        for (int c = threadIdx.x; c < nc; c += kSpT) {
+            const float2 p = __ldcg(p2 + r * nc + c);
+            if constexpr (OP == 2) {
+                acc = chan_merge(acc, Chan{static_cast<float>(chunk_len(c, H)), p.x, p.y});
+            } else {
+                acc.n = 1.f;
+                acc.m2 += p.x;  // sum of squares
+            }
+        }
+        // fixed tree: lanes, then warps in order
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const Chan o{__shfl_down_sync(0xffffffffu, acc.n, off),
+                         __shfl_down_sync(0xffffffffu, acc.mean, off),
+                         __shfl_down_sync(0xffffffffu, acc.m2, off)};
+            if (lane < off) {
+                if constexpr (OP == 2) {
+                    acc = chan_merge(acc, o);
+                } else {
+                    acc.m2 += o.m2;
+                }
+            }
+        }
+        if (lane == 0) sh[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            Chan t = sh[0];
+#pragma unroll
+            for (int w = 1; w < kSpT / 32; ++w) {
+                if constexpr (OP == 2) {
+                    t = chan_merge(t, sh[w]);
+                } else {
+                    t.m2 += sh[w].m2;
+                }
+            }
+            const float invH = 1.0f / static_cast<float>(H);
+            const float rstd = rsqrtf(t.m2 * invH + a.eps);
+            const float mean = OP == 2 ? t.mean : 0.f;
+            stat[r] = make_float2(mean, rstd);
+            if (OP == 2) {
+                if (a.mean) a.mean[r] = mean;
+                if (a.rstd) a.rstd[r] = rstd;
+            }
+        }
+        __syncthreads();  // sh is reused by the next row
+    }
+}
+
 // (mean, rstd) of row r from its nc chunk partials, merged by the whole CTA
 // in a fixed order (thread t takes chunks t, t + 256, ..., then lanes and
 // warps in a fixed tree), so every CTA that merges row r gets the same
@@ -224,11 +286,12 @@ __device__ __forceinline__ float2 merge_row_fwd(const DynArgs& a, const float* _
     return make_float2(OP == 2 ? t.mean : 0.f, rstd);
 }
 
-// The apply pass merges its row's chunk partials itself (every CTA of the
-// row does the same fixed-order merge), so the forward is two launches.
+// Apply pass.  RMSNorm (and the fused op) merge their row's chunk partials
+// here (every CTA of the row does the same fixed-order merge), so their
+// forward is two launches; LayerNorm reads `stat` from the merge launch.
 template <int OP>
 __global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float* __restrict__ part,
-                                                        int nc) {
+                                                        const float2* __restrict__ stat, int nc) {
     __shared__ Chan sh[kSpT / 32];
     const int c = blockIdx.x, H = a.hidden;
     if (blockIdx.y < a.rows) {
@@ -248,11 +311,7 @@ __global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float* 
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[k][e] += b[k][e];
         }
-        const float2 st = merge_row_fwd<OP>(a, part, r, nc, sh);
-        if (OP == 2 && c == 0 && threadIdx.x == 0) {
-            if (a.mean) a.mean[r] = st.x;
-            if (a.rstd) a.rstd[r] = st.y;
-        }
+        const float2 st = stat ? __ldcg(stat + r) : merge_row_fwd<OP>(a, part, r, nc, sh);
 #pragma unroll
         for (int k = 0; k < kSpV; ++k) {
             const int v = c * kSpVecs + k * kSpT + threadIdx.x;
@@ -533,10 +592,16 @@ cudaError_t fwd_t(const DynArgs& a, char* ws, int sms, cudaStream_t st) {
     float2* stat = reinterpret_cast<float2*>(ws + l.cols + l.part);
     const unsigned gy = static_cast<unsigned>(a.rows < kSpMaxGridY ? a.rows : kSpMaxGridY);
     const unsigned gr = static_cast<unsigned>(a.rows < 0x7FFFFFFF ? a.rows : 0x7FFFFFFF);
-    (void)stat;
-    (void)gr;
     if (cudaError_t e = launch_pdl(split_stats<OP>, dim3(nc, gy), st, a, part, nc)) return e;
-    return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float*>(part), nc);
+    if constexpr (OP == 2) {
+        if (cudaError_t e = launch_pdl(split_merge_fwd<OP>, dim3(gr), st, a,
+                                       static_cast<const float*>(part), stat, nc))
+            return e;
+        return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float*>(part),
+                          static_cast<const float2*>(stat), nc);
+    }
+    return launch_pdl(split_apply_fwd<OP>, dim3(nc, gy), st, a, static_cast<const float*>(part),
+                      static_cast<const float2*>(nullptr), nc);
 }
 
 template <int OP>
