@@ -55,11 +55,12 @@ int bwd_ctas_per_sm(int64_t hidden) {
 // graphs of back-to-back launches over L2-cold inputs, every op x size x
 // path):
 //  - forward ops: the register path is fastest at every row count, from 1
-//    row (about 2-3 us per launch, where a cluster split only adds its
-//    barrier latency) to 65536 rows (1.0x the measured copy bandwidth);
-//    the exceptions are hidden 12288 RMSNorm / LayerNorm forward from 1024
-//    rows and hidden 8192 LayerNorm forward from 16384 rows, where the bulk
-//    ring keeps more bytes in flight than the register-resident rows can;
+//    row (1.4-2.3 us per launch, where a cluster split only adds its
+//    barrier latency: 2.8-3.1 us) to 65536 rows (1.0x the measured copy
+//    bandwidth; LayerNorm 16384 x 8192: 0.98 against 0.88 for the bulk
+//    ring); the exception is hidden 12288 RMSNorm / LayerNorm forward from
+//    1024 rows, where the bulk ring keeps more bytes in flight than the
+//    register-resident rows can (LayerNorm 16384 x 12288: 0.96 against 0.72);
 //  - backward ops: the bulk path, at every size (its row groups fold their
 //    column partials inside the CTA, so stage 2 stays small).
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
@@ -71,7 +72,6 @@ nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
     if (hidden >= 12288 && rows >= 1024 &&
         (op == NF_OP_RMSNORM_FWD || op == NF_OP_LAYERNORM_FWD))
         return NF_PATH_BULK;
-    if (hidden == 8192 && rows >= 16384 && op == NF_OP_LAYERNORM_FWD) return NF_PATH_BULK;
     return NF_PATH_REG;
 }
 

@@ -216,7 +216,7 @@ rmsnorm_bwd_reg(uint16_t* dx, float* __restrict__ ws, const uint16_t* dy, const 
 // out1[j] = sum_{slot} ws[slot][1][j], in a fixed order.  Each float4
 // column gets Y slot lanes of one warp (Y = 16 or 32, so a warp covers
 // 32 / Y columns): lane ly sums slots ly, ly + Y, ly + 2Y, ... in that
-// order, issuing four loads before it adds them, and the Y lane sums are
+// order, issuing up to eight loads before it adds them, and the Y lane sums are
 // combined by a shuffle butterfly.  Every butterfly step adds the same two
 // values on both partner lanes, so all Y lanes end with the same bits and
 // the result does not depend on the launch.  No shared memory and no CTA
@@ -245,20 +245,23 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     const float4* src = reinterpret_cast<const float4*>(ws) + (ok ? c4 : 0);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ok) {
-        int p = ly;
-        for (; p + 3 * Y < nslots; p += 4 * Y) {
-            const float4 v0 = __ldcs(src + static_cast<int64_t>(p) * total4);
-            const float4 v1 = __ldcs(src + static_cast<int64_t>(p + Y) * total4);
-            const float4 v2 = __ldcs(src + static_cast<int64_t>(p + 2 * Y) * total4);
-            const float4 v3 = __ldcs(src + static_cast<int64_t>(p + 3 * Y) * total4);
-            s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
-            s.x += v1.x; s.y += v1.y; s.z += v1.z; s.w += v1.w;
-            s.x += v2.x; s.y += v2.y; s.z += v2.z; s.w += v2.w;
-            s.x += v3.x; s.y += v3.y; s.z += v3.z; s.w += v3.w;
-        }
-        for (; p < nslots; p += Y) {
-            const float4 v = __ldcs(src + static_cast<int64_t>(p) * total4);
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        // up to kColU slots per lane are loaded before any is added, so a
+        // lane waits for one L2 round trip per kColU slots (152 slots: one)
+        constexpr int kColU = 8;
+        for (int p0 = ly; p0 < nslots; p0 += kColU * Y) {
+            float4 v[kColU];
+#pragma unroll
+            for (int u = 0; u < kColU; ++u) {
+                const int p = p0 + u * Y;
+                v[u] = p < nslots ? __ldcs(src + static_cast<int64_t>(p) * total4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kColU; ++u) {
+                if (p0 + u * Y < nslots) {
+                    s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+                }
+            }
         }
     }
 #pragma unroll

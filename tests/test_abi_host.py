@@ -284,10 +284,8 @@ def test_forward_plans(hidden, rows):
         st, auto = nf.nf_plan_compute(op, rows, hidden, sms)
         assert st == nf.NF_OK
         # the measured rule: register path, but the bulk ring for hidden 12288
-        # RMSNorm / LayerNorm forward from 1024 rows and hidden 8192
-        # LayerNorm forward from 16384 rows
-        bulk = (hidden >= 12288 and rows >= 1024 and op in ("rmsnorm_fwd", "layernorm_fwd")) or \
-               (hidden == 8192 and rows >= 16384 and op == "layernorm_fwd")
+        # RMSNorm / LayerNorm forward from 1024 rows
+        bulk = hidden >= 12288 and rows >= 1024 and op in ("rmsnorm_fwd", "layernorm_fwd")
         assert auto["path"] == ("bulk" if bulk else "reg")
 
 
