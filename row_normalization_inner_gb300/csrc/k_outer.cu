@@ -73,9 +73,22 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // registers are held by the loads.  A thread only reads what it copied, so
 // cp.async.wait_group is the only synchronization.  Layout
 // [stage][array][row][thread] keeps a warp's 16-byte reads conflict-free.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem)
-                 : "memory");
+// 16-byte copy with an L2 eviction-priority policy: the statistics passes
+// ask L2 to keep x (and dy), which their apply pass reads again; the apply
+// passes mark them evict-first (their last use).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 ::"r"(smem_addr(smem)), "l"(gmem), "l"(pol) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_keep() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_last_use() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -87,6 +100,7 @@ struct RowRing {
     uint4* base;
     int64_t row0;  // this thread's first row; its rows are row0 + i * OY
     int cnt;       // number of rows of this thread
+    uint64_t pol;  // L2 policy of the copies
     __device__ __forceinline__ uint4* at(int st, int a, int u) const {
         return base + (((st % S) * A + a) * U + u) * kOT + threadIdx.x;
     }
@@ -99,7 +113,8 @@ struct RowRing {
             if (i < cnt) {
 #pragma unroll
                 for (int a = 0; a < A; ++a)
-                    cp_async16(at(st, a, u), src[a] + (row0 + static_cast<int64_t>(i) * OY) * hidden + c0);
+                    cp_async16(at(st, a, u), src[a] + (row0 + static_cast<int64_t>(i) * OY) * hidden + c0,
+                               pol);
             }
         }
         cp_commit();
@@ -143,14 +158,16 @@ constexpr int kBwdCtasPerSm = 2;
 // (float2).  Grid: (column tiles, stripes).
 template <int OX>
 __global__ void __launch_bounds__(kOT, kFwdCtasPerSm)
-outer_stats(const uint16_t* __restrict__ x, float2* __restrict__ part, Stripes sp, int hidden) {
+outer_stats(const uint16_t* __restrict__ x, float2* __restrict__ part, Stripes sp, int hidden,
+            int col0, int col1) {
     constexpr int OY = kOT / OX;
     extern __shared__ __align__(16) uint4 dsm[];
     pdl_wait();
     const int tx = threadIdx.x % OX, ty = threadIdx.x / OX, stripe = blockIdx.y;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
-    const bool ok = c0 < hidden;
-    const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0};
+    const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
+    const bool ok = c0 < col1;
+    const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0,
+                           policy_keep()};
     const uint16_t* const src[1] = {x};
     float2 nk[4], s1[4], s2[4];  // nk = -shift
 #pragma unroll
@@ -215,14 +232,16 @@ outer_stats(const uint16_t* __restrict__ x, float2* __restrict__ part, Stripes s
 // Forward pass 2: y = x * a + b with (a, b) = coef[0][j], coef[1][j].
 template <int OX>
 __global__ void __launch_bounds__(kOT, kFwdCtasPerSm)
-outer_apply(uint16_t* y, const uint16_t* x, const float* __restrict__ coef, Stripes sp, int hidden) {
+outer_apply(uint16_t* y, const uint16_t* x, const float* __restrict__ coef, Stripes sp, int hidden,
+            int col0, int col1) {
     constexpr int OY = kOT / OX;
     extern __shared__ __align__(16) uint4 dsm[];
     pdl_wait();
     const int tx = threadIdx.x % OX, ty = threadIdx.x / OX, stripe = blockIdx.y;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
-    if (c0 >= hidden) return;
-    const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty)};
+    const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
+    if (c0 >= col1) return;
+    const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty),
+                           policy_last_use()};
     const uint16_t* const src[1] = {x};
     ring.prologue(src, hidden, c0);
     float2 a[4], b[4];
@@ -252,14 +271,15 @@ template <int OX>
 __global__ void __launch_bounds__(kOT, kBwdCtasPerSm)
 outer_bwd_sums(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
                const float* __restrict__ mean, const float* __restrict__ rstd,
-               float* __restrict__ ws, Stripes sp, int hidden) {
+               float* __restrict__ ws, Stripes sp, int hidden, int col0, int col1) {
     constexpr int OY = kOT / OX;
     extern __shared__ __align__(16) uint4 dsm[];
     pdl_wait();
     const int tx = threadIdx.x % OX, ty = threadIdx.x / OX, stripe = blockIdx.y;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
-    const bool ok = c0 < hidden;
-    const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0};
+    const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
+    const bool ok = c0 < col1;
+    const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0,
+                           policy_keep()};
     const uint16_t* const src[2] = {x, dy};
     ring.prologue(src, hidden, c0);
     float2 sg[4], sb[4], nmu[4], rs[4];
@@ -325,14 +345,15 @@ __global__ void __launch_bounds__(kOT, kBwdCtasPerSm)
 outer_bwd_apply(uint16_t* dx, const uint16_t* dy, const uint16_t* x, const float* __restrict__ mean,
                 const float* __restrict__ rstd, const uint16_t* __restrict__ gamma,
                 const float* __restrict__ dgamma, const float* __restrict__ dbeta, float invR,
-                Stripes sp, int hidden) {
+                Stripes sp, int hidden, int col0, int col1) {
     constexpr int OY = kOT / OX;
     extern __shared__ __align__(16) uint4 dsm[];
     pdl_wait();
     const int tx = threadIdx.x % OX, ty = threadIdx.x / OX, stripe = blockIdx.y;
-    const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
-    if (c0 >= hidden) return;
-    const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty)};
+    const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
+    if (c0 >= col1) return;
+    const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty),
+                           policy_last_use()};
     const uint16_t* const src[2] = {x, dy};
     ring.prologue(src, hidden, c0);
     float2 nmu[4], c1[4], nk2[4], nk3[4];  // -mean, c1, -k2, -k3
@@ -505,60 +526,32 @@ cudaError_t ensure_smem_attrs() {
 static_assert(sizeof(Chan) * kOT * kVec <= kFwdBytes, "stats epilogue fits the ring");
 static_assert(sizeof(float4) * kOT * 4 <= kBwdBytes, "sums epilogue fits the ring");
 
-template <int OX>
-cudaError_t fwd_t(void* y, float* mean, float* rstd, const void* x, const void* gamma,
-                  const void* beta, int64_t rows, int64_t hidden, float eps, void* workspace,
-                  int stripes, cudaStream_t st) {
-    const Stripes sp = make_stripes(rows, stripes);
-    float2* part = static_cast<float2*>(workspace);
-    float* coef = reinterpret_cast<float*>(part + static_cast<int64_t>(stripes) * hidden);
-    const int h = static_cast<int>(hidden);
-    const dim3 grid(static_cast<unsigned>((hidden + OX * kVec - 1) / (OX * kVec)), stripes);
-    if (cudaError_t e = launch_pdl(outer_stats<OX>, grid, dim3(kOT), kFwdBytes, st,
-                                   static_cast<const uint16_t*>(x), part, sp, h))
-        return e;
-    if (cudaError_t e = launch_pdl(outer_finalize, dim3(static_cast<unsigned>((hidden + kMW - 1) / kMW)),
-                                   dim3(kMW * 32), 0, st, static_cast<const float2*>(part),
-                                   static_cast<const uint16_t*>(gamma),
-                                   static_cast<const uint16_t*>(beta), mean, rstd, coef, rows, h, 0,
-                                   h, stripes, sp, eps))
-        return e;
-    return launch_pdl(outer_apply<OX>, grid, dim3(kOT), kFwdBytes, st, static_cast<uint16_t*>(y),
-                      static_cast<const uint16_t*>(x), static_cast<const float*>(coef), sp, h);
+// Column chunks.  The statistics pass of a chunk streams its input with an
+// L2 evict-last hint and the chunk's apply pass reads it again right after
+// (evict-first), so a chunk whose input (x, or x and dy) is at most
+// kOuterChunkBytes is read from DRAM once: the second read comes from the
+// 129 MB L2.  Chunks are whole column tiles (1024 columns, or 256 below
+// that); rows too long for a 256-column chunk to fit are walked in one pass
+// over all columns, reading the input twice.
+constexpr int64_t kOuterChunkBytes = 64LL << 20;
+
+int64_t outer_chunk_cols(int64_t rows, int64_t hidden, int tensors) {
+    const int64_t per_col = (rows > 0 ? rows : 1) * 2 * tensors;
+    int64_t cw = kOuterChunkBytes / per_col;
+    if (cw >= hidden) return hidden;
+    const int64_t q = cw >= 1024 ? 1024 : 256;
+    cw = cw / q * q;
+    return cw >= 256 ? cw : hidden;
 }
 
-template <int OX>
-cudaError_t bwd_t(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
-                  const float* mean, const float* rstd, const void* gamma, int64_t rows,
-                  int64_t hidden, void* workspace, int stripes, cudaStream_t st) {
-    const Stripes sp = make_stripes(rows, stripes);
-    float* ws = static_cast<float*>(workspace);
-    const int h = static_cast<int>(hidden);
-    const dim3 grid(static_cast<unsigned>((hidden + OX * kVec - 1) / (OX * kVec)), stripes);
-    if (cudaError_t e = launch_pdl(outer_bwd_sums<OX>, grid, dim3(kOT), kBwdBytes, st,
-                                   static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(x),
-                                   mean, rstd, ws, sp, h))
-        return e;
-    if (cudaError_t e = launch_pdl(outer_bwd_reduce, dim3(static_cast<unsigned>((hidden + kMW - 1) / kMW)),
-                                   dim3(kMW * 32), 0, st, static_cast<const float*>(ws), dgamma,
-                                   dbeta, h, 0, h, stripes))
-        return e;
-    return launch_pdl(outer_bwd_apply<OX>, grid, dim3(kOT), kBwdBytes, st,
-                      static_cast<uint16_t*>(dx), static_cast<const uint16_t*>(dy),
-                      static_cast<const uint16_t*>(x), mean, rstd,
-                      static_cast<const uint16_t*>(gamma), static_cast<const float*>(dgamma),
-                      static_cast<const float*>(dbeta), 1.0f / static_cast<float>(rows), sp, h);
-}
-
-}  // namespace
-
-int outer_stripes(int64_t rows, int64_t hidden, int sms) {
-    // about one CTA per SM over the column tiles (measured faster than a
-    // full wave of 2-3 resident CTAs per SM: fewer stripe partials to merge
-    // and longer streams per thread), and at least 4 rows per row lane
+// Row stripes for a chunk of `cols` columns: about one CTA per SM over the
+// chunk's column tiles (measured faster than a full wave of 2-3 resident
+// CTAs per SM: fewer stripe partials to merge and longer streams per
+// thread), and at least 4 rows per row lane.
+int stripes_for(int64_t rows, int64_t cols, int sms) {
     const int64_t r = rows > 0 ? rows : 1;
-    const int ox = lanes_for(hidden);
-    const int64_t nt = (hidden + ox * kVec - 1) / (ox * kVec);
+    const int ox = lanes_for(cols);
+    const int64_t nt = (cols + ox * kVec - 1) / (ox * kVec);
     int64_t ns = sms / nt;
     const int64_t rows_min = 4LL * (kOT / ox);
     const int64_t most = (r + rows_min - 1) / rows_min;
@@ -567,6 +560,68 @@ int outer_stripes(int64_t rows, int64_t hidden, int sms) {
     if (ns < 1) ns = 1;
     return static_cast<int>(ns);
 }
+
+// The most stripes any chunk of a (rows, hidden) call uses, over both
+// directions (the workspace is sized for it).
+int max_stripes(int64_t rows, int64_t hidden, int sms) {
+    int most = 1;
+    for (int tensors = 1; tensors <= 2; ++tensors) {
+        const int64_t cw = outer_chunk_cols(rows, hidden, tensors);
+        const int64_t last = hidden - (hidden - 1) / cw * cw;
+        for (int64_t w : {cw, last}) {
+            const int ns = stripes_for(rows, w, sms);
+            if (ns > most) most = ns;
+        }
+    }
+    return most;
+}
+
+template <int OX>
+cudaError_t fwd_chunk(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                      const void* beta, int64_t rows, int64_t hidden, float eps, float2* part,
+                      float* coef, int64_t c0, int64_t c1, int stripes, cudaStream_t st) {
+    const Stripes sp = make_stripes(rows, stripes);
+    const int h = static_cast<int>(hidden), a = static_cast<int>(c0), b = static_cast<int>(c1);
+    const dim3 grid(static_cast<unsigned>((c1 - c0 + OX * kVec - 1) / (OX * kVec)), stripes);
+    if (cudaError_t e = launch_pdl(outer_stats<OX>, grid, dim3(kOT), kFwdBytes, st,
+                                   static_cast<const uint16_t*>(x), part, sp, h, a, b))
+        return e;
+    if (cudaError_t e = launch_pdl(outer_finalize, dim3(static_cast<unsigned>((c1 - c0 + kMW - 1) / kMW)),
+                                   dim3(kMW * 32), 0, st, static_cast<const float2*>(part),
+                                   static_cast<const uint16_t*>(gamma),
+                                   static_cast<const uint16_t*>(beta), mean, rstd, coef, rows, h, a,
+                                   b, stripes, sp, eps))
+        return e;
+    return launch_pdl(outer_apply<OX>, grid, dim3(kOT), kFwdBytes, st, static_cast<uint16_t*>(y),
+                      static_cast<const uint16_t*>(x), static_cast<const float*>(coef), sp, h, a, b);
+}
+
+template <int OX>
+cudaError_t bwd_chunk(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+                      const float* mean, const float* rstd, const void* gamma, int64_t rows,
+                      int64_t hidden, float* ws, int64_t c0, int64_t c1, int stripes,
+                      cudaStream_t st) {
+    const Stripes sp = make_stripes(rows, stripes);
+    const int h = static_cast<int>(hidden), a = static_cast<int>(c0), b = static_cast<int>(c1);
+    const dim3 grid(static_cast<unsigned>((c1 - c0 + OX * kVec - 1) / (OX * kVec)), stripes);
+    if (cudaError_t e = launch_pdl(outer_bwd_sums<OX>, grid, dim3(kOT), kBwdBytes, st,
+                                   static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(x),
+                                   mean, rstd, ws, sp, h, a, b))
+        return e;
+    if (cudaError_t e = launch_pdl(outer_bwd_reduce, dim3(static_cast<unsigned>((c1 - c0 + kMW - 1) / kMW)),
+                                   dim3(kMW * 32), 0, st, static_cast<const float*>(ws), dgamma,
+                                   dbeta, h, a, b, stripes))
+        return e;
+    return launch_pdl(outer_bwd_apply<OX>, grid, dim3(kOT), kBwdBytes, st,
+                      static_cast<uint16_t*>(dx), static_cast<const uint16_t*>(dy),
+                      static_cast<const uint16_t*>(x), mean, rstd,
+                      static_cast<const uint16_t*>(gamma), static_cast<const float*>(dgamma),
+                      static_cast<const float*>(dbeta), 1.0f / static_cast<float>(rows), sp, h, a, b);
+}
+
+}  // namespace
+
+int outer_stripes(int64_t rows, int64_t hidden, int sms) { return max_stripes(rows, hidden, sms); }
 
 size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
     const size_t ns = static_cast<size_t>(outer_stripes(rows, hidden, sms));
@@ -579,20 +634,38 @@ cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, c
                              const void* beta, int64_t rows, int64_t hidden, float eps,
                              void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
-    const int stripes = outer_stripes(rows, hidden, sms);
-    return lanes_for(hidden) == 128
-               ? fwd_t<128>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace, stripes, st)
-               : fwd_t<32>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace, stripes, st);
+    const int ns_max = outer_stripes(rows, hidden, sms);
+    float2* part = static_cast<float2*>(workspace);
+    float* coef = reinterpret_cast<float*>(part + static_cast<int64_t>(ns_max) * hidden);
+    const int64_t cw = outer_chunk_cols(rows, hidden, 1);
+    for (int64_t c0 = 0; c0 < hidden; c0 += cw) {
+        const int64_t c1 = c0 + cw < hidden ? c0 + cw : hidden;
+        const int ns = stripes_for(rows, c1 - c0, sms);
+        const cudaError_t e =
+            lanes_for(c1 - c0) == 128
+                ? fwd_chunk<128>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, c0, c1, ns, st)
+                : fwd_chunk<32>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, c0, c1, ns, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_outer_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                              const float* mean, const float* rstd, const void* gamma, int64_t rows,
                              int64_t hidden, void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
-    const int stripes = outer_stripes(rows, hidden, sms);
-    return lanes_for(hidden) == 128
-               ? bwd_t<128>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, workspace, stripes, st)
-               : bwd_t<32>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, workspace, stripes, st);
+    float* ws = static_cast<float*>(workspace);
+    const int64_t cw = outer_chunk_cols(rows, hidden, 2);
+    for (int64_t c0 = 0; c0 < hidden; c0 += cw) {
+        const int64_t c1 = c0 + cw < hidden ? c0 + cw : hidden;
+        const int ns = stripes_for(rows, c1 - c0, sms);
+        const cudaError_t e =
+            lanes_for(c1 - c0) == 128
+                ? bwd_chunk<128>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, c0, c1, ns, st)
+                : bwd_chunk<32>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, c0, c1, ns, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace nf
