@@ -217,6 +217,7 @@ struct BlockMap {
 template <int N> struct Log2 { static constexpr int v = 1 + Log2<N / 2>::v; };
 template <> struct Log2<1> { static constexpr int v = 0; };
 
+// [kernel-span norm_rows_bwd_kernel]
 template <int OP, int H>
 __global__ void __launch_bounds__(RGeo<OP, H>::THREADS, RGeo<OP, H>::CPS)
 norm_rows_bwd_kernel(RowsArgs a) {
@@ -495,6 +496,8 @@ norm_rows_bwd_kernel(RowsArgs a) {
         out[c4] = s;
     }
 }
+
+// [end kernel-span norm_rows_bwd_kernel]
 
 namespace {
 

@@ -31,6 +31,7 @@ struct Geo {
     static_assert(TPR % 32 == 0, "a row uses whole warps");
 };
 
+// [kernel-span fused_add_rmsnorm_reg]
 // A parameter vector (weight, gamma or beta) of this thread's columns.
 // With PRE the thread loads all VPT vectors once, before its first row, so
 // a call with few rows makes one memory round trip (the row and the
@@ -77,7 +78,6 @@ __device__ __forceinline__ void prefetch_first_row(const uint16_t* a, const uint
 }
 
 // residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
-// [kernel-span fused_add_rmsnorm_reg]
 template <int H, bool PRE>
 __global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
 fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
@@ -282,6 +282,7 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
     }
 }
 
+// [kernel-span layernorm_fwd_shift]
 // LayerNorm forward with one reduction per row: each warp shifts its values
 // by one of them (c = the first element its lane 0 holds) and sums d = x - c
 // and d^2; the warp's (mean, M2) = (c + sum d / n, sum d^2 - (sum d)^2 / n)
@@ -376,6 +377,8 @@ layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict
         if constexpr (G::W > 1) __syncthreads();  // `red` is reused by the next row block
     }
 }
+
+// [end kernel-span layernorm_fwd_shift]
 
 // Which LayerNorm forward statistics the register path uses (two passes
 // over the resident row, or one shifted pass).

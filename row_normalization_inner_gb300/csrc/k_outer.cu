@@ -28,6 +28,10 @@
 // apply pass forms dx = c1 * dy - k2 - (x - mean) * k3 with per-column
 // c1 = rstd * gamma, k2 = c1 * dbeta / R, k3 = c1 * rstd * dgamma / R.
 //
+// The statistics passes stream x (and dy) with an L2 evict-last hint and
+// the apply passes read them evict-first, so whatever part of the input L2
+// can hold is read from DRAM once (forward 16384 x 4096: 70.4 -> 65.9 us).
+//
 // Every kernel is launched as a programmatic dependent of the one before it
 // and starts with griddepcontrol.wait, so launch latency overlaps the tail
 // of the previous kernel while every read still follows its producer.
@@ -526,28 +530,9 @@ cudaError_t ensure_smem_attrs() {
 static_assert(sizeof(Chan) * kOT * kVec <= kFwdBytes, "stats epilogue fits the ring");
 static_assert(sizeof(float4) * kOT * 4 <= kBwdBytes, "sums epilogue fits the ring");
 
-// Column chunks.  The statistics pass of a chunk streams its input with an
-// L2 evict-last hint and the chunk's apply pass reads it again right after
-// (evict-first), so a chunk whose input (x, or x and dy) is at most
-// kOuterChunkBytes is read from DRAM once: the second read comes from the
-// 129 MB L2.  Chunks are whole column tiles (1024 columns, or 256 below
-// that); rows too long for a 256-column chunk to fit are walked in one pass
-// over all columns, reading the input twice.
-constexpr int64_t kOuterChunkBytes = 64LL << 20;
-
-int64_t outer_chunk_cols(int64_t rows, int64_t hidden, int tensors) {
-    const int64_t per_col = (rows > 0 ? rows : 1) * 2 * tensors;
-    int64_t cw = kOuterChunkBytes / per_col;
-    if (cw >= hidden) return hidden;
-    const int64_t q = cw >= 1024 ? 1024 : 256;
-    cw = cw / q * q;
-    return cw >= 256 ? cw : hidden;
-}
-
-// Row stripes for a chunk of `cols` columns: about one CTA per SM over the
-// chunk's column tiles (measured faster than a full wave of 2-3 resident
-// CTAs per SM: fewer stripe partials to merge and longer streams per
-// thread), and at least 4 rows per row lane.
+// Row stripes: about one CTA per SM over the column tiles (measured faster
+// than a full wave of 2-3 resident CTAs per SM: fewer stripe partials to
+// merge and longer streams per thread), and at least 4 rows per row lane.
 int stripes_for(int64_t rows, int64_t cols, int sms) {
     const int64_t r = rows > 0 ? rows : 1;
     const int ox = lanes_for(cols);
@@ -561,23 +546,8 @@ int stripes_for(int64_t rows, int64_t cols, int sms) {
     return static_cast<int>(ns);
 }
 
-// The most stripes any chunk of a (rows, hidden) call uses, over both
-// directions (the workspace is sized for it).
-int max_stripes(int64_t rows, int64_t hidden, int sms) {
-    int most = 1;
-    for (int tensors = 1; tensors <= 2; ++tensors) {
-        const int64_t cw = outer_chunk_cols(rows, hidden, tensors);
-        const int64_t last = hidden - (hidden - 1) / cw * cw;
-        for (int64_t w : {cw, last}) {
-            const int ns = stripes_for(rows, w, sms);
-            if (ns > most) most = ns;
-        }
-    }
-    return most;
-}
-
 template <int OX>
-cudaError_t fwd_chunk(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+cudaError_t fwd_pass(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                       const void* beta, int64_t rows, int64_t hidden, float eps, float2* part,
                       float* coef, int64_t c0, int64_t c1, int stripes, cudaStream_t st) {
     const Stripes sp = make_stripes(rows, stripes);
@@ -597,7 +567,7 @@ cudaError_t fwd_chunk(void* y, float* mean, float* rstd, const void* x, const vo
 }
 
 template <int OX>
-cudaError_t bwd_chunk(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
+cudaError_t bwd_pass(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                       const float* mean, const float* rstd, const void* gamma, int64_t rows,
                       int64_t hidden, float* ws, int64_t c0, int64_t c1, int stripes,
                       cudaStream_t st) {
@@ -621,7 +591,7 @@ cudaError_t bwd_chunk(void* dx, float* dgamma, float* dbeta, const void* dy, con
 
 }  // namespace
 
-int outer_stripes(int64_t rows, int64_t hidden, int sms) { return max_stripes(rows, hidden, sms); }
+int outer_stripes(int64_t rows, int64_t hidden, int sms) { return stripes_for(rows, hidden, sms); }
 
 size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
     const size_t ns = static_cast<size_t>(outer_stripes(rows, hidden, sms));
@@ -630,42 +600,32 @@ size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
     return fwd > bwd ? fwd : bwd;
 }
 
+// One pass over all columns.  (Walking the columns in chunks sized for L2,
+// so that each chunk's apply pass would re-read it from there, was measured
+// slower at every size, even with the eviction hints: each chunk adds three
+// launches and a merge bubble, and a chunk has fewer column tiles to spread
+// over the SMs.)
 cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                              const void* beta, int64_t rows, int64_t hidden, float eps,
                              void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
-    const int ns_max = outer_stripes(rows, hidden, sms);
+    const int ns = outer_stripes(rows, hidden, sms);
     float2* part = static_cast<float2*>(workspace);
-    float* coef = reinterpret_cast<float*>(part + static_cast<int64_t>(ns_max) * hidden);
-    const int64_t cw = outer_chunk_cols(rows, hidden, 1);
-    for (int64_t c0 = 0; c0 < hidden; c0 += cw) {
-        const int64_t c1 = c0 + cw < hidden ? c0 + cw : hidden;
-        const int ns = stripes_for(rows, c1 - c0, sms);
-        const cudaError_t e =
-            lanes_for(c1 - c0) == 128
-                ? fwd_chunk<128>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, c0, c1, ns, st)
-                : fwd_chunk<32>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, c0, c1, ns, st);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    float* coef = reinterpret_cast<float*>(part + static_cast<int64_t>(ns) * hidden);
+    return lanes_for(hidden) == 128
+               ? fwd_pass<128>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, 0, hidden, ns, st)
+               : fwd_pass<32>(y, mean, rstd, x, gamma, beta, rows, hidden, eps, part, coef, 0, hidden, ns, st);
 }
 
 cudaError_t launch_outer_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                              const float* mean, const float* rstd, const void* gamma, int64_t rows,
                              int64_t hidden, void* workspace, int sms, cudaStream_t st) {
     if (cudaError_t e = ensure_smem_attrs()) return e;
+    const int ns = outer_stripes(rows, hidden, sms);
     float* ws = static_cast<float*>(workspace);
-    const int64_t cw = outer_chunk_cols(rows, hidden, 2);
-    for (int64_t c0 = 0; c0 < hidden; c0 += cw) {
-        const int64_t c1 = c0 + cw < hidden ? c0 + cw : hidden;
-        const int ns = stripes_for(rows, c1 - c0, sms);
-        const cudaError_t e =
-            lanes_for(c1 - c0) == 128
-                ? bwd_chunk<128>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, c0, c1, ns, st)
-                : bwd_chunk<32>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, c0, c1, ns, st);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return lanes_for(hidden) == 128
+               ? bwd_pass<128>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, 0, hidden, ns, st)
+               : bwd_pass<32>(dx, dgamma, dbeta, dy, x, mean, rstd, gamma, rows, hidden, ws, 0, hidden, ns, st);
 }
 
 }  // namespace nf

@@ -100,22 +100,20 @@ def test_outer_full_size(rows, hidden):
 
 
 @pytest.mark.parametrize("rows,hidden", ((16384, 4104), (40000, 1000)))
-def test_outer_column_chunks(rows, hidden):
-    # inputs larger than one L2-sized column chunk: the forward walks 2048-
-    # (first case) or 768-column chunks (second), the backward 1024 / 256,
-    # each with a ragged last chunk, every chunk its own statistics, merge and
-    # apply launches
+def test_outer_large(rows, hidden):
+    # inputs of 134 / 80 MB per tensor (several column tiles with a ragged
+    # last one; 152 and 38 row stripes), forward and backward
     x, dy, g, b = workloads.outer_inputs(rows, hidden, seed=rows + hidden)
     y_ref, m_ref, r_ref = oracle.outer_norm_fwd(x, g, b, 1e-5)
     y, mean, rstd = nf.outer_norm_fwd(x.cuda(), g.cuda(), b.cuda(), 1e-5)
     torch.cuda.synchronize()
-    check_bf16(y, y_ref, f"outer chunked fwd y {rows}x{hidden}")
-    check_f32(mean, m_ref, f"outer chunked fwd mean {rows}x{hidden}")
-    check_f32(rstd, r_ref, f"outer chunked fwd rstd {rows}x{hidden}", rtol=1e-4)
+    check_bf16(y, y_ref, f"outer large fwd y {rows}x{hidden}")
+    check_f32(mean, m_ref, f"outer large fwd mean {rows}x{hidden}")
+    check_f32(rstd, r_ref, f"outer large fwd rstd {rows}x{hidden}", rtol=1e-4)
     m32, r32 = torch.from_numpy(m_ref.astype(np.float32)), torch.from_numpy(r_ref.astype(np.float32))
     dx_ref, dg_ref, db_ref = oracle.outer_norm_bwd(dy, x, m32, r32, g)
     dx, dg, db = nf.outer_norm_bwd(dy.cuda(), x.cuda(), m32.cuda(), r32.cuda(), g.cuda())
     torch.cuda.synchronize()
-    check_bf16(dx, dx_ref, f"outer chunked bwd dx {rows}x{hidden}")
-    check_f32(dg, dg_ref, f"outer chunked bwd dgamma {rows}x{hidden}")
-    check_f32(db, db_ref, f"outer chunked bwd dbeta {rows}x{hidden}")
+    check_bf16(dx, dx_ref, f"outer large bwd dx {rows}x{hidden}")
+    check_f32(dg, dg_ref, f"outer large bwd dgamma {rows}x{hidden}")
+    check_f32(db, db_ref, f"outer large bwd dbeta {rows}x{hidden}")
