@@ -31,6 +31,14 @@ struct Geo {
     static_assert(TPR % 32 == 0, "a row uses whole warps");
 };
 
+// Minimum resident CTAs per SM the RMSNorm / LayerNorm forward kernels are
+// compiled for: 5 at hidden 4096 (48 registers, 62.5 % occupancy instead of
+// 50 %; measured 40.9 -> 39.6 us and 42.6 -> 41.3 us at 16384 rows), 1
+// elsewhere (forcing it at 1024 or 8192, or on the fused kernel, was
+// slower), and never for the small-call variants (PRE), whose parameter
+// registers would spill.
+template <int H, bool PRE> struct FwdMinBlocks { static constexpr int v = (H == 4096 && !PRE) ? 5 : 1; };
+
 // [kernel-span fused_add_rmsnorm_reg]
 // A parameter vector (weight, gamma or beta) of this thread's columns.
 // With PRE the thread loads all VPT vectors once, before its first row, so
@@ -138,7 +146,7 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
 
 // y <- bf16(x * rsqrt(mean(x^2) + eps) * w)
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
 rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
                 int64_t rows, float eps, int64_t first_wave) {
     using G = Geo<H>;
@@ -190,7 +198,7 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
 // mean = sum(x)/H ; var = sum((x-mean)^2)/H ; rstd = rsqrt(var + eps)
 // y <- bf16((x - mean) * rstd * gamma + beta)
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
 layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                   const uint16_t* x, const uint16_t* __restrict__ gamma,
                   const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
@@ -292,7 +300,7 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 // sum d^2 - (sum d)^2 / n costs at most about n fp32 roundings relative to
 // M2 (n <= 1024 here): far below the bf16 output rounding.
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
 layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                     const uint16_t* x, const uint16_t* __restrict__ gamma,
                     const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
