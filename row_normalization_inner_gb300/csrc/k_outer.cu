@@ -98,6 +98,11 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// The apply passes walk each thread's rows last to first: the statistics
+// pass streamed them first to last, so the rows it read last are the ones
+// still in L2 when the apply pass starts.
+constexpr bool kApplyLastFirst = true;
+
 template <int S, int U, int A, int OY>
 struct RowRing {
     static constexpr int kBytes = S * A * U * kOT * 16;
@@ -105,6 +110,11 @@ struct RowRing {
     int64_t row0;  // this thread's first row; its rows are row0 + i * OY
     int cnt;       // number of rows of this thread
     uint64_t pol;  // L2 policy of the copies
+    bool rev;      // walk the rows last to first
+    // row of this thread's i-th step
+    __device__ __forceinline__ int64_t row(int i) const {
+        return row0 + static_cast<int64_t>(rev ? cnt - 1 - i : i) * OY;
+    }
     __device__ __forceinline__ uint4* at(int st, int a, int u) const {
         return base + (((st % S) * A + a) * U + u) * kOT + threadIdx.x;
     }
@@ -117,8 +127,7 @@ struct RowRing {
             if (i < cnt) {
 #pragma unroll
                 for (int a = 0; a < A; ++a)
-                    cp_async16(at(st, a, u), src[a] + (row0 + static_cast<int64_t>(i) * OY) * hidden + c0,
-                               pol);
+                    cp_async16(at(st, a, u), src[a] + row(i) * hidden + c0, pol);
             }
         }
         cp_commit();
@@ -171,7 +180,7 @@ outer_stats(const uint16_t* __restrict__ x, float2* __restrict__ part, Stripes s
     const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
     const bool ok = c0 < col1;
     const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0,
-                           policy_keep()};
+                           policy_keep(), false};
     const uint16_t* const src[1] = {x};
     float2 nk[4], s1[4], s2[4];  // nk = -shift
 #pragma unroll
@@ -245,7 +254,7 @@ outer_apply(uint16_t* y, const uint16_t* x, const float* __restrict__ coef, Stri
     const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
     if (c0 >= col1) return;
     const FwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty),
-                           policy_last_use()};
+                           policy_last_use(), kApplyLastFirst};
     const uint16_t* const src[1] = {x};
     ring.prologue(src, hidden, c0);
     float2 a[4], b[4];
@@ -262,7 +271,7 @@ outer_apply(uint16_t* y, const uint16_t* x, const float* __restrict__ coef, Stri
                 unpack8x2(*ring.at(st, 0, u), f);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) o[q] = __ffma2_rn(f[q], a[q], b[q]);
-                st_stream(y + (ring.row0 + static_cast<int64_t>(i) * OY) * hidden + c0, pack8x2(o));
+                st_stream(y + ring.row(i) * hidden + c0, pack8x2(o));
             }
         }
     }
@@ -283,7 +292,7 @@ outer_bwd_sums(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
     const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
     const bool ok = c0 < col1;
     const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, ok ? thread_rows<OY>(sp.size(stripe), ty) : 0,
-                           policy_keep()};
+                           policy_keep(), false};
     const uint16_t* const src[2] = {x, dy};
     ring.prologue(src, hidden, c0);
     float2 sg[4], sb[4], nmu[4], rs[4];
@@ -357,7 +366,7 @@ outer_bwd_apply(uint16_t* dx, const uint16_t* dy, const uint16_t* x, const float
     const int64_t c0 = col0 + (static_cast<int64_t>(blockIdx.x) * OX + tx) * kVec;
     if (c0 >= col1) return;
     const BwdRing<OY> ring{dsm, sp.begin(stripe) + ty, thread_rows<OY>(sp.size(stripe), ty),
-                           policy_last_use()};
+                           policy_last_use(), kApplyLastFirst};
     const uint16_t* const src[2] = {x, dy};
     ring.prologue(src, hidden, c0);
     float2 nmu[4], c1[4], nk2[4], nk3[4];  // -mean, c1, -k2, -k3
@@ -390,7 +399,7 @@ outer_bwd_apply(uint16_t* dx, const uint16_t* dy, const uint16_t* x, const float
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     o[q] = __ffma2_rn(__fadd2_rn(xf[q], nmu[q]), nk3[q], __ffma2_rn(c1[q], df[q], nk2[q]));
-                st_stream(dx + (ring.row0 + static_cast<int64_t>(i) * OY) * hidden + c0, pack8x2(o));
+                st_stream(dx + ring.row(i) * hidden + c0, pack8x2(o));
             }
         }
     }

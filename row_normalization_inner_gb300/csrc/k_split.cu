@@ -113,6 +113,11 @@ __device__ __forceinline__ void prefetch_chunk(const uint16_t* src, int64_t r, i
     }
 }
 
+// The apply passes take their (chunk, row) CTAs in the reverse of the
+// statistics pass's order: the chunks the statistics pass read last are the
+// ones still in L2 when the apply pass starts.
+constexpr bool kSplitApplyLastFirst = true;
+
 // ---- forward ----------------------------------------------------------------
 // OP: 0 fused add + RMSNorm, 1 RMSNorm, 2 LayerNorm.
 template <int OP>
@@ -293,14 +298,16 @@ template <int OP>
 __global__ void __launch_bounds__(kSpT) split_apply_fwd(DynArgs a, const float* __restrict__ part,
                                                         const float2* __restrict__ stat, int nc) {
     __shared__ Chan sh[kSpT / 32];
-    const int c = blockIdx.x, H = a.hidden;
-    if (blockIdx.y < a.rows) {
-        prefetch_chunk(a.in0, blockIdx.y, c, H);
-        if (OP == 0) prefetch_chunk(a.in1, blockIdx.y, c, H);
+    // CTAs take the grid last to first (see kSplitApplyLastFirst)
+    const int c = kSplitApplyLastFirst ? gridDim.x - 1 - blockIdx.x : blockIdx.x, H = a.hidden;
+    const int64_t rfirst = kSplitApplyLastFirst ? gridDim.y - 1 - blockIdx.y : blockIdx.y;
+    if (rfirst < a.rows) {
+        prefetch_chunk(a.in0, rfirst, c, H);
+        if (OP == 0) prefetch_chunk(a.in1, rfirst, c, H);
     }
     pdl_wait();
     const int NV = H / kVec;
-    for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+    for (int64_t r = rfirst; r < a.rows; r += gridDim.y) {
         float f[kSpV][8];
         load_chunk(a.in0, r, c, H, f);
         if constexpr (OP == 0) {
@@ -478,10 +485,13 @@ __global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2*
     constexpr int NP = OP == 3 ? 2 : 1;
     __shared__ float2 sh_stat[kSpMergeRows];
     __shared__ float red[(kSpT / 32) * kSpMergeRows * 2];
-    const int c = blockIdx.x, H = a.hidden;
+    // CTAs take the grid last to first (see kSplitApplyLastFirst); row block
+    // `blk` always feeds column-partial slot `blk`
+    const int c = kSplitApplyLastFirst ? gridDim.x - 1 - blockIdx.x : blockIdx.x, H = a.hidden;
     const int NV = H / kVec;
     const int64_t nb = gridDim.y;
-    const int64_t r0 = a.rows * blockIdx.y / nb, r1 = a.rows * (blockIdx.y + 1) / nb;
+    const int64_t blk = kSplitApplyLastFirst ? nb - 1 - blockIdx.y : blockIdx.y;
+    const int64_t r0 = a.rows * blk / nb, r1 = a.rows * (blk + 1) / nb;
     if (r0 < r1) {
         prefetch_chunk(a.in0, r0, c, H);
         prefetch_chunk(a.in1, r0, c, H);
@@ -532,7 +542,7 @@ __global__ void __launch_bounds__(kSpT) split_apply_bwd(DynArgs a, const float2*
         }
     }
     // one row block: the column sums are final and go straight to the outputs
-    float* wp = a.ws + static_cast<int64_t>(blockIdx.y) * NP * H;
+    float* wp = a.ws + blk * NP * H;
     float* w0 = a.cols0 ? a.cols0 : wp;
     float* w1 = a.cols0 ? a.cols1 : wp + H;
 #pragma unroll
