@@ -539,6 +539,10 @@ def ops_suite(nf, peak, stream, l2_bytes):
     # rows longer than a cluster holds: the split family
     for op in ("rmsnorm_fwd", "layernorm_fwd", "fused_add_rmsnorm", "layernorm_bwd", "rmsnorm_bwd"):
         entry(op, 4, 1 << 22, EPS)
+    # hidden sizes with no compiled kernel: the runtime-hidden family
+    for h in (3072, 6144):
+        for op in ("fused_add_rmsnorm", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
+            entry(op, ROWS, h, EPS)
     return out
 
 

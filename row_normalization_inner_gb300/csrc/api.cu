@@ -376,13 +376,16 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
             pl.grid = static_cast<int32_t>(rows < kMaxGrid ? rows : kMaxGrid);
             pl.launches = 1;
         } else {
-            const int64_t per_sm = 1024 / dyn_threads > 0 ? 1024 / dyn_threads : 1;
-            const int64_t resident = static_cast<int64_t>(sm_count) * per_sm;
+            // one wave of the CTAs that stay resident (for the RMSNorm
+            // backward, counted with the fused-add backward's larger ring)
+            const int64_t resident =
+                static_cast<int64_t>(sm_count) * dyn_bwd_per_sm(hidden, op == NF_OP_RMSNORM_BWD);
             int64_t g = rows < resident ? rows : resident;
             if (g < 1) g = 1;
             pl.grid = static_cast<int32_t>(g);
             pl.launches = 2;
             pl.partials = static_cast<int32_t>(g);
+            pl.smem_bytes = static_cast<int32_t>(dyn_bwd_smem(hidden, false));
         }
     } else if (p == NF_PATH_BULK) {
         int threads, stages, smem, groups, per_sm = 1;

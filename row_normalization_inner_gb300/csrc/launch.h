@@ -110,6 +110,10 @@ struct DynArgs {
     float eps;
 };
 bool dyn_shape(int op, int64_t hidden, int* threads);
+// Backward: resident CTAs per SM and the copy ring's shared memory; `add`:
+// the ring also carries the fused-add backward's residual-stream gradient.
+int dyn_bwd_per_sm(int64_t hidden, bool add);
+size_t dyn_bwd_smem(int64_t hidden, bool add);
 int64_t dyn_max_hidden(int op);
 cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st);
 

@@ -135,11 +135,25 @@ def test_dynamic_plans(hidden):
             st, p = nf.nf_plan_compute(op, rows, hidden, 152)
             assert st == nf.NF_OK and p["path"] == "dynamic"
             assert p["block"] % 32 == 0 and 32 <= p["block"] <= (512 if bwd else 1024)
-            assert p["block"] * 4 * 8 >= hidden          # four vectors per thread cover the row
-            assert p["block"] == 32 or (p["block"] - 32) * 4 * 8 < hidden   # no spare warp
+            # forward: four vectors per thread; backward: one for rows of at
+            # most 256 vectors, else four
+            nv = hidden // 8
+            vecs = 1 if bwd and nv <= 256 else 4
+            assert p["block"] * vecs * 8 >= hidden
+            assert p["block"] == 32 or (p["block"] - 32) * vecs * 8 < hidden   # no spare warp
             if bwd:
+                # one wave of the CTAs that stay resident: the launch bound
+                # keeps 1024 threads per SM with one vector per thread, else
+                # 512, and each CTA's copy ring (2 stages of x and dy, and for
+                # the RMSNorm backward room for the fused-add backward's third
+                # tensor) takes shared memory (228 KB per SM, 1 KB reserved per CTA)
+                ring = 2 * 2 * vecs * p["block"] * 16
+                assert p["smem_bytes"] == ring
+                ring_max = ring * 3 // 2 if op == "rmsnorm_bwd" else ring
+                per_sm = min((1024 if vecs == 1 else 512) // p["block"], 228 * 1024 // (ring_max + 1024 + 512))
+                per_sm = max(1, per_sm)
                 assert p["launches"] == 2 and p["partials"] == p["grid"] >= 1
-                assert p["grid"] <= min(rows, 152 * max(1, 1024 // p["block"]))
+                assert p["grid"] == min(rows, 152 * per_sm)
             else:
                 assert p["launches"] == 1 and p["grid"] == rows
         for path in ("reg", "bulk"):
