@@ -74,10 +74,13 @@ __device__ __forceinline__ void cta_sum(float (&v)[N], float* red) {
 }
 
 // OP: 0 fused add + RMSNorm, 1 RMSNorm fwd, 2 LayerNorm fwd.  MAXT bounds
-// the CTA size (so small rows keep a large register budget).
+// the CTA size (so small rows keep a large register budget).  LayerNorm
+// makes one reduction per row: the sums of d = x - c and d^2, with c the
+// row's first element (read by every thread; one cached line), give
+// mean = c + sum d / H and M2 = sum d^2 - (sum d)^2 / H.
 template <int OP, int MAXV, int MAXT>
 __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
-    __shared__ float red[2][kDynMaxWarps];
+    __shared__ float red[kDynMaxWarps * 2];
     grid_dep_wait();
     grid_dep_release();
     const int H = a.hidden;
@@ -86,7 +89,7 @@ __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
     const float invH = 1.0f / static_cast<float>(H);
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         uint4 v0[MAXV], v1[MAXV];
-        float s1[1] = {0.f};
+        const float c = OP == 2 ? __uint_as_float(static_cast<uint32_t>(__ldg(a.in0 + row * H)) << 16) : 0.f;
 #pragma unroll
         for (int k = 0; k < MAXV; ++k) {
             const int v = k * T + t;
@@ -98,6 +101,7 @@ __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
             }
         }
         float f[MAXV][8];
+        float sv[2] = {0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < MAXV; ++k) {
             unpack8(v0[k], f[k]);  // zero vectors beyond the row add nothing
@@ -107,27 +111,29 @@ __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[k][e] += b[e];
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s1[0] += (OP == 2) ? f[k][e] : f[k][e] * f[k][e];
-        }
-        cta_sum<1>(s1, red[0]);
-        float mean = 0.f, rstd;
-        if constexpr (OP == 2) {
-            mean = s1[0] * invH;
-            float s2[1] = {0.f};
-#pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
+            if constexpr (OP == 2) {
                 if (k * T + t < NV) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float d = f[k][e] - mean;
-                        s2[0] += d * d;
+                        const float d = f[k][e] - c;
+                        sv[0] += d;
+                        sv[1] = fmaf(d, d, sv[1]);
                     }
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sv[0] = fmaf(f[k][e], f[k][e], sv[0]);
             }
-            cta_sum<1>(s2, red[1]);
-            rstd = rsqrtf(s2[0] * invH + a.eps);
+        }
+        float mean = 0.f, rstd;
+        if constexpr (OP == 2) {
+            cta_sum<2>(sv, red);
+            const float dm = sv[0] * invH;
+            mean = c + dm;
+            rstd = rsqrtf(fmaxf(sv[1] - sv[0] * dm, 0.f) * invH + a.eps);
         } else {
+            float s1[1] = {sv[0]};
+            cta_sum<1>(s1, red);
             rstd = rsqrtf(s1[0] * invH + a.eps);
         }
 #pragma unroll
