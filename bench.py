@@ -55,6 +55,7 @@ EPS = 1e-5
 DOMINANT_HIDDEN = 8192
 FALLBACK_HBM_GBS = 6800.0
 E2E_CHUNKS = 2
+E2E_ROUNDS = 9      # end-to-end timing rounds (pipeline, then bare link, each round)
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -682,16 +683,18 @@ def run_gpu(args):
             b.synchronize()
             return a.elapsed_time(b)
 
-        # five rounds, each timing the pipeline and then the bare link on the
+        # nine rounds, each timing the pipeline and then the bare link on the
         # same bytes; the median round of each is reported (the host link is
-        # shared with the rest of the machine, so single rounds vary)
+        # shared with the rest of the machine: in one run three of five
+        # pipeline rounds and one of five link rounds fell from about 335 to
+        # about 250 GB/s)
         e2e_steps = max(3, min(args.steps // 40, 25))
         timed(1)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         e_round, c_round = [], []
-        for r in range(5):
+        for r in range(E2E_ROUNDS):
             e_round.append(max_over_ranks(timed(e2e_steps), dist, dev))
             if r == 0:
                 # check once that the round trip really returned the device

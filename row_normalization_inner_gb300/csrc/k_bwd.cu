@@ -274,6 +274,64 @@ column_reduce(const float* __restrict__ ws, float* __restrict__ dgamma,
     if (ok && ly == 0) *reinterpret_cast<float4*>((which == 0 ? dgamma : dbeta) + j) = s;
 }
 
+// The same sums when there are many slots (> kWideSlots, the runtime-hidden
+// backward's one slot per resident CTA): kSplitW warps per float4 column,
+// warp w adding the contiguous slot range [n w / kSplitW, n (w + 1) /
+// kSplitW) with 32 slot lanes as above, then the warps' totals added in
+// warp order.  A lane then waits for one or two L2 round trips instead of
+// n / 256, and four times as many warps share the work.
+constexpr int kWideSlots = 256;
+constexpr int kSplitW = 4;
+
+__global__ void __launch_bounds__(kSplitW * 32)
+column_reduce_split(const float* __restrict__ ws, float* __restrict__ dgamma,
+                    float* __restrict__ dbeta, int nslots, int hidden, int planes) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ float4 part[kSplitW];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c4 = blockIdx.x;  // one float4 column per CTA
+    const int64_t total4 = static_cast<int64_t>(planes) * hidden / 4;
+    const int which = static_cast<int>((c4 * 4) / hidden);
+    const int64_t j = (c4 * 4) % hidden;
+    const float4* src = reinterpret_cast<const float4*>(ws) + c4;
+    const int p_lo = static_cast<int>(static_cast<int64_t>(nslots) * warp / kSplitW);
+    const int p_hi = static_cast<int>(static_cast<int64_t>(nslots) * (warp + 1) / kSplitW);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kColU = 8;
+    for (int p0 = p_lo + lane; p0 < p_hi; p0 += kColU * 32) {
+        float4 v[kColU];
+#pragma unroll
+        for (int u = 0; u < kColU; ++u) {
+            const int p = p0 + u * 32;
+            v[u] = p < p_hi ? __ldcs(src + static_cast<int64_t>(p) * total4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kColU; ++u) {
+            if (p0 + u * 32 < p_hi) {
+                s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        s.x += __shfl_xor_sync(0xFFFFFFFFu, s.x, off);
+        s.y += __shfl_xor_sync(0xFFFFFFFFu, s.y, off);
+        s.z += __shfl_xor_sync(0xFFFFFFFFu, s.z, off);
+        s.w += __shfl_xor_sync(0xFFFFFFFFu, s.w, off);
+    }
+    if (lane == 0) part[warp] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float4 t = part[0];
+#pragma unroll
+        for (int w = 1; w < kSplitW; ++w) {
+            t.x += part[w].x; t.y += part[w].y; t.z += part[w].z; t.w += part[w].w;
+        }
+        *reinterpret_cast<float4*>((which == 0 ? dgamma : dbeta) + j) = t;
+    }
+}
+
 // The same sums when there are few slots (<= kNarrowSlots): one float4
 // column per thread, the slots added in order, so a CTA covers 1024
 // contiguous columns (the wide form would leave at least half of each
@@ -341,7 +399,11 @@ cudaError_t launch_column_reduce_planes(const float* ws, float* out0, float* out
                                   planes);
     };
     if (nslots <= 64) return launch(column_reduce<16>, 16);
-    return launch(column_reduce<32>, 32);
+    if (nslots <= kWideSlots) return launch(column_reduce<32>, 32);
+    cfg.gridDim = dim3(static_cast<unsigned>(cols4), 1, 1);
+    cfg.blockDim = dim3(kSplitW * 32, 1, 1);
+    return cudaLaunchKernelEx(&cfg, column_reduce_split, ws, out0, out1, nslots, static_cast<int>(hidden),
+                              planes);
 }
 
 cudaError_t launch_column_reduce(const float* ws, float* dgamma, float* dbeta, int nslots,
