@@ -61,14 +61,23 @@ int bwd_ctas_per_sm(int64_t hidden) {
 //    ring); the exception is hidden 12288 RMSNorm / LayerNorm forward from
 //    1024 rows, where the bulk ring keeps more bytes in flight than the
 //    register-resident rows can (LayerNorm 16384 x 12288: 0.96 against 0.72);
-//  - backward ops: the bulk path, at every size (its row groups fold their
-//    column partials inside the CTA, so stage 2 stays small).
+//  - backward ops: the bulk path (its row groups fold their column partials
+//    inside the CTA, so stage 2 stays small), except the RMSNorm backward
+//    (and with it the fused-add backward) at hidden 5120 and 12288 from 1024
+//    rows, where the runtime-hidden kernels with their per-thread copy ring
+//    were faster (fused-add 16384 x 12288: 238 against 310 us, RMSNorm 194
+//    against 228 us; 5120: 104 / 82 against 111 / 89 us; at 8192 and below,
+//    and for every LayerNorm size, the bulk and row-block kernels won).
 nf_path auto_path(nf_op op, int64_t rows, int64_t hidden, int rpc, int sms) {
     (void)rpc;
     (void)sms;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
-    if (!fwd) return NF_PATH_BULK;
+    if (!fwd) {
+        if (op == NF_OP_RMSNORM_BWD && rows >= 1024 && (hidden == 5120 || hidden == 12288))
+            return NF_PATH_DYNAMIC;
+        return NF_PATH_BULK;
+    }
     if (hidden >= 12288 && rows >= 1024 &&
         (op == NF_OP_RMSNORM_FWD || op == NF_OP_LAYERNORM_FWD))
         return NF_PATH_BULK;

@@ -326,8 +326,11 @@ def test_backward_plans(hidden, rows):
         a = nf.nf_plan_compute("rmsnorm_bwd", rows, hidden, 152, path)[1]
         b = nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152, path)[1]
         assert a == b    # same stripes and slots; only the planes per slot differ
+    # the measured rule: the bulk path, but the runtime-hidden kernels for the
+    # RMSNorm backward at hidden 5120 and 12288 from 1024 rows
     for op in ("layernorm_bwd", "rmsnorm_bwd"):
-        assert nf.nf_plan_compute(op, rows, hidden, 152)[1]["path"] == "bulk"
+        dyn = op == "rmsnorm_bwd" and hidden in (5120, 12288) and rows >= 1024
+        assert nf.nf_plan_compute(op, rows, hidden, 152)[1]["path"] == ("dynamic" if dyn else "bulk")
     for sms in (1, 152):
         st, p = nf.nf_plan_compute("layernorm_bwd", rows, hidden, sms, "bulk")
         assert st == nf.NF_OK and p["path"] == "bulk" and p["launches"] == 2
