@@ -325,7 +325,13 @@ def test_backward_plans(hidden, rows):
     for path in ("reg", "bulk"):
         a = nf.nf_plan_compute("rmsnorm_bwd", rows, hidden, 152, path)[1]
         b = nf.nf_plan_compute("layernorm_bwd", rows, hidden, 152, path)[1]
-        assert a == b    # same stripes and slots; only the planes per slot differ
+        # same stripes and slots; only the planes per slot differ, and at hidden
+        # 1024 the row-block kernels' group count (LayerNorm four, RMSNorm three:
+        # the CTA size and the rows in flight per CTA)
+        same = ("path", "grid", "partials", "launches", "cluster")
+        assert {k: a[k] for k in same} == {k: b[k] for k in same}
+        if hidden != 1024:
+            assert a == b
     # the measured rule: the bulk path, but the runtime-hidden kernels for the
     # RMSNorm backward at hidden 5120 and 12288 from 1024 rows
     for op in ("layernorm_bwd", "rmsnorm_bwd"):
