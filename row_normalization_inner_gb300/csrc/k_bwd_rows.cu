@@ -51,6 +51,7 @@ namespace nf {
 
 enum RowsOp { kRowsLn = 0, kRowsRms = 1, kRowsFused = 2 };
 
+// [kernel-span norm_rows_bwd_kernel] (with its shape table)
 // Per hidden size: VPT vectors per thread, R rows per block, NG groups;
 // IL = 0 gives each CTA a contiguous stripe of rows, IL = q >= 1 deals the
 // blocks out to the CTAs in chunks of q consecutive blocks, round robin;
@@ -222,7 +223,6 @@ struct BlockMap {
 template <int N> struct Log2 { static constexpr int v = 1 + Log2<N / 2>::v; };
 template <> struct Log2<1> { static constexpr int v = 0; };
 
-// [kernel-span norm_rows_bwd_kernel]
 template <int OP, int H>
 __global__ void __launch_bounds__(RGeo<OP, H>::THREADS, RGeo<OP, H>::CPS)
 norm_rows_bwd_kernel(RowsArgs a) {
