@@ -335,6 +335,32 @@ def test_rmsnorm_bwd_full_size(hidden, path):
     check_bf16(dx.cpu()[torch.from_numpy(idx)], dx_ref[idx], f"rms bwd full dx {hidden}/{path}")
 
 
+@pytest.mark.parametrize("hidden", (5120, 12288))
+def test_rmsnorm_bwd_automatic_runtime_hidden(hidden):
+    # from 1024 rows the automatic choice runs the RMSNorm and fused-add
+    # backward at these sizes on the runtime-hidden kernels
+    rows = 16384
+    assert nf.nf_plan_query("rmsnorm_bwd", rows, hidden)["path"] == "dynamic"
+    x, dy, w = workloads.rms_bwd_inputs(rows, hidden, seed=hidden)
+    dx, dw = nf.rmsnorm_bwd(dy.cuda(), x.cuda(), w.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    dx_ref, dw_ref = _rms_bwd_ref(dy, x, w, 1e-5)
+    check_f32(dw, dw_ref, f"rms bwd auto dw {hidden}")
+    idx = _sample_rows(rows, seed=hidden)
+    check_bf16(dx.cpu()[torch.from_numpy(idx)], dx_ref[idx], f"rms bwd auto dx {hidden}")
+    # the fused-add backward on the same kernels (the residual gradient in the ring)
+    rows = 2048
+    s_, w2, dy2, dres = workloads.fused_bwd_inputs(rows, hidden, seed=hidden + 1)
+    assert nf.nf_plan_query("rmsnorm_bwd", rows, hidden)["path"] == "dynamic"
+    ds_ref, dw2_ref = oracle.fused_add_rmsnorm_bwd(dy2, dres, s_, w2, 1e-6)
+    ds, dw2 = nf.fused_add_rmsnorm_bwd(dy2.cuda(), s_.cuda(), w2.cuda(), dres.cuda(), 1e-6)
+    ds_b, dw2_b = nf.fused_add_rmsnorm_bwd(dy2.cuda(), s_.cuda(), w2.cuda(), dres.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(ds, ds_ref, f"fused bwd auto dx {hidden}")
+    check_f32(dw2, dw2_ref, f"fused bwd auto dw {hidden}")
+    assert torch.equal(ds, ds_b) and torch.equal(dw2, dw2_b)
+
+
 @pytest.mark.parametrize("path", BWD_PATHS)
 def test_rmsnorm_bwd_in_place_and_deterministic(path):
     rows, hidden = 640, 8192
