@@ -20,10 +20,13 @@
 namespace nf {
 namespace {
 
-template <int H>
+// SMALL: the geometry of calls of at most kSmallCallRows rows, one row per
+// CTA so that a few rows spread over as many SMs (8 x 4096 fused: 2.0 ->
+// 1.6 us; at 16384 rows one row per CTA was slower at hidden 4096).
+template <int H, bool SMALL = false>
 struct Geo {
     static constexpr int TPR = RegShape<H>::TPR;
-    static constexpr int RPC = RegShape<H>::RPC;
+    static constexpr int RPC = SMALL ? 1 : RegShape<H>::RPC;
     static constexpr int NV = H / kVec;
     static constexpr int VPT = NV / TPR;
     static constexpr int W = TPR / 32;
@@ -89,10 +92,10 @@ __device__ __forceinline__ void prefetch_first_row(const uint16_t* a, const uint
 
 // residual <- x + residual ; x <- bf16(s * rsqrt(mean(s^2) + eps) * w)
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC)
+__global__ void __launch_bounds__(Geo<H, PRE>::TPR * Geo<H, PRE>::RPC)
 fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
                       const uint16_t* __restrict__ w, int64_t rows, float eps, int64_t first_wave) {
-    using G = Geo<H>;
+    using G = Geo<H, PRE>;
     __shared__ float red[G::RPC * G::W];
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     prefetch_first_row<G>(x, res, rows, group, t, first_wave);
@@ -148,10 +151,10 @@ fused_add_rmsnorm_reg(uint16_t* __restrict__ x, uint16_t* __restrict__ res,
 
 // y <- bf16(x * rsqrt(mean(x^2) + eps) * w)
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
+__global__ void __launch_bounds__(Geo<H, PRE>::TPR * Geo<H, PRE>::RPC, FwdMinBlocks<H, PRE>::v)
 rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
                 int64_t rows, float eps, int64_t first_wave) {
-    using G = Geo<H>;
+    using G = Geo<H, PRE>;
     __shared__ float red[G::RPC * G::W];
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
     prefetch_first_row<G>(x, nullptr, rows, group, t, first_wave);
@@ -200,11 +203,11 @@ rmsnorm_fwd_reg(uint16_t* y, const uint16_t* x, const uint16_t* __restrict__ w,
 // mean = sum(x)/H ; var = sum((x-mean)^2)/H ; rstd = rsqrt(var + eps)
 // y <- bf16((x - mean) * rstd * gamma + beta)
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
+__global__ void __launch_bounds__(Geo<H, PRE>::TPR * Geo<H, PRE>::RPC, FwdMinBlocks<H, PRE>::v)
 layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                   const uint16_t* x, const uint16_t* __restrict__ gamma,
                   const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
-    using G = Geo<H>;
+    using G = Geo<H, PRE>;
     __shared__ float red1[G::RPC * G::W];
     __shared__ float red2[G::RPC * G::W];
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
@@ -302,11 +305,11 @@ layernorm_fwd_reg(uint16_t* y, float* __restrict__ mean_out, float* __restrict__
 // sum d^2 - (sum d)^2 / n costs at most about n fp32 roundings relative to
 // M2 (n <= 1024 here): far below the bf16 output rounding.
 template <int H, bool PRE>
-__global__ void __launch_bounds__(Geo<H>::TPR * Geo<H>::RPC, FwdMinBlocks<H, PRE>::v)
+__global__ void __launch_bounds__(Geo<H, PRE>::TPR * Geo<H, PRE>::RPC, FwdMinBlocks<H, PRE>::v)
 layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
                     const uint16_t* x, const uint16_t* __restrict__ gamma,
                     const uint16_t* __restrict__ beta, int64_t rows, float eps, int64_t first_wave) {
-    using G = Geo<H>;
+    using G = Geo<H, PRE>;
     constexpr float kNW = 32.0f * G::VPT * kVec;  // elements per warp
     __shared__ float red[G::W > 1 ? G::RPC * G::W * 2 : 1];
     const int group = threadIdx.x / G::TPR, t = threadIdx.x % G::TPR;
@@ -394,9 +397,6 @@ layernorm_fwd_shift(uint16_t* y, float* __restrict__ mean_out, float* __restrict
 // over the resident row, or one shifted pass).
 constexpr bool kLnFwdShifted = true;
 
-// Calls of at most this many rows load their parameters before the first
-// row (ParamVecs with PRE).
-constexpr int64_t kPrefetchParamRows = 256;
 
 }  // namespace
 
@@ -416,11 +416,11 @@ int64_t first_wave_ctas(K kernel, int threads, int sms, int* slot) {
 
 cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, int64_t rows,
                              float eps, int grid, int sms, cudaStream_t st) {
-    const bool pre = rows <= kPrefetchParamRows;
+    const bool pre = rows <= kSmallCallRows;
     NF_HIDDEN_SWITCH(hidden, {
         static int occ[2] = {0, 0};
         const auto k = pre ? fused_add_rmsnorm_reg<H, true> : fused_add_rmsnorm_reg<H, false>;
-        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        const int threads = pre ? Geo<H, true>::TPR * Geo<H, true>::RPC : Geo<H>::TPR * Geo<H>::RPC;
         return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(x),
                                static_cast<uint16_t*>(res), static_cast<const uint16_t*>(w), rows,
                                eps, first_wave_ctas(k, threads, sms, &occ[pre]));
@@ -429,11 +429,11 @@ cudaError_t launch_fused_reg(int64_t hidden, void* x, void* res, const void* w, 
 
 cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w, int64_t rows,
                            float eps, int grid, int sms, cudaStream_t st) {
-    const bool pre = rows <= kPrefetchParamRows;
+    const bool pre = rows <= kSmallCallRows;
     NF_HIDDEN_SWITCH(hidden, {
         static int occ[2] = {0, 0};
         const auto k = pre ? rmsnorm_fwd_reg<H, true> : rmsnorm_fwd_reg<H, false>;
-        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        const int threads = pre ? Geo<H, true>::TPR * Geo<H, true>::RPC : Geo<H>::TPR * Geo<H>::RPC;
         return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(y),
                                static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w),
                                rows, eps, first_wave_ctas(k, threads, sms, &occ[pre]));
@@ -443,12 +443,12 @@ cudaError_t launch_rms_reg(int64_t hidden, void* y, const void* x, const void* w
 cudaError_t launch_ln_fwd_reg(int64_t hidden, void* y, float* mean, float* rstd, const void* x,
                               const void* gamma, const void* beta, int64_t rows, float eps,
                               int grid, int sms, cudaStream_t st) {
-    const bool pre = rows <= kPrefetchParamRows;
+    const bool pre = rows <= kSmallCallRows;
     NF_HIDDEN_SWITCH(hidden, {
         static int occ[2] = {0, 0};
         const auto k = kLnFwdShifted ? (pre ? layernorm_fwd_shift<H, true> : layernorm_fwd_shift<H, false>)
                                      : (pre ? layernorm_fwd_reg<H, true> : layernorm_fwd_reg<H, false>);
-        const int threads = Geo<H>::TPR * Geo<H>::RPC;
+        const int threads = pre ? Geo<H, true>::TPR * Geo<H, true>::RPC : Geo<H>::TPR * Geo<H>::RPC;
         return launch_with_pdl(k, dim3(grid), dim3(threads), 0, st, static_cast<uint16_t*>(y), mean,
                                rstd, static_cast<const uint16_t*>(x),
                                static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta),

@@ -12,6 +12,9 @@ namespace nf {
 // Row-group shape of the register path for `hidden`: threads per row,
 // rows per CTA.  False if `hidden` is not compiled.
 bool reg_shape(int64_t hidden, int* tpr, int* rpc);
+// Register-path forward calls of at most this many rows load their
+// parameters before the first row and run one row per CTA.
+constexpr int64_t kSmallCallRows = 256;
 // Cluster path: CTAs per row (the cluster size) and threads per CTA.
 bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);
 // Bulk path: threads per CTA (one producer warp group + consumer row

@@ -278,6 +278,8 @@ def test_forward_plans(hidden, rows):
         assert (hidden // 8) % tpr == 0          # static split into whole vectors
         assert 1 <= reg["grid"] <= 2 ** 31 - 1
         assert reg["grid"] == min(-(-rows // reg["rows_per_cta"]), 2 ** 31 - 1)
+        # calls of at most 256 rows run one row per CTA
+        assert (reg["rows_per_cta"] == 1) == (rows <= 256 or hidden >= 5120)
         st, cl = nf.nf_plan_compute(op, rows, hidden, sms, "cluster")
         assert st == nf.NF_OK
         assert cl["path"] == "cluster" and 2 <= cl["cluster"] <= 8
