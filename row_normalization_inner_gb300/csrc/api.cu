@@ -344,10 +344,12 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
             pl.partials = rb;
         }
     } else if (p == NF_PATH_REG && fwd) {
-        const int frpc = rows <= kSmallCallRows ? 1 : rpc;  // small calls: one row per CTA
+        // small calls: one row per CTA, twice the threads per row
+        const bool small = rows <= kSmallCallRows;
+        const int frpc = small ? 1 : rpc;
         const int64_t blocks = (rows + frpc - 1) / frpc;
         pl.grid = static_cast<int32_t>(blocks < kMaxGrid ? blocks : kMaxGrid);
-        pl.block = tpr * frpc;
+        pl.block = (small ? 2 * tpr : tpr) * frpc;
         pl.cluster = 1;
         pl.rows_per_cta = frpc;
         pl.launches = 1;

@@ -20,12 +20,15 @@
 namespace nf {
 namespace {
 
-// SMALL: the geometry of calls of at most kSmallCallRows rows, one row per
-// CTA so that a few rows spread over as many SMs (8 x 4096 fused: 2.0 ->
-// 1.6 us; at 16384 rows one row per CTA was slower at hidden 4096).
+// SMALL: the geometry of calls of at most kSmallCallRows rows: one row per
+// CTA, so that a few rows spread over as many SMs (8 x 4096 fused: 1.89 ->
+// 1.76 us; at 16384 rows one row per CTA was slower at hidden 4096), and
+// twice the threads per row, two vectors each, so each thread's chain of
+// loads and sums is shorter (fused 1 x 8192: 2.01 -> 1.79 us, 256 x 8192:
+// 3.97 -> 3.47 us).
 template <int H, bool SMALL = false>
 struct Geo {
-    static constexpr int TPR = RegShape<H>::TPR;
+    static constexpr int TPR = SMALL ? 2 * RegShape<H>::TPR : RegShape<H>::TPR;
     static constexpr int RPC = SMALL ? 1 : RegShape<H>::RPC;
     static constexpr int NV = H / kVec;
     static constexpr int VPT = NV / TPR;

@@ -13,7 +13,8 @@ namespace nf {
 // rows per CTA.  False if `hidden` is not compiled.
 bool reg_shape(int64_t hidden, int* tpr, int* rpc);
 // Register-path forward calls of at most this many rows load their
-// parameters before the first row and run one row per CTA.
+// parameters before the first row and run one row per CTA, with twice the
+// threads per row of larger calls.
 constexpr int64_t kSmallCallRows = 256;
 // Cluster path: CTAs per row (the cluster size) and threads per CTA.
 bool cluster_shape(int64_t hidden, int* ctas_per_row, int* threads);

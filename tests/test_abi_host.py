@@ -276,6 +276,8 @@ def test_forward_plans(hidden, rows):
         assert reg["block"] % 32 == 0 and reg["block"] <= 1024
         tpr = reg["block"] // reg["rows_per_cta"]
         assert (hidden // 8) % tpr == 0          # static split into whole vectors
+        # small calls: two vectors per thread, else four
+        assert (hidden // 8) // tpr == (2 if rows <= 256 else 4)
         assert 1 <= reg["grid"] <= 2 ** 31 - 1
         assert reg["grid"] == min(-(-rows // reg["rows_per_cta"]), 2 ** 31 - 1)
         # calls of at most 256 rows run one row per CTA
