@@ -122,7 +122,7 @@ constexpr bool kSplitApplyLastFirst = true;
 // OP: 0 fused add + RMSNorm, 1 RMSNorm, 2 LayerNorm.
 template <int OP>
 __global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict__ part, int nc) {
-    __shared__ float red[2][8 * 1];
+    __shared__ float red[(kSpT / 32) * 2];
     const int c = blockIdx.x, H = a.hidden;
     if (blockIdx.y < a.rows) {
         prefetch_chunk(a.in0, blockIdx.y, c, H);
@@ -143,33 +143,33 @@ __global__ void __launch_bounds__(kSpT) split_stats(DynArgs a, float* __restrict
         }
         float2 out;
         if constexpr (OP == 2) {
-            float s[1] = {0.f};
-#pragma unroll
-            for (int k = 0; k < kSpV; ++k)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s[0] += f[k][e];
-            cta_sum<1>(s, red[0]);
-            const float mean = s[0] / static_cast<float>(chunk_len(c, H));
-            float q[1] = {0.f};
+            // one reduction: the sums of d = x - K and d^2, K the chunk's first
+            // element (every thread reads it; one cached line), give the
+            // chunk's mean K + sum d / n and M2 = sum d^2 - (sum d)^2 / n
+            const float K = __uint_as_float(static_cast<uint32_t>(
+                                __ldg(a.in0 + r * H + static_cast<int64_t>(c) * kSpChunk)) << 16);
+            float q[2] = {0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < kSpV; ++k) {
                 if (c * kSpVecs + k * kSpT + static_cast<int>(threadIdx.x) < NV) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float d = f[k][e] - mean;
-                        q[0] = fmaf(d, d, q[0]);
+                        const float d = f[k][e] - K;
+                        q[0] += d;
+                        q[1] = fmaf(d, d, q[1]);
                     }
                 }
             }
-            cta_sum<1>(q, red[1]);
-            out = make_float2(mean, q[0]);
+            cta_sum<2>(q, red);
+            const float dm = q[0] / static_cast<float>(chunk_len(c, H));
+            out = make_float2(K + dm, fmaxf(q[1] - q[0] * dm, 0.f));
         } else {
             float q[1] = {0.f};
 #pragma unroll
             for (int k = 0; k < kSpV; ++k)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) q[0] = fmaf(f[k][e], f[k][e], q[0]);
-            cta_sum<1>(q, red[0]);
+            cta_sum<1>(q, red);
             out = make_float2(q[0], 0.f);
         }
         if (threadIdx.x == 0) reinterpret_cast<float2*>(part)[r * nc + c] = out;
