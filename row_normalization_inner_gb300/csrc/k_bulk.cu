@@ -109,8 +109,8 @@ struct BGeo {
     static constexpr int LAUNCH_REGS = LAUNCH_REGS0 > 248 ? 248 : LAUNCH_REGS0;
     static constexpr int CONS_REGS0 = (LAUNCH_REGS * THREADS - 128 * kProducerRegs) / NCT / 8 * 8;
     static constexpr int CONS_REGS = CONS_REGS0 > 248 ? 248 : CONS_REGS0;
-    // reduction scratch per group: 4 buffers (2 row parities x 2 reductions) x GW x 3 floats
-    static constexpr int RED_PER_GROUP = 4 * GW * 3;
+    // reduction scratch per group: one buffer per row parity, GW x 3 floats each
+    static constexpr int RED_PER_GROUP = 2 * GW * 3;
     // dynamic shared memory layout
     static constexpr int RING = S * STAGE_BYTES;
     static constexpr int BAR_OFF = RING;                     // full[S], empty[S]
@@ -346,10 +346,12 @@ norm_bulk_kernel(BulkArgs a) {
             if constexpr (OpIO<OP>::NIN >= 2) v1[k] = lds128(st + G::ROW_BYTES + (k * G::GT + gt) * 16);
             if constexpr (OpIO<OP>::NIN == 3) v2[k] = lds128(st + 2 * G::ROW_BYTES + (k * G::GT + gt) * 16);
         }
+        // LayerNorm shift: the row's first element, read before the stage is released
+        float c = 0.f;
+        if constexpr (OP == kLnFwd) c = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(st));
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled now
-        float* rb0 = red + ((j & 1) * 2 + 0) * G::GW * 3;
-        float* rb1 = red + ((j & 1) * 2 + 1) * G::GW * 3;
+        float* rb0 = red + (j & 1) * G::GW * 3;
 
         if constexpr (OP == kFused || OP == kRms) {
             float2 f[G::VPT][4];
@@ -386,31 +388,34 @@ norm_bulk_kernel(BulkArgs a) {
                 st_stream(a.out0 + row * H + (k * G::GT + gt) * kVec, pack8x2(o));
             }
         } else if constexpr (OP == kLnFwd) {
+            // one reduction of the shifted sums: with d = x - c,
+            // mean = c + sum d / H and var = sum d^2 / H - (sum d / H)^2
             float2 f[G::VPT][4];
-            float2 s1 = make_float2(0.f, 0.f);
+            const float2 nc2 = make_float2(-c, -c);
+            float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
                 unpack8x2(v0[k], f[k]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) s1 = __fadd2_rn(s1, f[k][q]);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 d = __fadd2_rn(f[k][q], nc2);
+                    s1 = __fadd2_rn(s1, d);
+                    s2 = __ffma2_rn(d, d, s2);
+                }
             }
-            float v[1 + NF] = {s1.x + s1.y};
-            if constexpr (NF) v[1] = fail;
-            group_reduce<G::GW, 1 + NF>(v, rb0, gwarp, lane, gid);
+            float v[2 + NF] = {s1.x + s1.y, s2.x + s2.y};
+            if constexpr (NF) v[2] = fail;
+            group_reduce<G::GW, 2 + NF>(v, rb0, gwarp, lane, gid);
             if (group_failed<NF>(v, ok)) { failed = true; break; }
-            const float mean = v[0] * (1.0f / H);
+            const float dm = v[0] * (1.0f / H);
+            const float mean = c + dm;
+            const float var = fmaxf(v[1] * (1.0f / H) - dm * dm, 0.f);
+            const float rstd = rsqrtf(var + a.eps);
             const float2 nmean2 = make_float2(-mean, -mean);
-            float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    f[k][q] = __fadd2_rn(f[k][q], nmean2);  // the row, centered in place
-                    s2 = __ffma2_rn(f[k][q], f[k][q], s2);
-                }
-            float sq[1] = {s2.x + s2.y};
-            group_reduce<G::GW, 1>(sq, rb1, gwarp, lane, gid);
-            const float rstd = rsqrtf(sq[0] * (1.0f / H) + a.eps);
+                for (int q = 0; q < 4; ++q) f[k][q] = __fadd2_rn(f[k][q], nmean2);  // the row, centered
             const float2 rstd2 = make_float2(rstd, rstd);
 #pragma unroll
             for (int k = 0; k < G::VPT; ++k) {
