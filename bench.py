@@ -471,10 +471,17 @@ def op_case(nf, op, rows, hidden, eps, l2_bytes, dev="cuda"):
     return launch, sets, nbytes
 
 
-def time_op(nf, op, rows, hidden, eps, l2_bytes, stream, min_launches=20):
+def time_op(nf, op, rows, hidden, eps, l2_bytes, stream, min_launches=20, path=None):
+    """Graph-timed device time of `op` at (rows, hidden); with `path` the
+    kernel family is forced while the launches are captured (the inputs are
+    prepared under the automatic choice)."""
     launch, sets, nbytes = op_case(nf, op, rows, hidden, eps, l2_bytes)
     n = max(sets, min_launches)
-    ms = graph_time_ms(launch, n, stream)
+    if path is None:
+        ms = graph_time_ms(launch, n, stream)
+    else:
+        with nf.forced_path(path):
+            ms = graph_time_ms(launch, n, stream)
     del launch
     torch.cuda.empty_cache()
     return ms, nbytes
@@ -488,11 +495,7 @@ def ops_suite(nf, peak, stream, l2_bytes):
     out = {}
 
     def entry(op, rows, h, eps, path=None):
-        if path is None:
-            ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
-        else:
-            with nf.forced_path(path):
-                ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream)
+        ms, nbytes = time_op(nf, op, rows, h, eps, l2_bytes, stream, path=path)
         gbs = nbytes / (ms * 1e-3) / 1e9
         if op.startswith("floor"):
             used = "probe"
@@ -537,9 +540,15 @@ def ops_suite(nf, peak, stream, l2_bytes):
     for rows, h in ((16384, 1024), (16384, 4096), (65536, 1024), (4096, 8192)):
         entry("outer_norm_fwd", rows, h, EPS)
         entry("outer_norm_bwd", rows, h, EPS)
-    # rows longer than a cluster holds: the split family
-    for op in ("rmsnorm_fwd", "layernorm_fwd", "fused_add_rmsnorm", "layernorm_bwd", "rmsnorm_bwd"):
+    # rows longer than a cluster holds: the automatic choice (the grid
+    # family where the rows fit on chip, the split family for the RMSNorm
+    # backward), and the other of the two forced
+    for op in ("rmsnorm_fwd", "layernorm_fwd", "fused_add_rmsnorm", "layernorm_bwd", "rmsnorm_bwd",
+               "fused_add_rmsnorm_bwd"):
         entry(op, 4, 1 << 22, EPS)
+        plan_op = "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op
+        auto = nf.nf_plan_query(plan_op, 4, 1 << 22)["path"]
+        entry(op, 4, 1 << 22, EPS, path="split" if auto == "grid" else "grid")
     # hidden sizes with no compiled kernel: the runtime-hidden family
     for h in (3072, 6144):
         for op in ("fused_add_rmsnorm", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):

@@ -117,14 +117,35 @@ typedef struct CUstream_st* nf_stream;
  *              any number of CTAs ("Llu/ln bwd"), for rows longer than a
  *              cluster holds (any multiple of 8 up to NF_SPLIT_MAX_HIDDEN).
  *              Forward calls on this family need a workspace: use the _ws
- *              entry points and nf_workspace_size.                          */
+ *              entry points and nf_workspace_size.
+ *   GRID    -- the split family's rows held on chip: one cooperative launch
+ *              of one 512-thread CTA per SM; CTA c keeps its slice of
+ *              ceil(hidden / 8 / SMs) vectors of EVERY row in shared memory,
+ *              the CTAs exchange the per-row partial sums through the
+ *              workspace across one grid barrier (a bounded wait: if it runs
+ *              out the kernel records NF_ERR_TIMEOUT in the device status
+ *              word and returns), and every CTA adds them in the same fixed
+ *              order.  Each input row is read from memory once (the
+ *              backward reads dy a second time, from L2), and a column's
+ *              every row is in one CTA, so the backward writes
+ *              dgamma / dbeta (dw) directly.  For 1 to 8 rows whose slices
+ *              fit (rows * ceil(hidden / 8 / SMs) * 16 bytes within about
+ *              226 KB): on GB300 up to 4 rows of 4194304 or 8 of 2097152.
+ *              The automatic choice takes it wherever the split family
+ *              would run and the rows fit, except for the RMSNorm backward
+ *              (the split family's apply pass measured faster there).
+ *              Forward calls need a workspace, as for SPLIT.  The fused op normalizes the residual as
+ *              stored (bf16), the literal reading of the in-place update;
+ *              the other families normalize the fp32 sum (both are within
+ *              the stated tolerance of the exact result).                   */
 typedef enum {
     NF_PATH_AUTO = 0,
     NF_PATH_REG = 1,
     NF_PATH_CLUSTER = 2,
     NF_PATH_BULK = 3,
     NF_PATH_DYNAMIC = 4,
-    NF_PATH_SPLIT = 5
+    NF_PATH_SPLIT = 5,
+    NF_PATH_GRID = 6
 } nf_path;
 
 /* Longest row any family handles (the split family). */
@@ -367,6 +388,15 @@ nf_status nf_get_device_status(nf_stream stream);
  * NF_ERR_TIMEOUT in the device status word and returns normally; the
  * context stays usable. */
 nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream);
+
+/* Test hook for the grid family's barrier: launch two cooperative CTAs that
+ * wait at the grid barrier for a third CTA that does not exist, giving up
+ * after `timeout_ns` nanoseconds (clamped to [1e3, 1e9]).  `workspace`: 16
+ * bytes of device memory, 16-byte aligned, for the arrival counter (zeroed
+ * on `stream` first).  The kernel records NF_ERR_TIMEOUT in the device
+ * status word and returns normally.  NF_ERR_INVALID_ARG (null) or
+ * NF_ERR_MISALIGNED before launching anything. */
+nf_status nf_selftest_grid_timeout(void* workspace, int64_t timeout_ns, nf_stream stream);
 
 /* Measurement hook: the launch floor set beside small-batch timings.
  * kind 0 launches one 32-thread CTA that only waits for the previous

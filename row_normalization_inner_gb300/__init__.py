@@ -31,10 +31,10 @@ NF_ERR_CUDA = 5
 NF_ERR_TIMEOUT = 6
 NF_ERR_UNSUPPORTED_PATH = 7
 
-NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_SPLIT = \
-    0, 1, 2, 3, 4, 5
+NF_PATH_AUTO, NF_PATH_REG, NF_PATH_CLUSTER, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_SPLIT, \
+    NF_PATH_GRID = 0, 1, 2, 3, 4, 5, 6
 PATHS = {"auto": NF_PATH_AUTO, "reg": NF_PATH_REG, "cluster": NF_PATH_CLUSTER, "bulk": NF_PATH_BULK,
-         "dynamic": NF_PATH_DYNAMIC, "split": NF_PATH_SPLIT}
+         "dynamic": NF_PATH_DYNAMIC, "split": NF_PATH_SPLIT, "grid": NF_PATH_GRID}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 
 NF_OP_FUSED_ADD_RMSNORM, NF_OP_RMSNORM_FWD, NF_OP_LAYERNORM_FWD, NF_OP_LAYERNORM_BWD, \
@@ -48,6 +48,7 @@ DYN_MAX_HIDDEN_BWD = 16384
 LONG_MAX_HIDDEN_FWD = 262144  # grid-parallel cluster path for longer rows
 LONG_MAX_HIDDEN_BWD = 131072
 SPLIT_MAX_HIDDEN = 1 << 26    # NF_SPLIT_MAX_HIDDEN: rows across any number of CTAs
+GRID_MAX_ROWS = 8             # the grid family (rows held on chip) takes 1 to 8 rows
 
 # Every symbol include/nf.h declares.
 EXPORTS = (
@@ -58,7 +59,8 @@ EXPORTS = (
     "nf_fused_add_rmsnorm_bwd", "nf_workspace_size", "nf_fused_add_rmsnorm_ws", "nf_rmsnorm_fwd_ws",
     "nf_layernorm_fwd_ws",
     "nf_set_path", "nf_plan_query", "nf_plan_compute", "nf_get_device_status",
-    "nf_selftest_wait_timeout", "nf_selftest_floor", "nf_status_string", "nf_version",
+    "nf_selftest_wait_timeout", "nf_selftest_grid_timeout", "nf_selftest_floor", "nf_status_string",
+    "nf_version",
 )
 
 
@@ -112,6 +114,7 @@ def _bind(lib):
         "nf_plan_compute": (_S, [_S, _I64, _I64, ctypes.c_int32, _S, ctypes.POINTER(Plan)]),
         "nf_get_device_status": (_S, [_P]),
         "nf_selftest_wait_timeout": (_S, [_I64, _P]),
+        "nf_selftest_grid_timeout": (_S, [_P, _I64, _P]),
         "nf_selftest_floor": (_S, [ctypes.c_int32, _P, _P, _I64, _P]),
         "nf_status_string": (ctypes.c_char_p, [_S]),
         "nf_version": (ctypes.c_char_p, []),
@@ -265,6 +268,10 @@ def nf_selftest_wait_timeout(timeout_ns, stream) -> int:
     return lib().nf_selftest_wait_timeout(timeout_ns, stream)
 
 
+def nf_selftest_grid_timeout(workspace, timeout_ns, stream) -> int:
+    return lib().nf_selftest_grid_timeout(workspace, timeout_ns, stream)
+
+
 def nf_selftest_floor(kind, dst, src, nbytes, stream) -> int:
     return lib().nf_selftest_floor(kind, dst, src, nbytes, stream)
 
@@ -303,11 +310,11 @@ def _rows_hidden(x):
 def _fwd_workspace(op, rows, hidden, device, workspace):
     """(pointer, bytes) of the workspace a forward call needs now: a caller
     tensor if given, else one allocated here (by PyTorch) only when the
-    plan is the split family."""
+    plan is the split or grid family."""
     import torch
     if workspace is not None:
         return workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    if rows == 0 or nf_plan_query(op, rows, hidden)["path"] != "split":
+    if rows == 0 or nf_plan_query(op, rows, hidden)["path"] not in ("split", "grid"):
         return None, 0
     n = nf_workspace_size(OPS[op], rows, hidden)
     # freed right after the launch: PyTorch's allocator hands the block to

@@ -172,6 +172,19 @@ nf_status common_checks(nf_op op, int64_t rows, int64_t hidden, float eps, bool 
 
 nf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NF_OK : NF_ERR_CUDA; }
 
+// The split and grid families: the launch of a planned call.
+nf_status launch_split_family(const nf_plan& pl, nf_op op, const DynArgs& a, void* workspace,
+                              cudaStream_t s) {
+    int sms;
+    if (nf_status st = device_sm_count(&sms)) return st;
+    if (pl.path == NF_PATH_GRID) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        return from_cuda(launch_grid(op, a, workspace, sms, status, s));
+    }
+    return from_cuda(launch_split(op, a, workspace, sms, s));
+}
+
 nf_status plan_for_call(nf_op op, int64_t rows, int64_t hidden, nf_plan* plan) {
     int sms;
     if (nf_status st = device_sm_count(&sms)) return st;
@@ -179,12 +192,12 @@ nf_status plan_for_call(nf_op op, int64_t rows, int64_t hidden, nf_plan* plan) {
                            static_cast<nf_path>(g_forced_path.load(std::memory_order_relaxed)), plan);
 }
 
-// The plan of a forward call.  Without a workspace, an automatic split plan
+// The plan of a forward call.  Without a workspace, an automatic split (or grid) plan
 // falls back to the cluster family where that holds the row, so the plain
 // forward entry points keep working up to the cluster limit.
 nf_status plan_for_fwd(nf_op op, int64_t rows, int64_t hidden, bool have_ws, nf_plan* plan) {
     if (nf_status st = plan_for_call(op, rows, hidden, plan)) return st;
-    if (have_ws || plan->path != NF_PATH_SPLIT ||
+    if (have_ws || (plan->path != NF_PATH_SPLIT && plan->path != NF_PATH_GRID) ||
         g_forced_path.load(std::memory_order_relaxed) != NF_PATH_AUTO)
         return NF_OK;
     int sms;
@@ -201,7 +214,7 @@ size_t any_path_workspace_bytes(nf_op op, int64_t rows, int64_t hidden) {
     int sms;
     if (device_sm_count(&sms) != NF_OK) return 0;
     size_t most = 0;
-    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER, NF_PATH_SPLIT}) {
+    for (nf_path p : {NF_PATH_REG, NF_PATH_BULK, NF_PATH_DYNAMIC, NF_PATH_CLUSTER, NF_PATH_SPLIT, NF_PATH_GRID}) {
         nf_plan pl;
         if (nf_plan_compute(op, rows, hidden, sms, p, &pl) != NF_OK) continue;
         const size_t b = plan_workspace_bytes(op, rows, hidden, sms, pl.path, pl.partials);
@@ -273,6 +286,7 @@ floor_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, int64_
 
 size_t plan_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms, int path, int partials) {
     if (path == NF_PATH_SPLIT) return split_workspace_bytes(op, rows, hidden, sms);
+    if (path == NF_PATH_GRID) return grid_workspace_bytes(op, rows, hidden, sms);
     if (op == NF_OP_LAYERNORM_BWD || op == NF_OP_RMSNORM_BWD)
         return static_cast<size_t>(partials) * bwd_planes(static_cast<nf_op>(op)) *
                static_cast<size_t>(hidden) * sizeof(float);
@@ -294,7 +308,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
                           nf_plan* out) {
     if (!out || rows < 0 || sm_count < 1) return NF_ERR_INVALID_ARG;
     if (op < NF_OP_FUSED_ADD_RMSNORM || op > NF_OP_RMSNORM_BWD) return NF_ERR_INVALID_ARG;
-    if (path < NF_PATH_AUTO || path > NF_PATH_SPLIT) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_GRID) return NF_ERR_INVALID_ARG;
     const bool fwd = op == NF_OP_FUSED_ADD_RMSNORM || op == NF_OP_RMSNORM_FWD ||
                      op == NF_OP_LAYERNORM_FWD;
     int tpr = 0, rpc = 1, dyn_threads = 0, long_c = 0, long_t = 0, long_slice = 0;
@@ -302,15 +316,24 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
     const bool dyn_ok = dyn_shape(op, hidden, &dyn_threads);
     const bool long_ok = long_shape(op, hidden, &long_c, &long_t, &long_slice);
     const bool splittable = split_ok(hidden);
+    int grid_vc = 0;
+    size_t grid_smem = 0;
+    const bool grid_fits = grid_shape(op, rows, hidden, sm_count, &grid_vc, &grid_smem);
     if (!compiled && !dyn_ok && !long_ok && !splittable) return NF_ERR_UNSUPPORTED_HIDDEN;
 
     nf_path p = path;
     if (p == NF_PATH_AUTO)
         // beyond the runtime-hidden limits the split family beat the
-        // cluster kernels at every measured row count (1.1-2.3x)
+        // cluster kernels at every measured row count (1.1-2.3x); where the
+        // rows fit on chip the grid family beat it for the forward ops and
+        // the LayerNorm backward (the RMSNorm backward keeps the split
+        // family's copy-ring apply pass, which measured faster)
         p = compiled ? auto_path(op, rows, hidden, rpc, sm_count)
-                     : dyn_ok ? NF_PATH_DYNAMIC : splittable ? NF_PATH_SPLIT : NF_PATH_CLUSTER;
+            : dyn_ok ? NF_PATH_DYNAMIC
+            : splittable ? (grid_fits && op != NF_OP_RMSNORM_BWD ? NF_PATH_GRID : NF_PATH_SPLIT)
+                         : NF_PATH_CLUSTER;
     if (p == NF_PATH_SPLIT && !splittable) return NF_ERR_UNSUPPORTED_PATH;
+    if (p == NF_PATH_GRID && !grid_fits) return NF_ERR_UNSUPPORTED_PATH;
     if ((p == NF_PATH_REG || p == NF_PATH_BULK) && !compiled) return NF_ERR_UNSUPPORTED_PATH;
     if (p == NF_PATH_DYNAMIC && !dyn_ok) return NF_ERR_UNSUPPORTED_PATH;
     // the cluster family: the static kernels for compiled forward sizes,
@@ -322,7 +345,17 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
     std::memset(&pl, 0, sizeof pl);
     pl.path = p;
     constexpr int64_t kMaxGrid = 0x7FFFFFFF;
-    if (p == NF_PATH_SPLIT) {
+    if (p == NF_PATH_GRID) {
+        // one cooperative launch, one CTA per SM holding its column slice of
+        // every row; the backward writes dgamma / dbeta (dw) itself
+        pl.grid = sm_count;
+        pl.block = 512;
+        pl.cluster = 1;
+        pl.rows_per_cta = static_cast<int32_t>(rows);
+        pl.smem_bytes = static_cast<int32_t>(grid_smem);
+        pl.launches = 1;
+        pl.partials = fwd ? 0 : 1;
+    } else if (p == NF_PATH_SPLIT) {
         int nc, rb;
         split_shape(op, rows, hidden, sm_count, &nc, &rb);
         const int64_t ry = rows < 65535 ? (rows > 0 ? rows : 1) : 65535;
@@ -431,7 +464,7 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
 }
 
 nf_status nf_set_path(nf_path path) {
-    if (path < NF_PATH_AUTO || path > NF_PATH_SPLIT) return NF_ERR_INVALID_ARG;
+    if (path < NF_PATH_AUTO || path > NF_PATH_GRID) return NF_ERR_INVALID_ARG;
     g_forced_path.store(path, std::memory_order_relaxed);
     return NF_OK;
 }
@@ -469,7 +502,7 @@ nf_status nf_fused_add_rmsnorm_ws(void* x, void* residual, const void* weight, i
     if (nf_status st = plan_for_fwd(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, workspace != nullptr, &pl))
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_SPLIT) {
+    if (pl.path == NF_PATH_SPLIT || pl.path == NF_PATH_GRID) {
         size_t need;
         if (nf_status st = check_workspace(NF_OP_FUSED_ADD_RMSNORM, rows, hidden, pl, workspace,
                                            workspace_bytes, &need))
@@ -486,9 +519,7 @@ nf_status nf_fused_add_rmsnorm_ws(void* x, void* residual, const void* weight, i
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
-        int sms;
-        if (nf_status st = device_sm_count(&sms)) return st;
-        return from_cuda(launch_split(NF_OP_FUSED_ADD_RMSNORM, a, workspace, sms, s));
+        return launch_split_family(pl, NF_OP_FUSED_ADD_RMSNORM, a, workspace, s);
     }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_fused_cluster(hidden, x, residual, weight, rows, eps, pl.grid, s));
@@ -534,7 +565,7 @@ nf_status nf_rmsnorm_fwd_ws(void* y, const void* x, const void* weight, int64_t 
     if (nf_status st = plan_for_fwd(NF_OP_RMSNORM_FWD, rows, hidden, workspace != nullptr, &pl))
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_SPLIT) {
+    if (pl.path == NF_PATH_SPLIT || pl.path == NF_PATH_GRID) {
         size_t need;
         if (nf_status st = check_workspace(NF_OP_RMSNORM_FWD, rows, hidden, pl, workspace,
                                            workspace_bytes, &need))
@@ -549,9 +580,7 @@ nf_status nf_rmsnorm_fwd_ws(void* y, const void* x, const void* weight, int64_t 
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
-        int sms;
-        if (nf_status st = device_sm_count(&sms)) return st;
-        return from_cuda(launch_split(NF_OP_RMSNORM_FWD, a, workspace, sms, s));
+        return launch_split_family(pl, NF_OP_RMSNORM_FWD, a, workspace, s);
     }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_rms_cluster(hidden, y, x, weight, rows, eps, pl.grid, s));
@@ -604,7 +633,7 @@ nf_status nf_layernorm_fwd_ws(void* y, float* mean, float* rstd, const void* x, 
     if (nf_status st = plan_for_fwd(NF_OP_LAYERNORM_FWD, rows, hidden, workspace != nullptr, &pl))
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (pl.path == NF_PATH_SPLIT) {
+    if (pl.path == NF_PATH_SPLIT || pl.path == NF_PATH_GRID) {
         size_t need;
         if (nf_status st = check_workspace(NF_OP_LAYERNORM_FWD, rows, hidden, pl, workspace,
                                            workspace_bytes, &need))
@@ -623,9 +652,7 @@ nf_status nf_layernorm_fwd_ws(void* y, float* mean, float* rstd, const void* x, 
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
-        int sms;
-        if (nf_status st = device_sm_count(&sms)) return st;
-        return from_cuda(launch_split(NF_OP_LAYERNORM_FWD, a, workspace, sms, s));
+        return launch_split_family(pl, NF_OP_LAYERNORM_FWD, a, workspace, s);
     }
     if (pl.path == NF_PATH_CLUSTER && hidden_ok(hidden))
         return from_cuda(launch_ln_fwd_cluster(hidden, y, mean, rstd, x, gamma, beta, rows, eps,
@@ -722,7 +749,8 @@ nf_status layernorm_bwd_impl(void* dx, float* dgamma, float* dbeta, const void* 
         if (nf_status st = scratch(&workspace)) return st;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT ||
+        pl.path == NF_PATH_GRID) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -734,12 +762,12 @@ nf_status layernorm_bwd_impl(void* dx, float* dgamma, float* dbeta, const void* 
         a.rows = rows;
         a.hidden = static_cast<int>(hidden);
         int sms = 0;
-        if (pl.path == NF_PATH_SPLIT) {
+        if (pl.path == NF_PATH_SPLIT || pl.path == NF_PATH_GRID) {
             if (nf_status st = device_sm_count(&sms)) return st;
             if (pl.partials == 1) {  // one row block: no column reduction
                 a.cols0 = dgamma;
                 a.cols1 = dbeta;
-                return from_cuda(launch_split(NF_OP_LAYERNORM_BWD, a, workspace, sms, s));
+                return launch_split_family(pl, NF_OP_LAYERNORM_BWD, a, workspace, s);
             }
         }
         const cudaError_t e =
@@ -803,7 +831,8 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         if (dx_clash || overlap(sdw, in) || overlap(sws, in)) return NF_ERR_INVALID_ARG;
     }
     float* ws = static_cast<float*>(workspace);
-    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT) {
+    if (pl.path == NF_PATH_DYNAMIC || pl.path == NF_PATH_CLUSTER || pl.path == NF_PATH_SPLIT ||
+        pl.path == NF_PATH_GRID) {
         DynArgs a{};
         a.out0 = static_cast<uint16_t*>(dx);
         a.in0 = static_cast<const uint16_t*>(x);
@@ -815,11 +844,11 @@ nf_status rms_bwd(void* dx, float* dw, const void* dy, const void* x, const void
         a.hidden = static_cast<int>(hidden);
         a.eps = eps;
         int sms = 0;
-        if (pl.path == NF_PATH_SPLIT) {
+        if (pl.path == NF_PATH_SPLIT || pl.path == NF_PATH_GRID) {
             if (nf_status st = device_sm_count(&sms)) return st;
             if (pl.partials == 1) {  // one row block: no column reduction
                 a.cols0 = dw;
-                return from_cuda(launch_split(NF_OP_RMSNORM_BWD, a, workspace, sms, s));
+                return launch_split_family(pl, NF_OP_RMSNORM_BWD, a, workspace, s);
             }
         }
         const cudaError_t e =
@@ -960,6 +989,17 @@ nf_status nf_selftest_wait_timeout(int64_t timeout_ns, nf_stream stream) {
     if (timeout_ns < 1000) timeout_ns = 1000;
     if (timeout_ns > 1000000000) timeout_ns = 1000000000;
     return from_cuda(launch_wait_selftest(addr, static_cast<uint64_t>(timeout_ns),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nf_status nf_selftest_grid_timeout(void* workspace, int64_t timeout_ns, nf_stream stream) {
+    if (!workspace) return NF_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return NF_ERR_MISALIGNED;
+    int* addr;
+    if (nf_status st = device_status_addr(&addr)) return st;
+    if (timeout_ns < 1000) timeout_ns = 1000;
+    if (timeout_ns > 1000000000) timeout_ns = 1000000000;
+    return from_cuda(launch_grid_selftest(workspace, static_cast<uint64_t>(timeout_ns), addr,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 

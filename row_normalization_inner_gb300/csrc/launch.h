@@ -138,6 +138,18 @@ bool split_shape(int op, int64_t rows, int64_t hidden, int sms, int* nchunks, in
 size_t split_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms);
 cudaError_t launch_split(int op, const DynArgs& a, void* workspace, int sms, cudaStream_t st);
 
+// Grid-resident rows (one cooperative launch, one CTA per SM, each holding
+// its column slice of every row in shared memory across a bounded grid
+// barrier): calls of at most kGridMaxRows rows whose slices fit.  *vc:
+// 8-element vectors per CTA per row; *smem: dynamic shared memory per CTA.
+constexpr int kGridMaxRows = 8;
+bool grid_shape(int op, int64_t rows, int64_t hidden, int sms, int* vc, size_t* smem);
+size_t grid_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms);
+cudaError_t launch_grid(int op, const DynArgs& a, void* workspace, int sms, int* status, cudaStream_t st);
+// Test hook: two cooperative CTAs wait at the grid barrier for a third that
+// never comes; the bounded wait runs out and records NF_ERR_TIMEOUT.
+cudaError_t launch_grid_selftest(void* counter16, uint64_t limit_ns, int* status, cudaStream_t st);
+
 // Workspace bytes the plan `pl` of (op, rows, hidden) needs on a device of
 // `sms` SMs (0 for forward plans that need none).
 size_t plan_workspace_bytes(int op, int64_t rows, int64_t hidden, int sms, int path, int partials);

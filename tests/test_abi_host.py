@@ -73,18 +73,41 @@ def test_unsupported_hidden(hidden):
     assert nf.nf_layernorm_bwd_workspace_size(4, hidden) == 0
 
 
+# The grid family's fit rule: 1 to 8 rows, each CTA (one per SM) holding
+# ceil(hidden / 8 / SMs) 16-byte vectors of every row in at most 227 KB of
+# shared memory less the kernel's 1104 bytes of static scratch.
+GRID_SMEM_LIMIT = 227 * 1024 - 1104
+
+
+def _grid_fits(rows, hidden, sms=152):
+    return 1 <= rows <= 8 and rows * -(-(hidden // 8) // sms) * 16 <= GRID_SMEM_LIMIT
+
+
+def _beyond_cluster(op, rows, hidden, sms=152):
+    """The automatic family past the runtime-hidden limits: grid where the
+    rows fit on chip (but never for the RMSNorm backward, whose split apply
+    pass measured faster), else split."""
+    return "grid" if _grid_fits(rows, hidden, sms) and op != "rmsnorm_bwd" else "split"
+
+
 def test_family_hidden_limits():
-    # runtime hidden up to 32768 / 16384, cluster up to 262144 / 131072, split beyond
+    # runtime hidden up to 32768 / 16384, cluster up to 262144 / 131072, split
+    # (grid when the rows fit on chip) beyond
     for h in (131080, 262144):
-        assert nf.nf_plan_compute("layernorm_bwd", 4, h, 152)[1]["path"] == "split"
-        assert nf.nf_plan_compute("rmsnorm_bwd", 4, h, 152)[1]["path"] == "split"
-    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262144, 152)[1]["path"] == "split"
+        for rows in (4, 9):
+            assert nf.nf_plan_compute("layernorm_bwd", rows, h, 152)[1]["path"] == \
+                ("grid" if rows == 4 else "split")
+            assert nf.nf_plan_compute("rmsnorm_bwd", rows, h, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262144, 152)[1]["path"] == "grid"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 9, 262144, 152)[1]["path"] == "split"
     assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262144, 152, "cluster")[1]["path"] == "cluster"
     assert nf.nf_plan_compute("rmsnorm_fwd", 4, 262152, 152, "cluster")[0] == \
         nf.NF_ERR_UNSUPPORTED_PATH
     assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32768, 152)[1]["path"] == "dynamic"
-    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32776, 152)[1]["path"] == "split"
-    assert nf.nf_plan_compute("layernorm_bwd", 4, 16392, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 32776, 152)[1]["path"] == "grid"
+    assert nf.nf_plan_compute("layernorm_bwd", 4, 16392, 152)[1]["path"] == "grid"
+    assert nf.nf_plan_compute("rmsnorm_fwd", 16, 32776, 152)[1]["path"] == "split"
+    assert nf.nf_plan_compute("layernorm_bwd", 16, 16392, 152)[1]["path"] == "split"
 
 
 @pytest.mark.parametrize("hidden", [32776, 40000, 65536, 131072, 200008, 262144])
@@ -94,8 +117,10 @@ def test_long_row_plans(hidden):
         if bwd and hidden > nf.LONG_MAX_HIDDEN_BWD:
             assert nf.nf_plan_compute(op, 16, hidden, 152)[1]["path"] == "split"
             continue
-        # automatic: the split family; forced: the cluster kernels
-        assert nf.nf_plan_compute(op, 7, hidden, 152)[1]["path"] == "split"
+        # automatic: the grid family (7 rows fit on chip), the split family
+        # for more rows; forced: the cluster kernels
+        assert nf.nf_plan_compute(op, 7, hidden, 152)[1]["path"] == _beyond_cluster(op, 7, hidden)
+        assert nf.nf_plan_compute(op, 9, hidden, 152)[1]["path"] == "split"
         for rows in (1, 7, 5000):
             st, p = nf.nf_plan_compute(op, rows, hidden, 152, "cluster")
             assert st == nf.NF_OK and p["path"] == "cluster", (op, hidden, p)
@@ -258,7 +283,7 @@ def test_rmsnorm_bwd_validation():
 
 def test_set_path_rejects_unknown():
     assert nf.nf_set_path(17) == nf.NF_ERR_INVALID_ARG
-    assert nf.nf_set_path(6) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(7) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(-1) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
 
@@ -437,14 +462,45 @@ def test_split_plans(hidden):
         # beyond the cluster limits the split family is the automatic choice
         limit = nf.LONG_MAX_HIDDEN_BWD if bwd else nf.LONG_MAX_HIDDEN_FWD
         if hidden > limit:
-            assert nf.nf_plan_compute(op, 2, hidden, 152)[1]["path"] == "split"
+            assert nf.nf_plan_compute(op, 2, hidden, 152)[1]["path"] == _beyond_cluster(op, 2, hidden)
+            assert nf.nf_plan_compute(op, 9, hidden, 152)[1]["path"] == "split"
             for path in ("reg", "bulk", "dynamic", "cluster"):
                 assert nf.nf_plan_compute(op, 2, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
 
 
+@pytest.mark.parametrize("hidden", [8, 1000, 65536, 270336, 1 << 20, 1 << 21, 1 << 22, 1 << 23])
+@pytest.mark.parametrize("sms", [152, 148, 132])
+def test_grid_plans(hidden, sms):
+    # one cooperative launch of one 512-thread CTA per SM, each holding
+    # ceil(hidden / 8 / SMs) vectors of every row; the backward writes its
+    # column sums itself (one "slot": the outputs)
+    vc = -(-(hidden // 8) // sms)
+    for op in OPS5:
+        bwd = op.endswith("_bwd")
+        for rows in (1, 2, 4, 5, 8, 9, 64):
+            st, p = nf.nf_plan_compute(op, rows, hidden, sms, "grid")
+            if not _grid_fits(rows, hidden, sms):
+                assert st == nf.NF_ERR_UNSUPPORTED_PATH, (op, rows, hidden)
+                continue
+            assert st == nf.NF_OK and p["path"] == "grid"
+            assert p["grid"] == sms and p["block"] == 512 and p["cluster"] == 1
+            assert p["rows_per_cta"] == rows and p["launches"] == 1
+            # the slices, and at least 116 KB (one CTA per SM whatever the registers)
+            assert rows * vc * 16 <= GRID_SMEM_LIMIT
+            assert p["smem_bytes"] == max(rows * vc * 16, 116 * 1024)
+            assert p["partials"] == (1 if bwd else 0)
+    # the bench shape: 4 rows of 4194304 fit at 152 SMs (220800 bytes per CTA)
+    assert nf.nf_plan_compute("rmsnorm_fwd", 4, 1 << 22, 152, "grid")[1]["smem_bytes"] == 220800
+    assert nf.nf_plan_compute("layernorm_bwd", 4, 1 << 22, 152)[1]["path"] == "grid"
+    assert nf.nf_plan_compute("rmsnorm_bwd", 4, 1 << 22, 152)[1]["path"] == "split"
+    # zero rows: nothing to hold
+    assert nf.nf_plan_compute("rmsnorm_fwd", 0, 1 << 20, 152, "grid")[0] == nf.NF_ERR_UNSUPPORTED_PATH
+
+
 def test_split_path_settable_and_workspace_queries_without_gpu():
     assert nf.nf_set_path(nf.NF_PATH_SPLIT) == nf.NF_OK
-    assert nf.nf_set_path(nf.NF_PATH_SPLIT + 1) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_set_path(nf.NF_PATH_GRID) == nf.NF_OK
+    assert nf.nf_set_path(nf.NF_PATH_GRID + 1) == nf.NF_ERR_INVALID_ARG
     assert nf.nf_set_path(nf.NF_PATH_AUTO) == nf.NF_OK
     # no device: the queries return 0 rather than failing
     if not HAVE_GPU:
@@ -473,7 +529,8 @@ def test_binding_constants_match_the_header():
     for name in ("NF_OK", "NF_ERR_INVALID_ARG", "NF_ERR_UNSUPPORTED_HIDDEN", "NF_ERR_MISALIGNED",
                  "NF_ERR_WORKSPACE_TOO_SMALL", "NF_ERR_CUDA", "NF_ERR_TIMEOUT",
                  "NF_ERR_UNSUPPORTED_PATH", "NF_PATH_AUTO", "NF_PATH_REG", "NF_PATH_CLUSTER",
-                 "NF_PATH_BULK", "NF_PATH_DYNAMIC", "NF_PATH_SPLIT", "NF_OP_FUSED_ADD_RMSNORM",
+                 "NF_PATH_BULK", "NF_PATH_DYNAMIC", "NF_PATH_SPLIT", "NF_PATH_GRID",
+                 "NF_OP_FUSED_ADD_RMSNORM",
                  "NF_OP_RMSNORM_FWD", "NF_OP_LAYERNORM_FWD", "NF_OP_LAYERNORM_BWD",
                  "NF_OP_RMSNORM_BWD"):
         assert getattr(nf, name) == h[name], name

@@ -8,8 +8,9 @@ them from a fixed scratch area inside the library.  This checks, through
 the C ABI, that on several calls in a row it returns exactly what
 nf_layernorm_bwd returns with a caller-owned workspace (the same kernels
 on the same plan, so bit for bit) and that both agree with the fp64
-oracle; and that a size needing more scratch than the area is refused
-before anything runs.  Named to be collected last."""
+oracle, including long rows on the grid family; and that a size needing
+more scratch than the area is refused before anything runs.  Named to be
+collected last."""
 import pytest
 import torch
 
@@ -65,11 +66,33 @@ def test_noalloc_matches_workspace_entry_point_and_oracle():
         check_f32(db, o_db, f"noalloc dbeta call {call}")
 
 
-def test_noalloc_refuses_sizes_beyond_the_area():
-    # rows of 2^22 elements run on the split family, whose column partials
-    # alone are 2 x 2^22 fp32 = 32 MiB per row block: more than the 16 MiB
-    # area on any device
+def test_noalloc_takes_long_rows_on_the_grid_family():
+    # 4 rows of 2^22 elements run on the grid family, whose workspace is the
+    # row partials only (rows x SMs float2): they fit the area
     rows, hidden = 4, 1 << 22
+    assert nf.nf_plan_query("layernorm_bwd", rows, hidden)["path"] == "grid"
+    x, dy, g, mean, rstd = _case(rows, hidden, seed=6)
+    dx = torch.empty_like(x)
+    dg = torch.empty(hidden, device="cuda")
+    db = torch.empty(hidden, device="cuda")
+    st = _noalloc(dx, dg, db, dy, x, mean, rstd, g, rows, hidden)
+    assert st == nf.NF_OK, nf.status_string(st)
+    torch.cuda.synchronize()
+    dx_ref, dg_ref, db_ref = nf.layernorm_bwd(dy, x, mean, rstd, g)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx_ref) and torch.equal(dg, dg_ref) and torch.equal(db, db_ref)
+    o_dx, o_dg, o_db = oracle.layernorm_bwd(dy, x, host_f64(mean), host_f64(rstd), g)
+    check_bf16(dx, o_dx, "noalloc grid dx")
+    check_f32(dg, o_dg, "noalloc grid dgamma")
+    check_f32(db, o_db, "noalloc grid dbeta")
+
+
+def test_noalloc_refuses_sizes_beyond_the_area():
+    # 9 rows of 2^22 elements run on the split family (more rows than the
+    # grid family holds), whose column partials alone are 2 x 2^22 fp32 =
+    # 32 MiB per row block: more than the 16 MiB area on any device
+    rows, hidden = 9, 1 << 22
+    assert nf.nf_plan_query("layernorm_bwd", rows, hidden)["path"] == "split"
     x, dy, g, mean, rstd = _case(rows, hidden, seed=7)
     dx = torch.full_like(x, 5.0)
     dg = torch.full((hidden,), 5.0, device="cuda")
