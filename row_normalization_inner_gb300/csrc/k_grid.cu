@@ -35,6 +35,7 @@
 
 namespace nf {
 
+// [kernel-span grid_norm] (with its barrier and copy helpers)
 // Arrivals at the grid barrier on this device, over all launches.  Every CTA
 // of a grid_norm launch adds 1 exactly once, and a launch occupies every SM
 // (one CTA per SM, the whole register file), so two launches never arrive
@@ -392,6 +393,8 @@ grid_norm(DynArgs a, float2* __restrict__ part, int vc, int* status) {
         }
     }
 }
+
+// [end kernel-span grid_norm]
 
 // Static shared memory of grid_norm (the reduction scratch, bounded by the
 // largest RM), left out of the dynamic budget below.

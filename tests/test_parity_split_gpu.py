@@ -195,12 +195,16 @@ def test_grid_fused(rows, hidden):
     # that stored value; both against the oracle's exact sum
     x, r, w = workloads.fused_inputs(rows, hidden, seed=rows + hidden, residual_scale=4.0)
     s_ref, y_ref, _ = oracle.fused_add_rmsnorm(x, r, w, 1e-5)
+    _, y_rnd, _ = oracle.fused_add_rmsnorm(x, r, w, 1e-5, normalize_rounded=True)
     xd, rd = x.cuda(), r.cuda()
     with nf.forced_path("grid"):
         assert nf.nf_plan_query("fused_add_rmsnorm", rows, hidden)["path"] == "grid"
         nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-5)
     torch.cuda.synchronize()
     check_bf16(xd, y_ref, f"grid fused {rows}x{hidden}")
+    # against the oracle's reading of normalizing the stored residual: one
+    # bf16 rounding apart at most
+    assert ulp_diff_bf16(xd, oracle.to_bf16(y_rnd)).max() <= 1
     d = ulp_diff_bf16(rd, oracle.to_bf16(s_ref))
     assert d.max() <= 1 and (d > 0).mean() < 1e-3
 
