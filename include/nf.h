@@ -337,7 +337,12 @@ nf_status nf_layernorm_bwd_noalloc(void* dx, float* dgamma, float* dbeta, const 
  * (Chan's pairwise formula), so results are deterministic.  workspace:
  * caller-owned, 16-byte aligned, at least
  * nf_outer_norm_workspace_size(rows, hidden) bytes, contents irrelevant.
- * y may be x itself. */
+ * y may be x itself.  Two forms: three streaming launches (statistics per
+ * row stripe, a merge per column, the apply pass), the default; and, with
+ * nf_set_path(NF_PATH_GRID), one cooperative launch that keeps each CTA's
+ * row stripe on chip band of columns by band and merges across bounded grid
+ * barriers (reads x once, but measured slower; NF_ERR_UNSUPPORTED_PATH when
+ * a stripe of rows / SMs rows does not fit two band buffers of 16 vectors). */
 size_t nf_outer_norm_workspace_size(int64_t rows, int64_t hidden);
 nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                             const void* beta, int64_t rows, int64_t hidden, float eps,

@@ -898,6 +898,20 @@ nf_status outer_checks(int64_t rows, int64_t hidden) {
     if (rows < 0 || rows > (INT64_MAX / 8) / hidden) return NF_ERR_INVALID_ARG;
     return NF_OK;
 }
+
+// Outer normalization's two forms: the three-launch streaming passes (the
+// automatic choice) and the grid family's single launch with the row
+// stripes on chip, forced with NF_PATH_GRID (it measured slower at every
+// size: 125-136 against 66 us at 16384 x 4096; its two grid barriers and
+// merge per band of columns leave DRAM idle between bands).  *grid says
+// which.
+nf_status outer_form(int64_t rows, int64_t hidden, int sms, bool* grid) {
+    const int forced = g_forced_path.load(std::memory_order_relaxed);
+    const bool fits = outer_grid_shape(rows, hidden, sms, nullptr, nullptr);
+    if (forced == NF_PATH_GRID && !fits) return NF_ERR_UNSUPPORTED_PATH;
+    *grid = forced == NF_PATH_GRID;
+    return NF_OK;
+}
 }  // namespace
 
 nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
@@ -912,6 +926,8 @@ nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, co
         return NF_ERR_MISALIGNED;
     int sms;
     if (nf_status st = device_sm_count(&sms)) return st;
+    bool grid;
+    if (nf_status st = outer_form(rows, hidden, sms, &grid)) return st;
     const size_t need = outer_workspace_bytes(rows, hidden, sms);
     if (workspace_bytes < need) return NF_ERR_WORKSPACE_TOO_SMALL;
     const int64_t act = rows * hidden * 2, par = hidden * 2, stat = hidden * 4;
@@ -926,6 +942,13 @@ nf_status nf_outer_norm_fwd(void* y, float* mean, float* rstd, const void* x, co
         if (overlap(o, sy) || overlap(o, sws) || overlap(o, ins[0]) || overlap(o, ins[1]) ||
             overlap(o, ins[2]))
             return NF_ERR_INVALID_ARG;
+    if (grid) {
+        int* status;
+        if (nf_status st = device_status_addr(&status)) return st;
+        return from_cuda(launch_outer_grid_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps,
+                                               workspace, sms, status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(launch_outer_fwd(y, mean, rstd, x, gamma, beta, rows, hidden, eps, workspace,
                                       sms, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -31,6 +31,7 @@
 // "residual += x; x = norm(residual) * w" with bf16 storage.
 #include "common.cuh"
 #include "launch.h"
+#include "pairs.cuh"
 #include "pdl.cuh"
 
 namespace nf {
@@ -440,6 +441,298 @@ cudaError_t launch_op(const DynArgs& a, float2* part, int vc, int sms, size_t sm
     return launch_coop<OP, 8, 1, ADD>(sms, smem, st, a, part, vc, status);
 }
 
+// ---- outer normalization with the matrix on chip, in column bands ----------
+// Per-column statistics over the rows, one read of x.  One cooperative launch
+// of one CTA per SM; CTA c owns the row stripe [r0, r0 + n) (rows / SMs,
+// the first rows % SMs stripes one row longer).  The columns are walked in
+// bands of `bvec` 16-byte vectors (bvec * 8 columns); each band of the
+// stripe is copied into one of two shared-memory buffers (row pitch bvec + 1
+// vectors, so reads down a column hit distinct banks) two bands ahead.  Per
+// band:
+//   statistics: thread t takes vector t / tpv of the band (tpv = 512 / bvec
+//     threads per vector) and rows t % tpv, t % tpv + tpv, ...; shifted sums
+//     per column (shift = its first value) give (count, mean, M2), merged
+//     across the tpv lanes with Chan's pairwise formula in a fixed tree; the
+//     CTA's partial per column goes to the workspace, then the CTA arrives
+//     at the first grid barrier;
+//   merge (after the first barrier): one warp per column over all warps of
+//     the grid (lanes take CTAs lane, lane + 32, ..., then a fixed shuffle
+//     tree) into mean, rstd and the affine pair a = rstd * gamma,
+//     b = beta - mean * a; second grid barrier;
+//   apply: every CTA reads the band's (a, b) and writes y = x * a + b from
+//     shared memory, in coalesced row segments.
+// The loop computes band k + 1's statistics and arrives before it applies
+// band k, so band k's stores drain while the grid gathers at the barrier.
+// Partials and pairs alternate between two workspace slots by band parity.
+
+constexpr int kOgMaxGrid = 256;  // CTAs (SMs) the column merge handles
+
+struct OuterGridArgs {
+    uint16_t* y;
+    const uint16_t* x;
+    const uint16_t* gamma;
+    const uint16_t* beta;
+    float* mean;        // per-column outputs, may be null
+    float* rstd;
+    float2* part;       // [2][SMs][bvec * 8]: the CTAs' (mean, M2) of a band
+    float2* ab;         // [2][bvec * 8]: a band's (a, b)
+    int64_t rows;
+    int hidden;
+    float eps;
+    int bvec;           // vectors per band (a power of two, 16 .. 512)
+};
+
+__device__ __forceinline__ void chan2(float& n, float& m, float& q, float nb, float mb, float qb) {
+    if (nb == 0.f) return;
+    if (n == 0.f) {
+        n = nb;
+        m = mb;
+        q = qb;
+        return;
+    }
+    const float nn = n + nb;
+    const float d = mb - m;
+    const float wb = nb / nn;
+    m += d * wb;
+    q += qb + d * d * n * wb;
+    n = nn;
+}
+
+// The grid barrier in two halves: every thread calls grid_arrive once its
+// writes are done (thread 0 publishes them and takes the ticket); later
+// every thread calls grid_wait, which returns false in every thread of a
+// CTA whose bounded wait ran out.  A CTA arrives at its next barrier only
+// after its wait on this one, so the arrival count still steps by whole
+// grids.
+__device__ __forceinline__ void grid_arrive(unsigned long long* arrivals, unsigned long long grid,
+                                            unsigned long long* target) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long ticket = atomicAdd(arrivals, 1ull);
+        *target = (ticket / grid + 1) * grid;
+    }
+}
+__device__ __forceinline__ bool grid_wait(unsigned long long* arrivals, const unsigned long long* target,
+                                          uint64_t limit_ns, int* status, int* give_up) {
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_ns();
+        int fail = 0;
+        while (ld_acquire_u64(arrivals) < *target) {
+            if (global_ns() - t0 > limit_ns) {
+                fail = 1;
+                break;
+            }
+        }
+        if (fail) record_status(status, kStatusTimeout);
+        *give_up = fail;
+        __threadfence();
+    }
+    __syncthreads();
+    return !*give_up;
+}
+
+__global__ void __launch_bounds__(kGrT, 1) outer_grid_fwd(OuterGridArgs g, int* status) {
+    extern __shared__ __align__(16) uint4 ob[];  // [2][stripe rows][bvec + 1], then (a, b) of a band
+    __shared__ int give_up;
+    __shared__ unsigned long long target;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int G = gridDim.x, c = blockIdx.x, H = g.hidden, NV = H / kVec;
+    const int bvec = g.bvec, pitch = bvec + 1, tpv = kGrT / bvec;
+    const int64_t base = g.rows / G;
+    const int rem = static_cast<int>(g.rows % G);
+    const int64_t r0 = c * base + (c < rem ? c : rem);
+    const int n = static_cast<int>(base + (c < rem ? 1 : 0));
+    const int rs = static_cast<int>(base + (rem ? 1 : 0));   // the longest stripe: buffer rows
+    uint4* const buf0 = ob;
+    uint4* const buf1 = ob + static_cast<int64_t>(rs) * pitch;
+    auto bufk = [&](int k) { return (k & 1) ? buf1 : buf0; };
+    float2* sab = reinterpret_cast<float2*>(ob + 2 * static_cast<int64_t>(rs) * pitch);
+    const int nb = (NV + bvec - 1) / bvec;                    // bands
+    const int BC = bvec * kVec;                               // columns per band
+    unsigned long long* arrivals = &g_grid_arrivals;
+    const unsigned long long grid = static_cast<unsigned long long>(G);
+    auto nvec = [&](int k) { return NV - k * bvec < bvec ? NV - k * bvec : bvec; };  // vectors of band k
+
+    // copy band k of the stripe into its buffer (thread t: vector t % bvec,
+    // rows t / bvec + (kGrT / bvec) * m: coalesced row segments)
+    auto issue = [&](int k) {
+        if (k < nb) {
+            const int vb = k * bvec, v = t % bvec;
+            if (vb + v < NV) {
+                uint4* dst = bufk(k);
+                const uint16_t* src = g.x + r0 * H + static_cast<int64_t>(vb + v) * kVec;
+                for (int i = t / bvec; i < n; i += tpv) gr_cp16(&dst[i * pitch + v], src + static_cast<int64_t>(i) * H);
+            }
+        }
+        gr_commit();
+    };
+    // the CTA's statistics of each column of band k -> its partial slot
+    auto stats = [&](int k) {
+        const uint4* buf = bufk(k);
+        const int nvb = nvec(k);
+        const int v = t / tpv, ro = t % tpv;
+        float cn = 0.f, cm[8], cq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = cq[e] = 0.f;
+        if (v < nvb && ro < n) {
+            float sh[8], s1[8], s2[8];
+            unpack8(buf[ro * pitch + v], sh);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s1[e] = s2[e] = 0.f;
+            int cnt = 0;
+#pragma unroll 4
+            for (int i = ro; i < n; i += tpv, ++cnt) {
+                float f[8];
+                unpack8(buf[i * pitch + v], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = f[e] - sh[e];
+                    s1[e] += d;
+                    s2[e] = fmaf(d, d, s2[e]);
+                }
+            }
+            cn = static_cast<float>(cnt);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float dm = s1[e] / cn;
+                cm[e] = sh[e] + dm;
+                cq[e] = fmaxf(s2[e] - s1[e] * dm, 0.f);
+            }
+        }
+        // the tpv lanes of the vector, in a fixed tree (lane ro takes ro + off)
+        for (int off = tpv >> 1; off > 0; off >>= 1) {
+            const float on = __shfl_down_sync(0xFFFFFFFFu, cn, off);
+            float om[8], oq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                om[e] = __shfl_down_sync(0xFFFFFFFFu, cm[e], off);
+                oq[e] = __shfl_down_sync(0xFFFFFFFFu, cq[e], off);
+            }
+            if (ro < off) {
+                float nn = cn;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    nn = cn;
+                    chan2(nn, cm[e], cq[e], on, om[e], oq[e]);
+                }
+                cn = nn;
+            }
+        }
+        if (ro == 0 && v < nvb) {
+            float4* q = reinterpret_cast<float4*>(g.part + (static_cast<int64_t>(k & 1) * G + c) * BC + v * kVec);
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) q[e / 2] = make_float4(cm[e], cq[e], cm[e + 1], cq[e + 1]);
+        }
+    };
+    // band k's columns merged across the CTAs, one warp per column over the grid
+    auto merge = [&](int k) {
+        const float2* part = g.part + static_cast<int64_t>(k & 1) * G * BC;
+        float2* ab = g.ab + static_cast<int64_t>(k & 1) * BC;
+        for (int j = c * kGrWarps + warp; j < nvec(k) * kVec; j += G * kGrWarps) {
+            const int col = k * BC + j;
+            const float ga = __uint_as_float(static_cast<uint32_t>(__ldg(g.gamma + col)) << 16);
+            const float be = __uint_as_float(static_cast<uint32_t>(__ldg(g.beta + col)) << 16);
+            float2 p[kOgMaxGrid / 32];  // every load in flight before the first merge
+#pragma unroll
+            for (int q = 0; q < kOgMaxGrid / 32; ++q) {
+                const int s = lane + 32 * q;
+                if (s < G) p[q] = __ldcg(part + static_cast<int64_t>(s) * BC + j);
+            }
+            float cn = 0.f, cm = 0.f, cq = 0.f;
+#pragma unroll
+            for (int q = 0; q < kOgMaxGrid / 32; ++q) {
+                const int s = lane + 32 * q;
+                if (s < G) chan2(cn, cm, cq, static_cast<float>(base + (s < rem ? 1 : 0)), p[q].x, p[q].y);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float on = __shfl_down_sync(0xFFFFFFFFu, cn, off);
+                const float om = __shfl_down_sync(0xFFFFFFFFu, cm, off);
+                const float oq = __shfl_down_sync(0xFFFFFFFFu, cq, off);
+                if (lane < off) chan2(cn, cm, cq, on, om, oq);
+            }
+            if (lane == 0) {
+                const float rstd = rsqrtf(cq / static_cast<float>(g.rows) + g.eps);
+                const float aa = rstd * ga;
+                ab[j] = make_float2(aa, be - cm * aa);
+                if (g.mean) g.mean[col] = cm;
+                if (g.rstd) g.rstd[col] = rstd;
+            }
+        }
+    };
+    // y = x * a + b for band k, from shared memory
+    auto apply = [&](int k) {
+        const uint4* buf = bufk(k);
+        const int nvb = nvec(k);
+        const float2* ab = g.ab + static_cast<int64_t>(k & 1) * BC;
+        for (int j = t; j < nvb * kVec; j += kGrT) sab[j] = __ldcg(ab + j);
+        __syncthreads();
+        const int v = t % bvec;
+        if (v < nvb) {
+            float2 a2[4], b2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 u0 = sab[v * kVec + 2 * q], u1 = sab[v * kVec + 2 * q + 1];
+                a2[q] = make_float2(u0.x, u1.x);
+                b2[q] = make_float2(u0.y, u1.y);
+            }
+            uint16_t* dst = g.y + r0 * H + static_cast<int64_t>(k * bvec + v) * kVec;
+            for (int i = t / bvec; i < n; i += tpv) {
+                float2 f[4], o[4];
+                unpack8x2(buf[i * pitch + v], f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = __ffma2_rn(f[q], a2[q], b2[q]);
+                st_stream(dst + static_cast<int64_t>(i) * H, pack8x2(o));
+            }
+        }
+        __syncthreads();  // the buffer and the staged pairs are free again
+    };
+
+    grid_dep_wait();
+    issue(0);
+    issue(1);
+    gr_wait<1>();
+    __syncthreads();  // band 0 has landed
+    stats(0);
+    // a CTA that gives up waits for its own copies in flight, then returns
+    grid_arrive(arrivals, grid, &target);
+    if (!grid_wait(arrivals, &target, kWaitLimitNs, status, &give_up)) {
+        gr_wait<0>();
+        return;
+    }
+    merge(0);
+    grid_arrive(arrivals, grid, &target);
+    if (!grid_wait(arrivals, &target, kWaitLimitNs, status, &give_up)) {
+        gr_wait<0>();
+        return;
+    }
+    for (int k = 0; k < nb; ++k) {
+        const bool next = k + 1 < nb;
+        if (next) {
+            gr_wait<0>();
+            __syncthreads();  // band k + 1 has landed
+            stats(k + 1);
+            grid_arrive(arrivals, grid, &target);
+        }
+        apply(k);  // its stores drain while the grid gathers
+        issue(k + 2);
+        if (next) {
+            if (!grid_wait(arrivals, &target, kWaitLimitNs, status, &give_up)) {
+                gr_wait<0>();
+                return;
+            }
+            merge(k + 1);
+            grid_arrive(arrivals, grid, &target);
+            if (!grid_wait(arrivals, &target, kWaitLimitNs, status, &give_up)) {
+                gr_wait<0>();
+                return;
+            }
+        }
+    }
+    gr_wait<0>();
+}
+
 size_t gr_align16(size_t b) { return (b + 15) / 16 * 16; }
 
 }  // namespace
@@ -476,6 +769,75 @@ cudaError_t launch_grid_selftest(void* counter16, uint64_t limit_ns, int* status
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, grid_barrier_selftest, arrivals, limit_ns, status);
+}
+
+// Outer normalization on chip: the widest band (a power of two from 16 to
+// 512 vectors, no wider than the matrix needs) whose two stripe buffers and
+// pairs fit one CTA's shared memory.
+bool outer_grid_shape(int64_t rows, int64_t hidden, int sms, int* bvec, size_t* smem) {
+    if (rows < 1 || sms < 1 || sms > kOgMaxGrid || hidden < kVec || hidden % kVec != 0) return false;
+    const int64_t rs = (rows + sms - 1) / sms;
+    const int64_t nv = hidden / kVec;
+    int cap = 512;
+    while (cap > 16 && cap / 2 >= nv) cap /= 2;
+    for (int b = cap; b >= 16; b /= 2) {
+        const int64_t bytes = 2 * rs * (b + 1) * 16 + static_cast<int64_t>(b) * kVec * 8;
+        if (bytes <= kGrDynMax) {
+            if (bvec) *bvec = b;
+            if (smem) *smem = static_cast<size_t>(bytes < kGrExclusiveSmem ? kGrExclusiveSmem : bytes);
+            return true;
+        }
+    }
+    return false;
+}
+
+// Workspace: the CTAs' partials of a band [2][sms][bvec * 8] float2, then
+// a band's (a, b) pairs [2][bvec * 8] float2 (two slots, by band parity).
+size_t outer_grid_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
+    int bvec;
+    if (!outer_grid_shape(rows, hidden, sms, &bvec, nullptr)) return 0;
+    return 2 * static_cast<size_t>(sms + 1) * bvec * kVec * sizeof(float2);
+}
+
+cudaError_t launch_outer_grid_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                                  const void* beta, int64_t rows, int64_t hidden, float eps,
+                                  void* workspace, int sms, int* status, cudaStream_t st) {
+    int bvec;
+    size_t smem;
+    if (!outer_grid_shape(rows, hidden, sms, &bvec, &smem)) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaError_t e = cudaFuncSetAttribute(outer_grid_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kGrDynMax))
+            return e;
+        attr_set = true;
+    }
+    OuterGridArgs g{};
+    g.y = static_cast<uint16_t*>(y);
+    g.x = static_cast<const uint16_t*>(x);
+    g.gamma = static_cast<const uint16_t*>(gamma);
+    g.beta = static_cast<const uint16_t*>(beta);
+    g.mean = mean;
+    g.rstd = rstd;
+    g.part = static_cast<float2*>(workspace);
+    g.ab = g.part + 2 * static_cast<int64_t>(sms) * bvec * kVec;
+    g.rows = rows;
+    g.hidden = static_cast<int>(hidden);
+    g.eps = eps;
+    g.bvec = bvec;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kGrT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, outer_grid_fwd, g, status);
 }
 
 // a.cols0 / a.cols1 are the backward column outputs (dgamma / dbeta, dw).

@@ -606,7 +606,9 @@ size_t outer_workspace_bytes(int64_t rows, int64_t hidden, int sms) {
     const size_t ns = static_cast<size_t>(outer_stripes(rows, hidden, sms));
     const size_t fwd = ns * hidden * sizeof(float2) + 2 * hidden * sizeof(float);
     const size_t bwd = ns * 2 * hidden * sizeof(float);
-    return fwd > bwd ? fwd : bwd;
+    const size_t grid = outer_grid_workspace_bytes(rows, hidden, sms);  // the on-chip form
+    const size_t most = fwd > bwd ? fwd : bwd;
+    return most > grid ? most : grid;
 }
 
 // One pass over all columns.  (Walking the columns in chunks sized for L2,

@@ -164,6 +164,14 @@ cudaError_t launch_outer_fwd(void* y, float* mean, float* rstd, const void* x, c
 cudaError_t launch_outer_bwd(void* dx, float* dgamma, float* dbeta, const void* dy, const void* x,
                              const float* mean, const float* rstd, const void* gamma, int64_t rows,
                              int64_t hidden, void* workspace, int sms, cudaStream_t st);
+// The same on chip (the grid family): one cooperative launch, the row
+// stripes held in shared memory band of columns by band, two bounded grid
+// barriers per band.  For shapes where outer_grid_shape holds.
+bool outer_grid_shape(int64_t rows, int64_t hidden, int sms, int* bvec, size_t* smem);
+size_t outer_grid_workspace_bytes(int64_t rows, int64_t hidden, int sms);
+cudaError_t launch_outer_grid_fwd(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                                  const void* beta, int64_t rows, int64_t hidden, float eps,
+                                  void* workspace, int sms, int* status, cudaStream_t st);
 
 // Bounded-wait self test (see nf_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -1,6 +1,9 @@
 """GPU parity of the outer (per-column) normalization kernels against the
 fp64 oracle: column tiles with a ragged tail, row stripes of uneven length,
-a single row, and determinism of the column sums."""
+a single row, and determinism of the column sums.  The forward has two
+forms: the three-launch streaming passes (the automatic choice; also under
+a forced split family) and the single launch with the row stripes on chip
+(forced with the grid family), both checked at every shape."""
 import numpy as np
 import pytest
 import torch
@@ -23,16 +26,33 @@ def built():
     yield
 
 
+@pytest.mark.parametrize("form", ("split", "grid"))
 @pytest.mark.parametrize("hidden", HIDDEN)
 @pytest.mark.parametrize("rows", ROWS)
-def test_outer_fwd(rows, hidden):
+def test_outer_fwd(rows, hidden, form):
     x, _, g, b = workloads.outer_inputs(rows, hidden, seed=rows * 7 + hidden)
     y_ref, m_ref, r_ref = oracle.outer_norm_fwd(x, g, b, 1e-5)
-    y, mean, rstd = nf.outer_norm_fwd(x.cuda(), g.cuda(), b.cuda(), 1e-5)
+    args = (x.cuda(), g.cuda(), b.cuda(), 1e-5)
+    with nf.forced_path(form):
+        y, mean, rstd = nf.outer_norm_fwd(*args)
+        y2, mean2, rstd2 = nf.outer_norm_fwd(*args)
     torch.cuda.synchronize()
-    check_bf16(y, y_ref, f"outer fwd y {rows}x{hidden}")
-    check_f32(mean, m_ref, f"outer fwd mean {rows}x{hidden}")
-    check_f32(rstd, r_ref, f"outer fwd rstd {rows}x{hidden}", rtol=1e-4)
+    check_bf16(y, y_ref, f"outer fwd y {rows}x{hidden} {form}")
+    check_f32(mean, m_ref, f"outer fwd mean {rows}x{hidden} {form}")
+    check_f32(rstd, r_ref, f"outer fwd rstd {rows}x{hidden} {form}", rtol=1e-4)
+    assert torch.equal(y, y2) and torch.equal(mean, mean2) and torch.equal(rstd, rstd2)
+
+
+def test_outer_grid_form_refuses_stripes_too_long():
+    # 65536 rows: a stripe of 432 rows does not fit two band buffers of the
+    # narrowest band (16 vectors), so the grid form is refused
+    rows, hidden = 65536, 1024
+    x = torch.zeros(rows, hidden, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(hidden, dtype=torch.bfloat16, device="cuda")
+    with nf.forced_path("grid"):
+        with pytest.raises(nf.NFError) as e:
+            nf.outer_norm_fwd(x, g, g, 1e-5)
+    assert e.value.status == nf.NF_ERR_UNSUPPORTED_PATH
 
 
 @pytest.mark.parametrize("hidden", HIDDEN)
@@ -52,12 +72,14 @@ def test_outer_bwd(rows, hidden):
     assert torch.equal(dx, dx2) and torch.equal(dg, dg2) and torch.equal(db, db2)
 
 
-def test_outer_in_place():
+@pytest.mark.parametrize("form", ("split", "grid"))
+def test_outer_in_place(form):
     rows, hidden = 600, 1032
     x, dy, g, b = workloads.outer_inputs(rows, hidden, seed=5)
     y_ref, m_ref, r_ref = oracle.outer_norm_fwd(x, g, b, 1e-5)
     xd = x.cuda()
-    y, mean, rstd = nf.outer_norm_fwd(xd, g.cuda(), b.cuda(), 1e-5, out=xd)
+    with nf.forced_path(form):
+        y, mean, rstd = nf.outer_norm_fwd(xd, g.cuda(), b.cuda(), 1e-5, out=xd)
     torch.cuda.synchronize()
     assert y.data_ptr() == xd.data_ptr()
     check_bf16(xd, y_ref, "outer fwd in place")
