@@ -810,10 +810,13 @@ def run_profile_case(spec: str, reps: int):
     """Run `reps` launches of one operation at one size and exit: the small,
     self-contained command the ncu captures use.  spec = OP:ROWSxHIDDEN with
     OP in fused_add_rmsnorm, rmsnorm_fwd, layernorm_fwd, layernorm_bwd,
-    rmsnorm_bwd, fused_add_rmsnorm_bwd, outer_norm_fwd, outer_norm_bwd."""
+    rmsnorm_bwd, fused_add_rmsnorm_bwd, outer_norm_fwd, outer_norm_bwd; an
+    optional @FAMILY suffix (e.g. @split) forces that kernel family for the
+    timed calls (inputs are prepared under the automatic choice)."""
     import row_normalization_inner_gb300 as nf
     from row_normalization_inner_gb300 import build as nf_build
     nf_build.build()
+    spec, _, family = spec.partition("@")
     op, shape = spec.split(":")
     rows, hidden = (int(v) for v in shape.split("x"))
     dev = "cuda"
@@ -859,12 +862,16 @@ def run_profile_case(spec: str, reps: int):
             fn = lambda: nf.outer_norm_bwd(dy, x, mean, rstd, g, workspace=ws, out=y)  # noqa: E731
     else:
         raise SystemExit(f"unknown op {op}")
-    for _ in range(reps):
-        fn()
-    torch.cuda.synchronize()
-    plan = "outer" if op.startswith("outer") else nf.nf_plan_query(
-        "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op, rows, hidden)
-    print(f"profile case {spec}: {reps} call(s), plan {plan}")
+    nf.set_path(family or "auto")
+    try:
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        plan = "outer" if op.startswith("outer") else nf.nf_plan_query(
+            "rmsnorm_bwd" if op == "fused_add_rmsnorm_bwd" else op, rows, hidden)
+    finally:
+        nf.set_path("auto")
+    print(f"profile case {spec}{'@' + family if family else ''}: {reps} call(s), plan {plan}")
     return 0
 
 
