@@ -166,12 +166,12 @@ __global__ void __launch_bounds__(MAXT) norm_dyn_fwd(DynArgs a) {
 }
 
 // OP: 3 LayerNorm backward, 4 RMSNorm backward (rstd recomputed from x).
-// MAXV is 1 vector per thread for rows of at most 256 vectors (short rows
-// get more, lighter threads), else 4 (dyn_bwd_vecs).  With one vector a
-// thread needs few registers and the launch bound guarantees 1024 resident
-// threads per SM; with four, 512 (dyn_bwd_per_sm).
+// MAXV is the vectors per thread (dyn_bwd_vecs): 1 for rows of at most 256
+// vectors, 2 up to 768, else 4.  The launch bound guarantees 1024 resident
+// threads per SM with one vector, 768 with two (at most 384 threads, two
+// CTAs) and 512 with four (dyn_bwd_per_sm).
 template <int OP, int MAXV, bool ADD>
-__global__ void __launch_bounds__(kDynBwdMaxT, MAXV == 1 ? 2 : 1) norm_dyn_bwd(DynArgs a) {
+__global__ void __launch_bounds__(MAXV == 2 ? 384 : kDynBwdMaxT, MAXV == 4 ? 1 : 2) norm_dyn_bwd(DynArgs a) {
     constexpr int NP = OP == 3 ? 2 : 1;  // partial planes
     constexpr int NT = ADD ? 3 : 2;      // tensors in the ring
     __shared__ float red[2][kDynMaxWarps * 2];
@@ -333,11 +333,18 @@ __global__ void __launch_bounds__(kDynBwdMaxT, MAXV == 1 ? 2 : 1) norm_dyn_bwd(D
 }  // namespace
 
 // Vectors per thread of the backward kernel: one for rows of at most 256
-// vectors, else four.  Measured on GB300 at 16384 rows (graph-timed):
+// vectors, two up to 768, else four.  Measured on GB300 at 16384 rows (graph-timed):
 // hidden 1000 LayerNorm backward 50.1 -> 32.6 us with one vector against
 // four; from hidden 2560 up four were faster (RMSNorm 3072: 61.7 against
 // 90.1 us), as a CTA then keeps more of a row in flight per thread.
-int dyn_bwd_vecs(int64_t nv) { return nv <= 256 ? 1 : kDynMaxV; }
+//
+// Two vectors per thread from 257 to 768 vectors: twice the threads per row
+// and half the column sums per thread (75-79 registers, no spill, against
+// 128 and a spill for the LayerNorm backward with four).  At 16384 rows:
+// LayerNorm backward 2560 / 3072 / 4000 / 6144: 71.2 / 78.3 / 103.2 / 164.3
+// -> 58.4 / 66.9 / 81.6 / 126.4 us; RMSNorm backward 1 % faster; fused-add
+// backward 3072 / 4000: 68.4 / 88.8 -> 65.4 / 83.7 us (2560: 56.0 -> 58.0).
+int dyn_bwd_vecs(int64_t nv) { return nv <= 256 ? 1 : nv <= 768 ? 2 : kDynMaxV; }
 
 // Threads per CTA for a runtime hidden size, or false if the op has no
 // dynamic kernel for it.  Forward: four vectors per thread; backward: see
@@ -363,13 +370,15 @@ size_t dyn_bwd_smem(int64_t hidden, bool add) {
 }
 
 // Resident CTAs per SM of the backward kernel: what its launch bound
-// guarantees (1024 threads per SM with one vector per thread, else 512),
+// guarantees (1024 threads per SM with one vector per thread, 768 with two,
+// 512 with four),
 // and what its ring leaves room for (228 KB of shared memory per SM, 1 KB
 // of it reserved per CTA, plus the kernel's static reduction buffer).
 int dyn_bwd_per_sm(int64_t hidden, bool add) {
     int t;
     if (!dyn_shape(3, hidden, &t)) return 1;
-    int per_sm = (dyn_bwd_vecs(hidden / kVec) == 1 ? 1024 : 512) / t;
+    const int vecs = dyn_bwd_vecs(hidden / kVec);
+    int per_sm = (vecs == 1 ? 1024 : vecs == 2 ? 768 : 512) / t;
     const size_t cta = dyn_bwd_smem(hidden, add) + 1024 + 2 * kDynMaxWarps * 2 * sizeof(float);
     const int by_smem = static_cast<int>((228 * 1024) / cta);
     if (by_smem < per_sm) per_sm = by_smem;
@@ -396,6 +405,9 @@ cudaError_t dyn_bwd_attrs() {
     if (!e) e = set(norm_dyn_bwd<4, kDynMaxV, false>);
     if (!e) e = set(norm_dyn_bwd<4, 1, true>);
     if (!e) e = set(norm_dyn_bwd<4, kDynMaxV, true>);
+    if (!e) e = set(norm_dyn_bwd<3, 2, false>);
+    if (!e) e = set(norm_dyn_bwd<4, 2, false>);
+    if (!e) e = set(norm_dyn_bwd<4, 2, true>);
     if (!e && dev >= 0 && dev < kMaxDev) done[dev] = true;
     return e;
 }
@@ -423,11 +435,14 @@ cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st) {
             if (cudaError_t e = dyn_bwd_attrs()) return e;
             if (op == 3)
                 return v == 1 ? launch_with_pdl(norm_dyn_bwd<3, 1, false>, g, b, smem, st, a)
+                     : v == 2 ? launch_with_pdl(norm_dyn_bwd<3, 2, false>, g, b, smem, st, a)
                               : launch_with_pdl(norm_dyn_bwd<3, kDynMaxV, false>, g, b, smem, st, a);
             if (add)
                 return v == 1 ? launch_with_pdl(norm_dyn_bwd<4, 1, true>, g, b, smem, st, a)
+                     : v == 2 ? launch_with_pdl(norm_dyn_bwd<4, 2, true>, g, b, smem, st, a)
                               : launch_with_pdl(norm_dyn_bwd<4, kDynMaxV, true>, g, b, smem, st, a);
             return v == 1 ? launch_with_pdl(norm_dyn_bwd<4, 1, false>, g, b, smem, st, a)
+                 : v == 2 ? launch_with_pdl(norm_dyn_bwd<4, 2, false>, g, b, smem, st, a)
                           : launch_with_pdl(norm_dyn_bwd<4, kDynMaxV, false>, g, b, smem, st, a);
         }
         default: return cudaErrorInvalidValue;

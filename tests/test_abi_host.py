@@ -148,7 +148,7 @@ def test_cluster_path_forced_for_any_hidden():
     assert st == nf.NF_OK and p["launches"] == 2 and p["partials"] >= 1
 
 
-@pytest.mark.parametrize("hidden", [8, 24, 264, 768, 1000, 3072, 6144, 14336, 16384, 32768])
+@pytest.mark.parametrize("hidden", [8, 24, 264, 768, 1000, 2056, 3072, 6144, 6152, 14336, 16384, 32768])
 def test_dynamic_plans(hidden):
     for op in ("fused_add_rmsnorm", "rmsnorm_fwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_bwd"):
         bwd = op.endswith("_bwd")
@@ -161,21 +161,22 @@ def test_dynamic_plans(hidden):
             assert st == nf.NF_OK and p["path"] == "dynamic"
             assert p["block"] % 32 == 0 and 32 <= p["block"] <= (512 if bwd else 1024)
             # forward: four vectors per thread; backward: one for rows of at
-            # most 256 vectors, else four
+            # most 256 vectors, two up to 768, else four
             nv = hidden // 8
-            vecs = 1 if bwd and nv <= 256 else 4
+            vecs = (1 if nv <= 256 else 2 if nv <= 768 else 4) if bwd else 4
             assert p["block"] * vecs * 8 >= hidden
             assert p["block"] == 32 or (p["block"] - 32) * vecs * 8 < hidden   # no spare warp
             if bwd:
                 # one wave of the CTAs that stay resident: the launch bound
-                # keeps 1024 threads per SM with one vector per thread, else
-                # 512, and each CTA's copy ring (2 stages of x and dy, and for
-                # the RMSNorm backward room for the fused-add backward's third
-                # tensor) takes shared memory (228 KB per SM, 1 KB reserved per CTA)
+                # keeps 1024 threads per SM with one vector per thread, 768
+                # with two, 512 with four, and each CTA's copy ring (2 stages
+                # of x and dy, and for the RMSNorm backward room for the
+                # fused-add backward's third tensor) takes shared memory
+                # (228 KB per SM, 1 KB reserved per CTA)
                 ring = 2 * 2 * vecs * p["block"] * 16
                 assert p["smem_bytes"] == ring
                 ring_max = ring * 3 // 2 if op == "rmsnorm_bwd" else ring
-                per_sm = min((1024 if vecs == 1 else 512) // p["block"], 228 * 1024 // (ring_max + 1024 + 512))
+                per_sm = min({1: 1024, 2: 768, 4: 512}[vecs] // p["block"], 228 * 1024 // (ring_max + 1024 + 512))
                 per_sm = max(1, per_sm)
                 assert p["launches"] == 2 and p["partials"] == p["grid"] >= 1
                 assert p["grid"] == min(rows, 152 * per_sm)

@@ -13,7 +13,7 @@ from gpu_helpers import check_bf16, check_f32, ulp_diff_bf16
 pytestmark = pytest.mark.gpu
 
 FWD_HIDDEN = (8, 264, 768, 1000, 3072, 6144, 14336, 32768)
-BWD_HIDDEN = (8, 264, 768, 1000, 3072, 6144, 16384)
+BWD_HIDDEN = (8, 264, 768, 1000, 2056, 3072, 6144, 6152, 16384)   # 2056 / 6152: the first sizes with two / four vectors per thread
 ROWS = (1, 37, 300)
 
 
