@@ -159,72 +159,103 @@ grid_norm(DynArgs a, float2* __restrict__ part, int vc, int* status) {
             }
         }
     }
+    // one batch of the second tensor (and the weight): `sb` holds row r's
+    // vectors i0, i0 + kGrT, ... (kGrBatch of them), `wb` the weight's
+    auto consume = [&](int r, int i0, const uint4 (&sb)[kGrBatch], const uint4 (&wb)[kGrBatch]) {
+        const int64_t roff = static_cast<int64_t>(r) * H + static_cast<int64_t>(vbeg) * kVec;
+#pragma unroll
+        for (int k = 0; k < kGrBatch; ++k) {
+            const int i = i0 + k * kGrT;
+            if (i >= nv) break;
+            float f[8];
+            unpack8(gr_rows[r * vc + i], f);
+            if constexpr (OP == 0) {
+                float b[8];
+                unpack8(sb[k], b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] += b[e];
+                const uint4 h = pack8(f);  // the stored residual, normalized in phase 2
+                gr_rows[r * vc + i] = h;
+                st_stream(a.out1 + roff + static_cast<int64_t>(i) * kVec, h);
+                unpack8(h, f);
+            }
+            if constexpr (OP <= 1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r][0] = fmaf(f[e], f[e], acc[r][0]);
+            } else if constexpr (OP == 2) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = f[e] - rc0[r];
+                    acc[r][0] += d;
+                    acc[r][1] = fmaf(d, d, acc[r][1]);
+                }
+            } else {
+                float dy[8], w[8];
+                unpack8(sb[k], dy);
+                unpack8(wb[k], w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float g = dy[e] * w[e];
+                    if constexpr (OP == 3) {
+                        acc[r][0] += g;
+                        acc[r][1] = fmaf(g, (f[e] - rc0[r]) * rc1[r], acc[r][1]);
+                    } else {
+                        acc[r][0] = fmaf(f[e], f[e], acc[r][0]);
+                        acc[r][1] = fmaf(g, f[e], acc[r][1]);
+                    }
+                }
+            }
+        }
+    };
+    // the second tensor's batch of row r at vectors i0, i0 + kGrT, ...
+    auto load_row = [&](int r, int i0, uint4 (&sb)[kGrBatch]) {
+        const int64_t roff = static_cast<int64_t>(r) * H + static_cast<int64_t>(vbeg) * kVec;
+#pragma unroll
+        for (int k = 0; k < kGrBatch; ++k) {
+            const int i = i0 + k * kGrT;
+            if (i < nv) sb[k] = ld_stream(a.in1 + roff + static_cast<int64_t>(i) * kVec);
+        }
+    };
+    auto load_w1 = [&](int i0, uint4 (&wb)[kGrBatch]) {
+#pragma unroll
+        for (int k = 0; k < kGrBatch; ++k) {
+            const int i = i0 + k * kGrT;
+            if (i < nv) wb[k] = ld_param(p0 + static_cast<int64_t>(i) * kVec);
+        }
+    };
+    // The fused op, when a row is one batch per thread, loads row r + 1's
+    // residual while row r is summed (two register buffers).  Longer rows,
+    // and the backward (a second dy buffer, or the weight held across rows,
+    // spills), take their batches one at a time.
+    const bool one = OP == 0 && nv <= kGrBatch * kGrT;
+    uint4 sbA[kGrBatch], sbB[kGrBatch];  // unused (and dropped) by the other ops
+    if constexpr (OP == 0) {
+        if (one) load_row(0, t, sbA);
+    }
 #pragma unroll
     for (int r = 0; r < RM; ++r) {
         if (r >= R) break;
-        const int64_t roff = static_cast<int64_t>(r) * H + static_cast<int64_t>(vbeg) * kVec;
         if (r + 1 < R) {
             const uint16_t* src = a.in0 + static_cast<int64_t>(r + 1) * H + static_cast<int64_t>(vbeg) * kVec;
             for (int i = t; i < nv; i += kGrT) gr_cp16(&gr_rows[(r + 1) * vc + i], src + static_cast<int64_t>(i) * kVec);
         }
         gr_commit();
+        if constexpr (OP == 0) {
+            if (one) {
+                uint4 (&cur)[kGrBatch] = (r & 1) ? sbB : sbA;
+                uint4 (&nxt)[kGrBatch] = (r & 1) ? sbA : sbB;
+                if (r + 1 < R) load_row(r + 1, t, nxt);
+                gr_wait<1>();  // this thread's copies of row r have landed (only row r + 1's may be pending)
+                consume(r, t, cur, cur);  // (no weight in the fused op's first phase)
+                continue;
+            }
+        }
         for (int i0 = t; i0 < nv; i0 += kGrBatch * kGrT) {
-            uint4 sb[kTwo ? kGrBatch : 1], wb[kBwd ? kGrBatch : 1];
-            if constexpr (kTwo) {
-#pragma unroll
-                for (int k = 0; k < kGrBatch; ++k) {
-                    const int i = i0 + k * kGrT;
-                    if (i < nv) {
-                        const uint16_t* p = a.in1 + roff + static_cast<int64_t>(i) * kVec;
-                        sb[k] = ld_stream(p);
-                        if constexpr (kBwd) wb[k] = ld_param(p0 + static_cast<int64_t>(i) * kVec);
-                    }
-                }
-            }
+            uint4 sb[kGrBatch], wb[kGrBatch];
+            if constexpr (kTwo) load_row(r, i0, sb);
+            if constexpr (kBwd) load_w1(i0, wb);
             gr_wait<1>();  // this thread's copies of row r have landed (only row r + 1's may be pending)
-#pragma unroll
-            for (int k = 0; k < kGrBatch; ++k) {
-                const int i = i0 + k * kGrT;
-                if (i >= nv) break;
-                float f[8];
-                unpack8(gr_rows[r * vc + i], f);
-                if constexpr (OP == 0) {
-                    float b[8];
-                    unpack8(sb[k], b);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] += b[e];
-                    const uint4 h = pack8(f);  // the stored residual, normalized in phase 2
-                    gr_rows[r * vc + i] = h;
-                    st_stream(a.out1 + roff + static_cast<int64_t>(i) * kVec, h);
-                    unpack8(h, f);
-                }
-                if constexpr (OP <= 1) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[r][0] = fmaf(f[e], f[e], acc[r][0]);
-                } else if constexpr (OP == 2) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float d = f[e] - rc0[r];
-                        acc[r][0] += d;
-                        acc[r][1] = fmaf(d, d, acc[r][1]);
-                    }
-                } else {
-                    float dy[8], w[8];
-                    unpack8(sb[k], dy);
-                    unpack8(wb[k], w);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float g = dy[e] * w[e];
-                        if constexpr (OP == 3) {
-                            acc[r][0] += g;
-                            acc[r][1] = fmaf(g, (f[e] - rc0[r]) * rc1[r], acc[r][1]);
-                        } else {
-                            acc[r][0] = fmaf(f[e], f[e], acc[r][0]);
-                            acc[r][1] = fmaf(g, f[e], acc[r][1]);
-                        }
-                    }
-                }
-            }
+            consume(r, i0, sb, wb);
         }
     }
     gr_wait<0>();  // nothing left in flight (the last row committed an empty group)
