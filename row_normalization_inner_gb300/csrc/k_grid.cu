@@ -56,6 +56,14 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// The arrival: an acquire-release add, so the CTA's writes (ordered before
+// it by the CTA barrier) are published by it, and the last CTA to arrive
+// sees every other CTA's writes through the chain of adds.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void gr_cp16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
 }
@@ -65,30 +73,32 @@ template <int N>
 __device__ __forceinline__ void gr_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Grid barrier, called by every thread of every CTA once its writes are
-// done: thread 0 makes the CTA's writes visible, takes a ticket and waits
-// until the arrivals reach the next multiple of `grid` above it, or until
-// `limit_ns` has passed; in the second case it records NF_ERR_TIMEOUT in the
-// device status word.  Returns false in every thread of a CTA that gave up
-// (it must then return without further work).  Only valid when all `grid`
-// CTAs are resident (a cooperative launch).
+// done: thread 0 publishes the CTA's writes with its arrival (a ticket) and
+// waits until the arrivals reach the next multiple of `grid` above it, or
+// until `limit_ns` has passed; in the second case it records NF_ERR_TIMEOUT
+// in the device status word.  The last CTA to arrive completes the count
+// itself and does not wait.  Returns false in every thread of a CTA that
+// gave up (it must then return without further work).  Only valid when all
+// `grid` CTAs are resident (a cooperative launch).
 __device__ __forceinline__ bool grid_barrier(unsigned long long* arrivals, unsigned long long grid,
                                              uint64_t limit_ns, int* status, int* give_up) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned long long ticket = atomicAdd(arrivals, 1ull);
+        const unsigned long long ticket = atom_add_acq_rel(arrivals, 1ull);
         const unsigned long long target = (ticket / grid + 1) * grid;
-        const uint64_t t0 = global_ns();
         int fail = 0;
-        while (ld_acquire_u64(arrivals) < target) {
-            if (global_ns() - t0 > limit_ns) {
-                fail = 1;
-                break;
+        if (ticket + 1 != target) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u64(arrivals) < target) {
+                if (global_ns() - t0 > limit_ns) {
+                    fail = 1;
+                    break;
+                }
             }
+            __threadfence();
         }
         if (fail) record_status(status, kStatusTimeout);
         *give_up = fail;
-        __threadfence();
     }
     __syncthreads();
     return !*give_up;
@@ -539,25 +549,27 @@ __device__ __forceinline__ void grid_arrive(unsigned long long* arrivals, unsign
                                             unsigned long long* target) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned long long ticket = atomicAdd(arrivals, 1ull);
-        *target = (ticket / grid + 1) * grid;
+        const unsigned long long ticket = atom_add_acq_rel(arrivals, 1ull);
+        const unsigned long long tg = (ticket / grid + 1) * grid;
+        *target = ticket + 1 == tg ? 0ull : tg;  // 0: this CTA completed the count
     }
 }
 __device__ __forceinline__ bool grid_wait(unsigned long long* arrivals, const unsigned long long* target,
                                           uint64_t limit_ns, int* status, int* give_up) {
     if (threadIdx.x == 0) {
-        const uint64_t t0 = global_ns();
         int fail = 0;
-        while (ld_acquire_u64(arrivals) < *target) {
-            if (global_ns() - t0 > limit_ns) {
-                fail = 1;
-                break;
+        if (*target != 0ull) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u64(arrivals) < *target) {
+                if (global_ns() - t0 > limit_ns) {
+                    fail = 1;
+                    break;
+                }
             }
+            __threadfence();
         }
         if (fail) record_status(status, kStatusTimeout);
         *give_up = fail;
-        __threadfence();
     }
     __syncthreads();
     return !*give_up;
