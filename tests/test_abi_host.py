@@ -554,6 +554,12 @@ def test_floor_probe_rejects_bad_arguments_before_launch():
     assert nf.nf_selftest_floor(1, A, A + 512, 1024, None) == nf.NF_ERR_INVALID_ARG
 
 
+def test_grid_barrier_selftest_rejects_bad_arguments_before_launch():
+    # the counter pointer is checked before any CUDA call
+    assert nf.nf_selftest_grid_timeout(0, 2_000_000, None) == nf.NF_ERR_INVALID_ARG
+    assert nf.nf_selftest_grid_timeout(A + 8, 2_000_000, None) == nf.NF_ERR_MISALIGNED
+
+
 def test_noalloc_argument_errors_match_the_workspace_entry_point():
     # null and misaligned arguments are reported as nf_layernorm_bwd reports
     # them, before the scratch area's size or address is looked at (a size
