@@ -39,9 +39,11 @@
  *           cluster kernels (NF_PATH_CLUSTER), which split one row over a
  *           cluster of 2, 4 or 8 CTAs; longer still, up to
  *           NF_SPLIT_MAX_HIDDEN, on the split kernels (NF_PATH_SPLIT), which
- *           spread a row over any number of CTAs and need a workspace (the
- *           forward ops then take the _ws entry points).  Other values
- *           (not a positive multiple of 8, or longer) return
+ *           spread a row over any number of CTAs, or, for up to 8 rows that
+ *           fit on chip, the grid kernels (NF_PATH_GRID), which hold the
+ *           rows in shared memory across one grid barrier; both need a
+ *           workspace (the forward ops then take the _ws entry points).
+ *           Other values (not a positive multiple of 8, or longer) return
  *           NF_ERR_UNSUPPORTED_HIDDEN.
  * rows.     Any value >= 0; rows == 0 returns NF_OK without launching.
  * eps.      Finite and > 0.
