@@ -316,3 +316,38 @@ def test_grid_barrier_wait_runs_out_and_context_survives():
         y = nf.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6)
     torch.cuda.synchronize()
     check_bf16(y, oracle.rmsnorm_fwd(x, w, 1e-6)[0], "grid after timeout")
+
+
+@pytest.mark.parametrize("family", ("grid", "split"))
+def test_long_rows_degenerate_cases(family):
+    # a constant LayerNorm row (var = 0: y = beta exactly, rstd = 1/sqrt(eps)),
+    # an all-zero RMSNorm row (y = 0), rows scaled by 1e3 and 1e-3, and the
+    # fused op with residual = -x (the stored sum is 0, so is the output)
+    rows, hidden = 4, 1 << 20
+    x = torch.full((rows, hidden), 3.25, dtype=torch.bfloat16)
+    _, g, b = workloads.layernorm_fwd_inputs(1, hidden, seed=2)
+    with nf.forced_path(family):
+        y, mean, rstd = nf.layernorm_fwd(x.cuda(), g.cuda(), b.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), b.expand(rows, hidden))
+    assert torch.allclose(mean.cpu(), torch.full((rows,), 3.25))
+    assert torch.allclose(rstd.cpu(), torch.full((rows,), 1e-5 ** -0.5), rtol=1e-5)
+
+    xr, w = workloads.rms_inputs(rows, hidden, seed=3)
+    xr[0] = 0
+    xr[1] = (xr[1].float() * 1000).to(torch.bfloat16)
+    xr[2] = (xr[2].float() * 1e-3).to(torch.bfloat16)
+    y_ref, _ = oracle.rmsnorm_fwd(xr, w, 1e-6)
+    with nf.forced_path(family):
+        yr = nf.rmsnorm_fwd(xr.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(yr, y_ref, f"long rows rms extremes/{family}")
+    assert torch.count_nonzero(yr[0]) == 0
+
+    xf = xr.clone()
+    rf = (-xf.float()).to(torch.bfloat16)
+    xd, rd = xf.cuda(), rf.cuda()
+    with nf.forced_path(family):
+        nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(rd) == 0 and torch.count_nonzero(xd) == 0
