@@ -101,3 +101,28 @@ def test_dynamic_rmsnorm_bwd(rows, hidden):
     # fixed-order sums (with more than 256 partial slots at 2000 rows the
     # column reduction splits each column over four warps): bit-identical
     assert torch.equal(dw, dw2) and torch.equal(dx, dx2)
+
+
+@pytest.mark.parametrize("hidden", (264, 3072, 14336))
+def test_dynamic_degenerate_rows(hidden):
+    # a constant LayerNorm row: var = 0, so y = beta exactly and rstd =
+    # 1/sqrt(eps); an all-zero RMSNorm row gives y = 0; rows scaled by 1e3
+    # and 1e-3 stay within the tolerance
+    rows = 3
+    x = torch.full((rows, hidden), -1.5, dtype=torch.bfloat16)
+    _, g, b = workloads.layernorm_fwd_inputs(1, hidden, seed=hidden)
+    y, mean, rstd = nf.layernorm_fwd(x.cuda(), g.cuda(), b.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    assert nf.nf_plan_query("layernorm_fwd", rows, hidden)["path"] == "dynamic"
+    assert torch.equal(y.cpu(), b.expand(rows, hidden))
+    assert torch.allclose(mean.cpu(), torch.full((rows,), -1.5))
+    assert torch.allclose(rstd.cpu(), torch.full((rows,), 1e-5 ** -0.5), rtol=1e-5)
+    xr, w = workloads.rms_inputs(rows, hidden, seed=hidden + 1)
+    xr[0] = 0
+    xr[1] = (xr[1].float() * 1000).to(torch.bfloat16)
+    xr[2] = (xr[2].float() * 1e-3).to(torch.bfloat16)
+    y_ref, _ = oracle.rmsnorm_fwd(xr, w, 1e-6)
+    yr = nf.rmsnorm_fwd(xr.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(yr, y_ref, f"dynamic rms extremes {hidden}")
+    assert torch.count_nonzero(yr[0]) == 0
