@@ -118,6 +118,10 @@ bool dyn_shape(int op, int64_t hidden, int* threads);
 // the ring also carries the fused-add backward's residual-stream gradient.
 int dyn_bwd_per_sm(int64_t hidden, bool add);
 size_t dyn_bwd_smem(int64_t hidden, bool add);
+// Forward: the same for the RMSNorm / LayerNorm forward's copy ring, used
+// for rows of one warp (0 bytes: one CTA per row, no ring).
+int dyn_fwd_per_sm(int op, int64_t hidden);
+size_t dyn_fwd_smem(int op, int64_t hidden);
 int64_t dyn_max_hidden(int op);
 cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st);
 

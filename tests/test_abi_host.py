@@ -180,8 +180,14 @@ def test_dynamic_plans(hidden):
                 per_sm = max(1, per_sm)
                 assert p["launches"] == 2 and p["partials"] == p["grid"] >= 1
                 assert p["grid"] == min(rows, 152 * per_sm)
+            elif op != "fused_add_rmsnorm" and p["block"] == 32:
+                # rows of one warp: one wave of resident CTAs (32 per SM, the
+                # limit) walking the rows through a two-stage copy ring of
+                # four vectors per thread
+                assert p["launches"] == 1 and p["smem_bytes"] == 2 * 4 * 32 * 16
+                assert p["grid"] == min(rows, 152 * 32)
             else:
-                assert p["launches"] == 1 and p["grid"] == rows
+                assert p["launches"] == 1 and p["grid"] == rows and p["smem_bytes"] == 0
         for path in ("reg", "bulk"):
             assert nf.nf_plan_compute(op, 16, hidden, 152, path)[0] == nf.NF_ERR_UNSUPPORTED_PATH
         assert nf.nf_plan_compute(op, 16, hidden, 152, "cluster")[1]["path"] == "cluster"
