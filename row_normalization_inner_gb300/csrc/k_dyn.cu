@@ -246,6 +246,13 @@ __global__ void __launch_bounds__(MAXT, 1024 / MAXT) norm_dyn_fwd(DynArgs a) {
 template <int OP, int MAXV, bool ADD>
 __global__ void __launch_bounds__(MAXV == 2 ? 384 : kDynBwdMaxT, MAXV == 4 ? 1 : 2) norm_dyn_bwd(DynArgs a) {
     constexpr int NP = OP == 3 ? 2 : 1;  // partial planes
+    // The LayerNorm backward with four vectors per thread (OP 3, MAXV 4)
+    // reads gamma again (through L1) where it is used instead of holding it:
+    // that frees the registers its two planes of column sums need (128
+    // registers and a spill -> 106 and none; 16384 x 8200 / 14336: 265 / 333
+    // -> 218 / 277 us).  Elsewhere the reload cost more than it saved
+    // (RMSNorm 16384 x 8200: 170 -> 272 us): the copy ring leaves L1 little
+    // room.
     constexpr int NT = ADD ? 3 : 2;      // tensors in the ring
     __shared__ float red[2][kDynMaxWarps * 2];
     grid_dep_wait();
@@ -323,7 +330,8 @@ __global__ void __launch_bounds__(MAXV == 2 ? 384 : kDynBwdMaxT, MAXV == 4 ? 1 :
                 float2 xf[4], df[4], gf[4];
                 unpack8x2(xv[k], xf);
                 unpack8x2(dv[k], df);
-                unpack8x2(pv[k], gf);
+                if constexpr (OP == 3 && MAXV == 4) unpack8x2(ld_param(a.p0 + (k * T + t) * kVec), gf);
+                else unpack8x2(pv[k], gf);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if constexpr (OP == 3) {
@@ -361,9 +369,22 @@ __global__ void __launch_bounds__(MAXV == 2 ? 384 : kDynBwdMaxT, MAXV == 4 ? 1 :
             const int v = k * T + t;
             if (v < NV) {
                 float2 xf[4], df[4], gf[4], o[4];
-                unpack8x2(xv[k], xf);
-                unpack8x2(dv[k], df);
-                unpack8x2(pv[k], gf);
+                if constexpr (MAXV >= 2) {
+                    // read again from the ring (this row's stage is not refilled
+                    // before the next iteration) instead of holding x and dy in
+                    // registers across the row reduction: at 16384 rows LayerNorm
+                    // backward 3072 / 6144 / 8200 / 14336 67.2 / 127.1 / 296 / 367
+                    // -> 65.4 / 122.4 / 267 / 334.5 us, RMSNorm 14336 233.7 -> 215 us
+                    // (LayerNorm 1000, one vector per thread: 27.8 -> 29.7 us, so
+                    // one vector keeps them in registers)
+                    unpack8x2(*slot(st, 0, k), xf);
+                    unpack8x2(*slot(st, 1, k), df);
+                } else {
+                    unpack8x2(xv[k], xf);
+                    unpack8x2(dv[k], df);
+                }
+                if constexpr (OP == 3 && MAXV == 4) unpack8x2(ld_param(a.p0 + (k * T + t) * kVec), gf);
+                else unpack8x2(pv[k], gf);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float2 dw = __fmul2_rn(df[q], gf[q]);
