@@ -109,9 +109,12 @@ typedef struct CUstream_st* nf_stream;
  *              from shared memory; registers move from producer to
  *              consumers ("TMA inner persistent scheduler").
  *   DYNAMIC -- the hidden size is a runtime argument (any multiple of 8 up
- *              to 32768 forward, 16384 backward); the row still sits in
- *              registers under a compile-time per-thread bound ("TMA inner
- *              persistent scheduler": dynamic block dimensions).  The only
+ *              to 32768 forward, 16384 backward); a thread owns at most
+ *              four 16-byte vectors of a row, a compile-time bound ("TMA
+ *              inner persistent scheduler": dynamic block dimensions).  The
+ *              backward, and the RMSNorm / LayerNorm forward on rows of one
+ *              warp, stream the next row through a per-thread copy ring in
+ *              shared memory (nf_plan_query reports its bytes).  The only
  *              family for hidden sizes outside the compiled set.
  *   SPLIT   -- one row cut into 8192-element chunks, one CTA per (chunk,
  *              row), the row statistics passed through a caller workspace
