@@ -69,6 +69,36 @@ def test_dynamic_layernorm_fwd(rows, hidden):
     check_f32(rstd, r_ref, f"dyn ln rstd {rows}x{hidden}", rtol=1e-4)
 
 
+@pytest.mark.parametrize("hidden", (24, 264, 1000))
+def test_dynamic_fwd_ring_walks_many_rows(hidden):
+    # rows of one warp run as one wave of 32 resident CTAs per SM that walk
+    # the rows through a two-stage copy ring: with more rows than CTAs each
+    # CTA takes several rows, the stages alternate, and the last rows of the
+    # walk leave empty copy groups behind
+    rows = 10007
+    for op in ("rmsnorm_fwd", "layernorm_fwd"):
+        p = nf.nf_plan_query(op, rows, hidden)
+        assert p["path"] == "dynamic" and p["block"] == 32 and p["smem_bytes"] > 0
+        assert rows > p["grid"] > rows // 4
+    x, w = workloads.rms_inputs(rows, hidden, seed=hidden + 11)
+    y_ref, _ = oracle.rmsnorm_fwd(x, w, 1e-6)
+    y = nf.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6)
+    torch.cuda.synchronize()
+    check_bf16(y, y_ref, f"dyn rms ring {rows}x{hidden}")
+    x, g, b = workloads.layernorm_fwd_inputs(rows, hidden, seed=hidden + 12)
+    y_ref, m_ref, r_ref = oracle.layernorm_fwd(x, g, b, 1e-5)
+    xd = x.cuda()
+    y, mean, rstd = nf.layernorm_fwd(xd, g.cuda(), b.cuda(), 1e-5)
+    torch.cuda.synchronize()
+    check_bf16(y, y_ref, f"dyn ln ring {rows}x{hidden}")
+    check_f32(mean, m_ref, f"dyn ln ring mean {rows}x{hidden}")
+    check_f32(rstd, r_ref, f"dyn ln ring rstd {rows}x{hidden}", rtol=1e-4)
+    # in place: y over x (each row is read, through the ring, before it is written)
+    nf.layernorm_fwd(xd, g.cuda(), b.cuda(), 1e-5, out=xd)
+    torch.cuda.synchronize()
+    assert torch.equal(xd, y)
+
+
 @pytest.mark.parametrize("hidden", BWD_HIDDEN + (1024, 8192))
 @pytest.mark.parametrize("rows", ROWS + (2000,))
 def test_dynamic_layernorm_bwd(rows, hidden):
