@@ -418,8 +418,8 @@ nf_status nf_plan_compute(nf_op op, int64_t rows, int64_t hidden, int32_t sm_cou
         pl.cluster = 1;
         pl.rows_per_cta = 1;
         if (fwd) {
-            // one CTA per row, or on rows of one warp (RMSNorm / LayerNorm)
-            // one wave of resident CTAs with a copy ring each
+            // one CTA per row, or on rows of one warp one wave of resident
+            // CTAs with a copy ring each
             const size_t ring = dyn_fwd_smem(op, hidden);
             const int64_t most = ring ? static_cast<int64_t>(sm_count) * dyn_fwd_per_sm(op, hidden) : kMaxGrid;
             pl.grid = static_cast<int32_t>(rows < most ? rows : most);

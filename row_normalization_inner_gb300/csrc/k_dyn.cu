@@ -85,14 +85,17 @@ __device__ __forceinline__ void cta_sum(float (&v)[N], float* red) {
 // A CTA takes one row at a time with plain loads, the grid as large as the
 // rows, so the hardware keeps as many rows in flight per SM as CTAs fit.
 // Rows of one warp (hidden up to 1024: 32 threads of four vectors) hit the
-// limit of 32 resident CTAs per SM, so the RMSNorm and LayerNorm forward
-// then run RING: one wave of resident CTAs that walk rows blockIdx.x,
-// + gridDim.x, ... and stream each thread's vectors of the row ahead
-// through a per-thread cp.async ring (kDynFwdStages stages of dynamic
-// shared memory, layout [stage][vector][thread]) while the current row is
-// reduced (16384 x 1000: RMSNorm 17.3 -> 14.0 us, LayerNorm 17.3 ->
-// 15.7 us).  For wider rows the ring measured slower than one CTA per row
-// (LayerNorm 16384 x 3072: 43.2 against 34.5 us, with two or three stages).
+// limit of 32 resident CTAs per SM, so the forward ops then run RING (when
+// the row's inputs are at most 2 KB, see dyn_fwd_smem): one wave of resident
+// CTAs that walk rows blockIdx.x, + gridDim.x, ... and
+// stream each thread's vectors of the row ahead (x, and for the fused op
+// the residual) through a per-thread cp.async ring (kDynFwdStages stages
+// of dynamic shared memory, layout [stage][tensor][vector][thread]) while
+// the current row is reduced (16384 x 1000: RMSNorm 17.3 -> 14.0 us,
+// LayerNorm 17.3 -> 15.7 us).  For wider rows the ring measured slower
+// than one CTA per row (LayerNorm 16384 x 3072: 43.2 against 34.5 us, with
+// two or three stages).
+
 // One row of the forward once this thread's vectors are in registers:
 // v0 = x (fused: plus v1 = the residual), c = LayerNorm's shift.
 template <int OP, int MAXV>
@@ -172,7 +175,6 @@ __device__ __forceinline__ void dyn_fwd_row(const DynArgs& a, int64_t row, const
 
 template <int OP, int MAXV, int MAXT, bool RING>
 __global__ void __launch_bounds__(MAXT, 1024 / MAXT) norm_dyn_fwd(DynArgs a) {
-    static_assert(!RING || OP != 0, "the ring carries one input tensor");
     __shared__ float red[kDynMaxWarps * 2];
     grid_dep_wait();
     grid_dep_release();
@@ -197,16 +199,20 @@ __global__ void __launch_bounds__(MAXT, 1024 / MAXT) norm_dyn_fwd(DynArgs a) {
         }
     } else {
         constexpr int S = kDynFwdStages;
-        extern __shared__ __align__(16) uint4 fring[];  // [S][MAXV][T]
+        constexpr int NT = OP == 0 ? 2 : 1;              // x (and the residual)
+        extern __shared__ __align__(16) uint4 fring[];  // [S][NT][MAXV][T]
         const int64_t G = gridDim.x;
-        const auto slot = [&](int st, int k) { return fring + (st * MAXV + k) * T + t; };
+        const auto slot = [&](int st, int tsr, int k) { return fring + ((st * NT + tsr) * MAXV + k) * T + t; };
         // one commit group per row: this thread's vectors (empty past the end)
         const auto issue = [&](int64_t r, int st) {
             if (r < a.rows) {
 #pragma unroll
                 for (int k = 0; k < MAXV; ++k) {
                     const int v = k * T + t;
-                    if (v < NV) dyn_cp16(slot(st, k), a.in0 + r * H + v * kVec);
+                    if (v < NV) {
+                        dyn_cp16(slot(st, 0, k), a.in0 + r * H + v * kVec);
+                        if constexpr (OP == 0) dyn_cp16(slot(st, 1, k), a.in1 + r * H + v * kVec);
+                    }
                 }
             }
             dyn_commit();
@@ -229,8 +235,9 @@ __global__ void __launch_bounds__(MAXT, 1024 / MAXT) norm_dyn_fwd(DynArgs a) {
             uint4 v0[MAXV], v1[MAXV];
 #pragma unroll
             for (int k = 0; k < MAXV; ++k) {
-                v0[k] = k * T + t < NV ? *slot(st, k) : make_uint4(0, 0, 0, 0);
-                v1[k] = make_uint4(0, 0, 0, 0);
+                const bool in = k * T + t < NV;
+                v0[k] = in ? *slot(st, 0, k) : make_uint4(0, 0, 0, 0);
+                v1[k] = OP == 0 && in ? *slot(st, NT - 1, k) : make_uint4(0, 0, 0, 0);
             }
             dyn_fwd_row<OP, MAXV>(a, row, v0, v1, c, red);
         }
@@ -479,13 +486,17 @@ int dyn_bwd_per_sm(int64_t hidden, bool add) {
     return per_sm > 0 ? per_sm : 1;
 }
 
-// Dynamic shared memory of the forward kernel: the copy ring of the
-// RMSNorm and LayerNorm forward on rows of one warp, else 0 (one CTA per
-// row, no ring).
+// Dynamic shared memory of the forward kernel: the copy ring on rows of one
+// warp whose inputs are at most 2 KB (x, and for the fused op the residual:
+// hidden up to 512 there), else 0 (one CTA per row, no ring).  The fused op
+// at 16384 x 264 took 17.0 -> 9.65 us on the ring, at 16384 x 1000
+// 21.4 -> 24.1 us: with 4 KB of inputs per row one CTA per row already
+// keeps enough in flight, and two-tensor rings fit only 24 CTAs per SM.
 size_t dyn_fwd_smem(int op, int64_t hidden) {
     int t;
-    if ((op != 1 && op != 2) || !dyn_shape(op, hidden, &t) || t != 32) return 0;
-    return static_cast<size_t>(kDynFwdStages) * kDynMaxV * t * 16;
+    if (op < 0 || op > 2 || !dyn_shape(op, hidden, &t) || t != 32) return 0;
+    if ((op == 0 ? 2 : 1) * hidden * 2 > 2048) return 0;
+    return static_cast<size_t>(kDynFwdStages) * (op == 0 ? 2 : 1) * kDynMaxV * t * 16;
 }
 
 // Resident CTAs per SM of the forward kernel on the ring: the launch bound
@@ -538,6 +549,7 @@ cudaError_t launch_dyn(int op, const DynArgs& a, int grid, cudaStream_t st) {
     const size_t ring = dyn_fwd_smem(op, a.hidden);  // > 0: one-warp rows on the ring
     switch (op) {
         case 0:
+            if (ring) return launch_with_pdl(norm_dyn_fwd<0, kDynMaxV, 256, true>, g, b, ring, st, a);
             return big ? launch_with_pdl(norm_dyn_fwd<0, kDynMaxV, 1024, false>, g, b, 0, st, a)
                        : launch_with_pdl(norm_dyn_fwd<0, kDynMaxV, 256, false>, g, b, 0, st, a);
         case 1:

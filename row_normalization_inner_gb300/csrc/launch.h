@@ -96,6 +96,7 @@ cudaError_t launch_rms_bwd_rows(int64_t hidden, void* dx, float* ws, const void*
 
 // Runtime-hidden path (any hidden that is a multiple of 8 up to
 // dyn_max_hidden(op)).  op: 0 fused, 1 rms fwd, 2 ln fwd, 3 ln bwd, 4 rms bwd.
+// [kernel-span grid_norm] (the argument block the grid kernels read)
 struct DynArgs {
     uint16_t* out0;          // fused: x; rms/ln fwd: y; bwd: dx
     uint16_t* out1;          // fused: residual
@@ -113,13 +114,14 @@ struct DynArgs {
     int hidden;
     float eps;
 };
+// [end kernel-span grid_norm]
 bool dyn_shape(int op, int64_t hidden, int* threads);
 // Backward: resident CTAs per SM and the copy ring's shared memory; `add`:
 // the ring also carries the fused-add backward's residual-stream gradient.
 int dyn_bwd_per_sm(int64_t hidden, bool add);
 size_t dyn_bwd_smem(int64_t hidden, bool add);
-// Forward: the same for the RMSNorm / LayerNorm forward's copy ring, used
-// for rows of one warp (0 bytes: one CTA per row, no ring).
+// Forward: the same for the forward's copy ring, used for rows of one warp
+// (0 bytes: one CTA per row, no ring).
 int dyn_fwd_per_sm(int op, int64_t hidden);
 size_t dyn_fwd_smem(int op, int64_t hidden);
 int64_t dyn_max_hidden(int op);

@@ -180,12 +180,18 @@ def test_dynamic_plans(hidden):
                 per_sm = max(1, per_sm)
                 assert p["launches"] == 2 and p["partials"] == p["grid"] >= 1
                 assert p["grid"] == min(rows, 152 * per_sm)
-            elif op != "fused_add_rmsnorm" and p["block"] == 32:
-                # rows of one warp: one wave of resident CTAs (32 per SM, the
-                # limit) walking the rows through a two-stage copy ring of
-                # four vectors per thread
-                assert p["launches"] == 1 and p["smem_bytes"] == 2 * 4 * 32 * 16
-                assert p["grid"] == min(rows, 152 * 32)
+            elif p["block"] == 32 and (op != "fused_add_rmsnorm" or hidden <= 512):
+                # rows of one warp with at most 2 KB of inputs: one wave of
+                # resident CTAs walking the rows through a two-stage copy ring
+                # of four vectors per thread (x, and for the fused op the
+                # residual); 32 CTAs per SM (the limit), or as many rings as
+                # fit 228 KB with 1 KB reserved per CTA and the 256-byte
+                # reduction buffer
+                tensors = 2 if op == "fused_add_rmsnorm" else 1
+                ring = 2 * tensors * 4 * 32 * 16
+                assert p["launches"] == 1 and p["smem_bytes"] == ring
+                per_sm = min(32, 228 * 1024 // (ring + 1024 + 256))
+                assert p["grid"] == min(rows, 152 * per_sm)
             else:
                 assert p["launches"] == 1 and p["grid"] == rows and p["smem_bytes"] == 0
         for path in ("reg", "bulk"):

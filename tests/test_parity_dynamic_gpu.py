@@ -76,10 +76,21 @@ def test_dynamic_fwd_ring_walks_many_rows(hidden):
     # CTA takes several rows, the stages alternate, and the last rows of the
     # walk leave empty copy groups behind
     rows = 10007
-    for op in ("rmsnorm_fwd", "layernorm_fwd"):
+    for op in ("rmsnorm_fwd", "layernorm_fwd", "fused_add_rmsnorm"):
         p = nf.nf_plan_query(op, rows, hidden)
-        assert p["path"] == "dynamic" and p["block"] == 32 and p["smem_bytes"] > 0
-        assert rows > p["grid"] > rows // 4
+        assert p["path"] == "dynamic" and p["block"] == 32
+        if op == "fused_add_rmsnorm" and hidden > 512:  # more than 2 KB of inputs a row: no ring
+            assert p["smem_bytes"] == 0 and p["grid"] == rows
+        else:
+            assert p["smem_bytes"] > 0 and rows > p["grid"] > rows // 4
+    x, r, w = workloads.fused_inputs(rows, hidden, seed=hidden + 10, residual_scale=4.0)
+    s_ref, y_ref, _ = oracle.fused_add_rmsnorm(x, r, w, 1e-5)
+    xd, rd = x.cuda(), r.cuda()
+    nf.fused_add_rmsnorm(xd, rd, w.cuda(), 1e-5)  # in place: x becomes y, r the sum
+    torch.cuda.synchronize()
+    check_bf16(xd, y_ref, f"dyn fused ring {rows}x{hidden}")
+    d = ulp_diff_bf16(rd, oracle.to_bf16(s_ref))
+    assert d.max() <= 1 and (d > 0).mean() < 1e-3
     x, w = workloads.rms_inputs(rows, hidden, seed=hidden + 11)
     y_ref, _ = oracle.rmsnorm_fwd(x, w, 1e-6)
     y = nf.rmsnorm_fwd(x.cuda(), w.cuda(), 1e-6)
