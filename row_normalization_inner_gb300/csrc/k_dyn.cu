@@ -61,6 +61,15 @@ template <int N>
 __device__ __forceinline__ void cta_sum(float (&v)[N], float* red) {
     warp_sum<N>(v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (nw == 1) {
+        // one warp: its shuffle totals are the CTA's; 0 + v keeps the bits of
+        // the loop below (a -0 total becomes +0).  Rows of one warp at 16384
+        // rows: 3-9 % faster (LayerNorm forward 264 10.1 -> 9.3 us, RMSNorm
+        // backward 24 12.8 -> 12.0 us)
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = 0.f + v[i];
+        return;
+    }
     if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < N; ++i) red[warp * N + i] = v[i];
